@@ -1,0 +1,135 @@
+"""Seeded synthetic inputs for the MoE layer (shared by the CUDA path's tests,
+the bench and the oracle's tests).
+
+This module holds no arithmetic of the layer: it only draws numbers.  Every
+tensor has its own torch generator seeded from (workload seed, tensor id), so
+a tensor does not change when another one is added or resized.  Normal draws
+are made in float32 and rounded to bf16 (round to nearest even, torch's
+conversion); the same bits then feed both the CUDA library and the oracle.
+
+Distributions:
+  x                 ~ N(0, 1)
+  router_w          ~ N(0, 1/H), or N(0, router_std^2) when given
+  w_gate_up (gate and up rows)   ~ N(0, 1/H)       (fan_in = H)
+  w_down            ~ N(0, 1/I)  with I = n_sub * I_sub, the intermediate size
+                      of the monolithic expert the sub-experts slice (fan_in)
+  shared expert     the same rules with I = I_shared
+  expert bias       N(0, 1) per expert, or -s * ln(rank) with a seeded random
+                    rank permutation (Zipf(s) popularity in logit space)
+  k_per_token       uniform over the workload's choices, drawn per token or per
+                    request (then shared by the request's tokens)
+"""
+from __future__ import annotations
+
+import math
+from typing import Dict, Optional
+
+import torch
+
+from .workloads import Workload
+
+_IDS = {"x": 1, "router_w": 2, "w_gate_up": 3, "w_down": 4, "bias": 5, "k": 6,
+        "w_shared_gate_up": 7, "w_shared_down": 8, "logits": 9}
+
+
+def _gen(seed: int, name: str, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed) * 1000 + _IDS[name])
+    return g
+
+
+def _normal_bf16(shape, std: float, g: torch.Generator, device, chunk_dim0: bool = True):
+    """N(0, std^2) draws rounded to bf16, generated in slabs along dim 0 to
+    bound the float32 temporary."""
+    out = torch.empty(shape, dtype=torch.bfloat16, device=device)
+    if len(shape) >= 3 and chunk_dim0:
+        for i in range(shape[0]):
+            out[i] = (torch.randn(shape[1:], generator=g, device=device,
+                                  dtype=torch.float32) * std).to(torch.bfloat16)
+    else:
+        out.copy_((torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+                   * std).to(torch.bfloat16))
+    return out
+
+
+def draw_k(wl: Workload, device="cpu", seed: Optional[int] = None) -> torch.Tensor:
+    seed = wl.seed if seed is None else seed
+    g = _gen(seed, "k", "cpu")
+    choices = torch.tensor(wl.k_choices, dtype=torch.int32)
+    if wl.k_per == "token":
+        pick = torch.randint(0, len(choices), (wl.T,), generator=g)
+        k = choices[pick]
+    else:
+        n_req = (wl.T + wl.tokens_per_request - 1) // wl.tokens_per_request
+        pick = torch.randint(0, len(choices), (n_req,), generator=g)
+        k = choices[pick].repeat_interleave(wl.tokens_per_request)[: wl.T]
+    return k.to(torch.int32).contiguous().to(device)
+
+
+def draw_bias(wl: Workload, seed: Optional[int] = None) -> Optional[torch.Tensor]:
+    seed = wl.seed if seed is None else seed
+    g = _gen(seed, "bias", "cpu")
+    if wl.bias == "none":
+        return None
+    if wl.bias == "normal":
+        return torch.randn(wl.n_experts, generator=g, dtype=torch.float32)
+    if wl.bias == "zipf":
+        rank = torch.randperm(wl.n_experts, generator=g).to(torch.float64) + 1.0
+        return (-wl.zipf_s * torch.log(rank)).to(torch.float32)
+    raise ValueError(wl.bias)
+
+
+def make_layer_inputs(wl: Workload, device="cpu", seed: Optional[int] = None,
+                      with_weights: bool = True) -> Dict[str, torch.Tensor]:
+    """All inputs of one layer call, on ``device``.
+
+    Keys: x [T,H] bf16, router_w [E_r,H] bf16, expert_bias [n_experts] f32 or
+    None, w_gate_up [E_r, 2*I_sub, H] bf16, w_down [E_r, H, I_sub] bf16,
+    k_per_token [T] int32, and for a shared expert w_shared_gate_up
+    [2*I_shared, H] / w_shared_down [H, I_shared].
+    """
+    seed = wl.seed if seed is None else seed
+    dev = torch.device(device)
+    T, H, E_r, I_sub = wl.T, wl.H, wl.E_r, wl.I_sub
+    d: Dict[str, torch.Tensor] = {}
+    d["x"] = _normal_bf16((T, H), 1.0, _gen(seed, "x", dev), dev)
+    rstd = wl.router_std if wl.router_std is not None else 1.0 / math.sqrt(H)
+    d["router_w"] = _normal_bf16((E_r, H), rstd, _gen(seed, "router_w", dev), dev)
+    b = draw_bias(wl, seed)
+    d["expert_bias"] = None if b is None else b.to(dev)
+    d["k_per_token"] = draw_k(wl, dev, seed)
+    if with_weights:
+        d["w_gate_up"] = _normal_bf16((E_r, 2 * I_sub, H), 1.0 / math.sqrt(H),
+                                      _gen(seed, "w_gate_up", dev), dev)
+        d["w_down"] = _normal_bf16((E_r, H, I_sub), 1.0 / math.sqrt(wl.I),
+                                   _gen(seed, "w_down", dev), dev)
+        if wl.I_shared > 0:
+            d["w_shared_gate_up"] = _normal_bf16((2 * wl.I_shared, H), 1.0 / math.sqrt(H),
+                                                 _gen(seed, "w_shared_gate_up", dev), dev)
+            d["w_shared_down"] = _normal_bf16((H, wl.I_shared), 1.0 / math.sqrt(wl.I_shared),
+                                              _gen(seed, "w_shared_down", dev), dev)
+    return d
+
+
+def make_logits(T: int, E_r: int, device="cpu", seed: int = 7, kind: str = "normal"):
+    """Float32 logits for routing-only tests.
+
+    kind: "normal" N(0,1); "ties" values from a 5-point set so that many ties
+    occur, with -0.0 and +0.0 both present; "flat" every logit equal.
+    """
+    g = _gen(seed, "logits", "cpu")
+    if kind == "normal":
+        L = torch.randn(T, E_r, generator=g, dtype=torch.float32)
+    elif kind == "ties":
+        vals = torch.tensor([-1.5, -0.0, 0.0, 0.25, 2.0], dtype=torch.float32)
+        L = vals[torch.randint(0, len(vals), (T, E_r), generator=g)]
+    elif kind == "flat":
+        L = torch.full((T, E_r), 0.5, dtype=torch.float32)
+    else:
+        raise ValueError(kind)
+    return L.contiguous().to(device)
+
+
+def bf16_bits(t: torch.Tensor):
+    """Host numpy uint16 view of a bf16 tensor's bit patterns (for the oracle)."""
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view("uint16")

@@ -1,0 +1,246 @@
+"""Thin ctypes binding of libmoe.so, one Python function per C entry point.
+
+Argument marshalling only: tensors are passed as device pointers, streams as
+cudaStream_t handles.  Every step of the layer runs in the CUDA library; if
+the library is missing or fails to load, every call raises.  The functions
+return the moe_status code (an int) and never synchronise, except
+``moe_get_device_status``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe.so")
+
+MOE_OK = 0
+STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARGUMENT", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
+                3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_TIMEOUT",
+                6: "MOE_ERR_NONFINITE", 7: "MOE_ERR_K_RANGE", 8: "MOE_ERR_BAD_INDEX"}
+SCORE = {"softmax": 0, "sigmoid": 1}
+DEBUG_SKIP_FIRST_LOAD = 1
+
+EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_gate_up", "moe_down",
+           "moe_grouped_ffn", "moe_shared_ffn", "moe_combine", "moe_layer_forward",
+           "moe_get_device_status", "moe_status_string")
+
+
+class MoeLayerDesc(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32), ("n_experts", ctypes.c_int32),
+                ("n_sub", ctypes.c_int32), ("I_sub", ctypes.c_int32), ("k_max", ctypes.c_int32),
+                ("score", ctypes.c_int), ("renorm", ctypes.c_int32),
+                ("route_scale", ctypes.c_float), ("expert_bias", ctypes.c_void_p),
+                ("I_shared", ctypes.c_int32), ("w_shared_gate_up", ctypes.c_void_p),
+                ("w_shared_down", ctypes.c_void_p), ("path", ctypes.c_int),
+                ("debug_flags", ctypes.c_uint32)]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {STATUS_NAMES.get(code, code)}")
+        self.code = code
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmoe.so (raises if it is not built: there is no fallback)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libmoe.so is not built ({LIB_PATH}); run "
+                               "`python -m aware_moe_expert_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32p = ctypes.c_void_p, ctypes.c_void_p
+        D = ctypes.POINTER(MoeLayerDesc)
+        sig = {
+            "moe_workspace_size": (ctypes.c_size_t, [D]),
+            "moe_route": (ctypes.c_int, [D, vp, vp, vp, i32p, vp, i32p, vp, i32p, vp, vp]),
+            "moe_permute": (ctypes.c_int, [D, i32p, i32p, i32p, i32p, i32p, i32p, i32p, vp, vp]),
+            "moe_gate_up": (ctypes.c_int, [D, vp, i32p, i32p, vp, vp, i32p, vp, vp]),
+            "moe_down": (ctypes.c_int, [D, vp, i32p, vp, vp, i32p, vp, vp]),
+            "moe_grouped_ffn": (ctypes.c_int, [D, vp, i32p, i32p, vp, vp, vp, i32p, vp, vp]),
+            "moe_shared_ffn": (ctypes.c_int, [D, vp, vp, i32p, vp, vp]),
+            "moe_combine": (ctypes.c_int, [D, vp, vp, i32p, vp, i32p, vp, i32p, vp]),
+            "moe_layer_forward": (ctypes.c_int, [D, vp, vp, vp, vp, i32p, vp, i32p, vp, vp]),
+            "moe_get_device_status": (ctypes.c_int, [i32p, vp]),
+            "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+@dataclass
+class LayerDesc:
+    """Python mirror of moe_layer_desc; tensors kept alive by reference."""
+    T: int
+    H: int
+    n_experts: int
+    n_sub: int
+    I_sub: int
+    k_max: int
+    score: str = "softmax"
+    renorm: bool = False
+    route_scale: float = 1.0
+    expert_bias: Optional[torch.Tensor] = None
+    I_shared: int = 0
+    w_shared_gate_up: Optional[torch.Tensor] = None
+    w_shared_down: Optional[torch.Tensor] = None
+    debug_flags: int = 0
+
+    @property
+    def E_r(self) -> int:
+        return self.n_experts * self.n_sub
+
+    def c(self) -> MoeLayerDesc:
+        d = MoeLayerDesc()
+        d.T, d.H, d.n_experts, d.n_sub = self.T, self.H, self.n_experts, self.n_sub
+        d.I_sub, d.k_max = self.I_sub, self.k_max
+        d.score = SCORE[self.score]
+        d.renorm = int(bool(self.renorm))
+        d.route_scale = float(self.route_scale)
+        d.expert_bias = _ptr(self.expert_bias)
+        d.I_shared = self.I_shared
+        d.w_shared_gate_up = _ptr(self.w_shared_gate_up)
+        d.w_shared_down = _ptr(self.w_shared_down)
+        d.path = 0
+        d.debug_flags = int(self.debug_flags)
+        return d
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def desc_for(wl, T=None, expert_bias=None, w_shared_gate_up=None, w_shared_down=None,
+             debug_flags=0) -> LayerDesc:
+    """LayerDesc for a workload definition (aware_moe_expert_gb300.workloads)."""
+    return LayerDesc(T=wl.T if T is None else T, H=wl.H, n_experts=wl.n_experts, n_sub=wl.n_sub,
+                     I_sub=wl.I_sub, k_max=wl.k_max, score=wl.score, renorm=wl.renorm,
+                     route_scale=wl.route_scale, expert_bias=expert_bias, I_shared=wl.I_shared,
+                     w_shared_gate_up=w_shared_gate_up, w_shared_down=w_shared_down,
+                     debug_flags=debug_flags)
+
+
+def moe_workspace_size(desc: LayerDesc) -> int:
+    d = desc.c()
+    return int(lib().moe_workspace_size(ctypes.byref(d)))
+
+
+def moe_route(desc, x, router_w, logits_in, k_per_token, logits_out, topk_idx, topk_w,
+              dev_status, workspace, stream=None) -> int:
+    d = desc.c()
+    return lib().moe_route(ctypes.byref(d), _ptr(x), _ptr(router_w), _ptr(logits_in),
+                           _ptr(k_per_token), _ptr(logits_out), _ptr(topk_idx), _ptr(topk_w),
+                           _ptr(dev_status), _ptr(workspace), _stream(stream))
+
+
+def moe_permute(desc, topk_idx, k_per_token, counts, offsets, sorted_token, inv_row, dev_status,
+                workspace, stream=None) -> int:
+    d = desc.c()
+    return lib().moe_permute(ctypes.byref(d), _ptr(topk_idx), _ptr(k_per_token), _ptr(counts),
+                             _ptr(offsets), _ptr(sorted_token), _ptr(inv_row), _ptr(dev_status),
+                             _ptr(workspace), _stream(stream))
+
+
+def moe_gate_up(desc, x, sorted_token, offsets, w_gate_up, act, dev_status, workspace,
+                stream=None) -> int:
+    d = desc.c()
+    return lib().moe_gate_up(ctypes.byref(d), _ptr(x), _ptr(sorted_token), _ptr(offsets),
+                             _ptr(w_gate_up), _ptr(act), _ptr(dev_status), _ptr(workspace),
+                             _stream(stream))
+
+
+def moe_down(desc, act, offsets, w_down, y_perm, dev_status, workspace, stream=None) -> int:
+    d = desc.c()
+    return lib().moe_down(ctypes.byref(d), _ptr(act), _ptr(offsets), _ptr(w_down), _ptr(y_perm),
+                          _ptr(dev_status), _ptr(workspace), _stream(stream))
+
+
+def moe_grouped_ffn(desc, x, sorted_token, offsets, w_gate_up, w_down, y_perm, dev_status,
+                    workspace, stream=None) -> int:
+    d = desc.c()
+    return lib().moe_grouped_ffn(ctypes.byref(d), _ptr(x), _ptr(sorted_token), _ptr(offsets),
+                                 _ptr(w_gate_up), _ptr(w_down), _ptr(y_perm), _ptr(dev_status),
+                                 _ptr(workspace), _stream(stream))
+
+
+def moe_shared_ffn(desc, x, y_shared, dev_status, workspace, stream=None) -> int:
+    d = desc.c()
+    return lib().moe_shared_ffn(ctypes.byref(d), _ptr(x), _ptr(y_shared), _ptr(dev_status),
+                                _ptr(workspace), _stream(stream))
+
+
+def moe_combine(desc, y_perm, y_shared, inv_row, topk_w, k_per_token, out, dev_status,
+                stream=None) -> int:
+    d = desc.c()
+    return lib().moe_combine(ctypes.byref(d), _ptr(y_perm), _ptr(y_shared), _ptr(inv_row),
+                             _ptr(topk_w), _ptr(k_per_token), _ptr(out), _ptr(dev_status),
+                             _stream(stream))
+
+
+def moe_layer_forward(desc, x, router_w, w_gate_up, w_down, k_per_token, out, dev_status,
+                      workspace, stream=None) -> int:
+    d = desc.c()
+    return lib().moe_layer_forward(ctypes.byref(d), _ptr(x), _ptr(router_w), _ptr(w_gate_up),
+                                   _ptr(w_down), _ptr(k_per_token), _ptr(out), _ptr(dev_status),
+                                   _ptr(workspace), _stream(stream))
+
+
+def moe_get_device_status(dev_status, stream=None) -> int:
+    return lib().moe_get_device_status(_ptr(dev_status), _stream(stream))
+
+
+def moe_status_string(code: int) -> str:
+    return lib().moe_status_string(int(code)).decode()
+
+
+def check(code: int, where: str = "moe") -> None:
+    if code != MOE_OK:
+        raise MoeError(code, where)
+
+
+class MoeLayer:
+    """Convenience owner of the workspace and status word for one layer shape
+    on one device; every call goes straight to the C ABI."""
+
+    def __init__(self, desc: LayerDesc, device="cuda"):
+        self.desc = desc
+        self.device = torch.device(device)
+        n = moe_workspace_size(desc)
+        if n == 0:
+            raise MoeError(2, "moe_workspace_size")
+        self.workspace = torch.empty(n, dtype=torch.uint8, device=self.device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+
+    def forward(self, x, router_w, w_gate_up, w_down, k_per_token, out=None, stream=None):
+        if out is None:
+            out = torch.empty(self.desc.T, self.desc.H, dtype=torch.bfloat16, device=self.device)
+        check(moe_layer_forward(self.desc, x, router_w, w_gate_up, w_down, k_per_token, out,
+                                self.status, self.workspace, stream), "moe_layer_forward")
+        return out
+
+    def device_status(self, stream=None) -> int:
+        return moe_get_device_status(self.status, stream)

@@ -1,0 +1,443 @@
+// C ABI of libmoe.so (declared in include/moe.h): argument validation,
+// workspace carving and launch sequencing on the caller's stream.  No call
+// here allocates, frees or synchronises, except moe_get_device_status.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/moe.h"
+#include "moe_internal.h"
+
+namespace {
+
+using moe::GemmArgs;
+
+constexpr size_t kAlign = 256;
+constexpr int kMaxDevices = 64;
+
+inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Byte offsets of every workspace region for one desc.
+struct Layout {
+  size_t logits, topk_idx, topk_w, counts, offsets, sorted_token, inv_row, bitmap, wprefix, xperm,
+      act, yperm, act_sh, ysh, total;
+};
+
+Layout layout_of(const moe_layer_desc& d) {
+  const size_t T = static_cast<size_t>(d.T), E_r = static_cast<size_t>(d.n_experts) * d.n_sub;
+  const size_t n_cap = T * d.k_max, W = (T + 31) / 32;
+  Layout l;
+  size_t o = 0;
+  auto take = [&o](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes);
+    return at;
+  };
+  l.logits = take(T * E_r * 4);
+  l.topk_idx = take(n_cap * 4);
+  l.topk_w = take(n_cap * 4);
+  l.counts = take(E_r * 4);
+  l.offsets = take((E_r + 1) * 4);
+  l.sorted_token = take(n_cap * 4);
+  l.inv_row = take(n_cap * 4);
+  l.bitmap = take(E_r * W * 4);
+  l.wprefix = take(E_r * W * 4);
+  l.xperm = take(n_cap * d.H * 2);
+  l.act = take(n_cap * d.I_sub * 2);
+  l.yperm = take(n_cap * d.H * 2);
+  l.act_sh = take(T * static_cast<size_t>(d.I_shared) * 2);
+  l.ysh = take(T * static_cast<size_t>(d.H) * 2);
+  l.total = o;
+  return l;
+}
+
+template <typename P>
+inline P* at(void* ws, size_t off) {
+  return reinterpret_cast<P*>(static_cast<char*>(ws) + off);
+}
+
+moe_status validate(const moe_layer_desc* d) {
+  if (d == nullptr) return MOE_ERR_INVALID_ARGUMENT;
+  if (d->T < 0 || d->H <= 0 || d->n_experts <= 0 || d->n_sub <= 0 || d->I_sub <= 0 ||
+      d->k_max <= 0 || d->I_shared < 0)
+    return MOE_ERR_INVALID_ARGUMENT;
+  if (d->score != MOE_SCORE_SOFTMAX && d->score != MOE_SCORE_SIGMOID)
+    return MOE_ERR_INVALID_ARGUMENT;
+  const long long E_r = static_cast<long long>(d->n_experts) * d->n_sub;
+  if (d->H % 64 != 0 || d->I_sub % 64 != 0 || d->I_shared % 64 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (E_r > 256 || d->k_max > E_r || d->k_max > 32) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (static_cast<long long>(d->T) * d->k_max > (1ll << 30)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (d->I_shared > 0 && (d->w_shared_gate_up == nullptr || d->w_shared_down == nullptr))
+    return MOE_ERR_INVALID_ARGUMENT;
+  if (d->I_shared > 0 && (!aligned16(d->w_shared_gate_up) || !aligned16(d->w_shared_down)))
+    return MOE_ERR_INVALID_ARGUMENT;
+  return MOE_OK;
+}
+
+moe_status check_ptrs(std::initializer_list<const void*> ptrs) {
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return MOE_ERR_INVALID_ARGUMENT;
+  return MOE_OK;
+}
+
+// int32 / fp32 arrays only need 4-byte alignment
+moe_status check_ptrs4(std::initializer_list<const void*> ptrs) {
+  for (const void* p : ptrs)
+    if (p == nullptr || (reinterpret_cast<uintptr_t>(p) & 3u) != 0) return MOE_ERR_INVALID_ARGUMENT;
+  return MOE_OK;
+}
+
+moe_status check_ws(const void* ws) {
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0)
+    return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+int sm_count() {
+  static int cache[kMaxDevices] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+      cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+inline moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY(expr)                      \
+  do {                                     \
+    const moe_status _st = (expr);         \
+    if (_st != MOE_OK) return _st;         \
+  } while (0)
+
+inline int E_r_of(const moe_layer_desc* d) { return d->n_experts * d->n_sub; }
+
+// ---- the steps, without argument checks (callers check)
+
+moe_status do_route(const moe_layer_desc* d, const void* x, const void* router_w,
+                    const float* logits_in, const int32_t* kpt, float* logits_out,
+                    int32_t* topk_idx, float* topk_w, int32_t* status, void* ws,
+                    cudaStream_t s) {
+  const int E_r = E_r_of(d);
+  const float* L = logits_in;
+  if (L == nullptr) {
+    float* dst = logits_out != nullptr ? logits_out : at<float>(ws, layout_of(*d).logits);
+    if (d->T >= 128 && moe::gemm_supports_f32_router(E_r)) {
+      GemmArgs g{};
+      g.epi = moe::EPI_F32;
+      g.a = x;
+      g.a_rows = d->T;
+      g.b = router_w;
+      g.b_rows = E_r;
+      g.K = d->H;
+      g.offsets = nullptr;
+      g.n_groups = 1;
+      g.dense_rows = d->T;
+      g.n_out = E_r;
+      g.b_group_rows = 0;
+      g.out = dst;
+      g.ld_out = E_r;
+      g.out_rows = d->T;
+      g.bias = d->expert_bias;
+      g.bias_div = d->n_sub;
+      g.status = status;
+      g.debug_flags = 0;
+      g.sm_count = sm_count();
+      g.max_rows_hint = d->T;
+      MOE_TRY(cuda_status(moe::launch_gemm(g, s)));
+    } else {
+      MOE_TRY(cuda_status(moe::launch_router_logits_small(x, router_w, d->expert_bias, d->T,
+                                                          d->H, E_r, d->n_sub, dst, s)));
+    }
+    L = dst;
+  }
+  return cuda_status(moe::launch_topk_gate(L, kpt, d->T, E_r, d->k_max, d->score, d->renorm,
+                                           d->route_scale, topk_idx, topk_w, status, s));
+}
+
+moe_status do_permute(const moe_layer_desc* d, const int32_t* topk_idx, const int32_t* kpt,
+                      int32_t* counts, int32_t* offsets, int32_t* sorted_token,
+                      int32_t* inv_row, int32_t* status, void* ws, cudaStream_t s) {
+  const Layout l = layout_of(*d);
+  return cuda_status(moe::launch_permute(topk_idx, kpt, d->T, d->k_max, E_r_of(d),
+                                         at<uint32_t>(ws, l.bitmap), at<int32_t>(ws, l.wprefix),
+                                         counts, offsets, sorted_token, inv_row, status, s));
+}
+
+moe_status do_gate_up(const moe_layer_desc* d, const void* x, const int32_t* sorted_token,
+                      const int32_t* offsets, const void* w_gate_up, void* act, int32_t* status,
+                      void* ws, cudaStream_t s) {
+  const Layout l = layout_of(*d);
+  const int E_r = E_r_of(d);
+  const long long n_cap = static_cast<long long>(d->T) * d->k_max;
+  if (n_cap == 0) return MOE_OK;
+  void* xperm = at<void>(ws, l.xperm);
+  MOE_TRY(cuda_status(moe::launch_gather_rows(x, sorted_token, offsets, E_r, d->T, d->H,
+                                              static_cast<int>(n_cap), xperm, status,
+                                              sm_count(), s)));
+  GemmArgs g{};
+  g.epi = moe::EPI_SWIGLU;
+  g.a = xperm;
+  g.a_rows = n_cap;
+  g.b = w_gate_up;
+  g.b_rows = static_cast<long long>(E_r) * 2 * d->I_sub;
+  g.K = d->H;
+  g.offsets = offsets;
+  g.n_groups = E_r;
+  g.n_out = d->I_sub;
+  g.b_group_rows = 2 * d->I_sub;
+  g.out = act;
+  g.ld_out = d->I_sub;
+  g.out_rows = n_cap;
+  g.status = status;
+  g.debug_flags = d->debug_flags;
+  g.sm_count = sm_count();
+  g.max_rows_hint = static_cast<int>(n_cap);
+  return cuda_status(moe::launch_gemm(g, s));
+}
+
+moe_status do_down(const moe_layer_desc* d, const void* act, const int32_t* offsets,
+                   const void* w_down, void* y_perm, int32_t* status, cudaStream_t s) {
+  const int E_r = E_r_of(d);
+  const long long n_cap = static_cast<long long>(d->T) * d->k_max;
+  if (n_cap == 0) return MOE_OK;
+  GemmArgs g{};
+  g.epi = moe::EPI_BF16;
+  g.a = act;
+  g.a_rows = n_cap;
+  g.b = w_down;
+  g.b_rows = static_cast<long long>(E_r) * d->H;
+  g.K = d->I_sub;
+  g.offsets = offsets;
+  g.n_groups = E_r;
+  g.n_out = d->H;
+  g.b_group_rows = d->H;
+  g.out = y_perm;
+  g.ld_out = d->H;
+  g.out_rows = n_cap;
+  g.status = status;
+  g.debug_flags = 0;
+  g.sm_count = sm_count();
+  g.max_rows_hint = static_cast<int>(n_cap);
+  return cuda_status(moe::launch_gemm(g, s));
+}
+
+moe_status do_shared(const moe_layer_desc* d, const void* x, void* y_shared, int32_t* status,
+                     void* ws, cudaStream_t s) {
+  if (d->T == 0) return MOE_OK;
+  const Layout l = layout_of(*d);
+  void* act = at<void>(ws, l.act_sh);
+  GemmArgs g{};
+  g.epi = moe::EPI_SWIGLU;
+  g.a = x;
+  g.a_rows = d->T;
+  g.b = d->w_shared_gate_up;
+  g.b_rows = 2ll * d->I_shared;
+  g.K = d->H;
+  g.offsets = nullptr;
+  g.n_groups = 1;
+  g.dense_rows = d->T;
+  g.n_out = d->I_shared;
+  g.b_group_rows = 2 * d->I_shared;
+  g.out = act;
+  g.ld_out = d->I_shared;
+  g.out_rows = d->T;
+  g.status = status;
+  g.sm_count = sm_count();
+  g.max_rows_hint = d->T;
+  MOE_TRY(cuda_status(moe::launch_gemm(g, s)));
+  GemmArgs h{};
+  h.epi = moe::EPI_BF16;
+  h.a = act;
+  h.a_rows = d->T;
+  h.b = d->w_shared_down;
+  h.b_rows = d->H;
+  h.K = d->I_shared;
+  h.offsets = nullptr;
+  h.n_groups = 1;
+  h.dense_rows = d->T;
+  h.n_out = d->H;
+  h.b_group_rows = d->H;
+  h.out = y_shared;
+  h.ld_out = d->H;
+  h.out_rows = d->T;
+  h.status = status;
+  h.sm_count = sm_count();
+  h.max_rows_hint = d->T;
+  return cuda_status(moe::launch_gemm(h, s));
+}
+
+moe_status do_combine(const moe_layer_desc* d, const void* y_perm, const void* y_shared,
+                      const int32_t* inv_row, const float* topk_w, const int32_t* kpt, void* out,
+                      int32_t* status, cudaStream_t s) {
+  const long long n_cap = static_cast<long long>(d->T) * d->k_max;
+  return cuda_status(moe::launch_combine(y_perm, y_shared, inv_row, topk_w, kpt, d->T, d->H,
+                                         d->k_max, static_cast<int>(n_cap), out, status, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_workspace_size(const moe_layer_desc* desc) {
+  if (validate(desc) != MOE_OK) return 0;
+  return layout_of(*desc).total;
+}
+
+moe_status moe_route(const moe_layer_desc* desc, const void* x, const void* router_w,
+                     const float* logits_in, const int32_t* k_per_token, float* logits_out,
+                     int32_t* topk_idx, float* topk_w, int32_t* dev_status, void* workspace,
+                     void* stream) {
+  MOE_TRY(validate(desc));
+  if (desc->T == 0) return MOE_OK;
+  MOE_TRY(check_ptrs4({k_per_token, topk_idx, topk_w, dev_status}));
+  if (logits_in != nullptr) {
+    MOE_TRY(check_ptrs4({logits_in}));
+  } else {
+    MOE_TRY(check_ptrs({x, router_w}));
+    if (logits_out != nullptr) {
+      MOE_TRY(check_ptrs({logits_out}));
+    } else {
+      MOE_TRY(check_ws(workspace));
+    }
+  }
+  return do_route(desc, x, router_w, logits_in, k_per_token, logits_out, topk_idx, topk_w,
+                  dev_status, workspace, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_permute(const moe_layer_desc* desc, const int32_t* topk_idx,
+                       const int32_t* k_per_token, int32_t* counts, int32_t* offsets,
+                       int32_t* sorted_token, int32_t* inv_row, int32_t* dev_status,
+                       void* workspace, void* stream) {
+  MOE_TRY(validate(desc));
+  MOE_TRY(check_ptrs4({counts, offsets, dev_status}));
+  if (desc->T > 0) MOE_TRY(check_ptrs4({topk_idx, k_per_token, sorted_token, inv_row}));
+  MOE_TRY(check_ws(workspace));
+  return do_permute(desc, topk_idx, k_per_token, counts, offsets, sorted_token, inv_row,
+                    dev_status, workspace, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_gate_up(const moe_layer_desc* desc, const void* x, const int32_t* sorted_token,
+                       const int32_t* offsets, const void* w_gate_up, void* act,
+                       int32_t* dev_status, void* workspace, void* stream) {
+  MOE_TRY(validate(desc));
+  if (desc->T == 0) return MOE_OK;
+  MOE_TRY(check_ptrs({x, w_gate_up, act}));
+  MOE_TRY(check_ptrs4({sorted_token, offsets, dev_status}));
+  MOE_TRY(check_ws(workspace));
+  return do_gate_up(desc, x, sorted_token, offsets, w_gate_up, act, dev_status, workspace,
+                    static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_down(const moe_layer_desc* desc, const void* act, const int32_t* offsets,
+                    const void* w_down, void* y_perm, int32_t* dev_status, void* workspace,
+                    void* stream) {
+  (void)workspace;
+  MOE_TRY(validate(desc));
+  if (desc->T == 0) return MOE_OK;
+  MOE_TRY(check_ptrs({act, w_down, y_perm}));
+  MOE_TRY(check_ptrs4({offsets, dev_status}));
+  return do_down(desc, act, offsets, w_down, y_perm, dev_status,
+                 static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_grouped_ffn(const moe_layer_desc* desc, const void* x,
+                           const int32_t* sorted_token, const int32_t* offsets,
+                           const void* w_gate_up, const void* w_down, void* y_perm,
+                           int32_t* dev_status, void* workspace, void* stream) {
+  MOE_TRY(validate(desc));
+  if (desc->T == 0) return MOE_OK;
+  MOE_TRY(check_ptrs({x, w_gate_up, w_down, y_perm}));
+  MOE_TRY(check_ptrs4({sorted_token, offsets, dev_status}));
+  MOE_TRY(check_ws(workspace));
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* act = at<void>(workspace, layout_of(*desc).act);
+  MOE_TRY(do_gate_up(desc, x, sorted_token, offsets, w_gate_up, act, dev_status, workspace, s));
+  return do_down(desc, act, offsets, w_down, y_perm, dev_status, s);
+}
+
+moe_status moe_shared_ffn(const moe_layer_desc* desc, const void* x, void* y_shared,
+                          int32_t* dev_status, void* workspace, void* stream) {
+  MOE_TRY(validate(desc));
+  if (desc->I_shared <= 0) return MOE_ERR_INVALID_ARGUMENT;
+  if (desc->T == 0) return MOE_OK;
+  MOE_TRY(check_ptrs({x, y_shared}));
+  MOE_TRY(check_ptrs4({dev_status}));
+  MOE_TRY(check_ws(workspace));
+  return do_shared(desc, x, y_shared, dev_status, workspace, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_combine(const moe_layer_desc* desc, const void* y_perm, const void* y_shared,
+                       const int32_t* inv_row, const float* topk_w, const int32_t* k_per_token,
+                       void* out, int32_t* dev_status, void* stream) {
+  MOE_TRY(validate(desc));
+  if (desc->T == 0) return MOE_OK;
+  MOE_TRY(check_ptrs({y_perm, out}));
+  if (y_shared != nullptr) MOE_TRY(check_ptrs({y_shared}));
+  MOE_TRY(check_ptrs4({inv_row, topk_w, k_per_token, dev_status}));
+  return do_combine(desc, y_perm, y_shared, inv_row, topk_w, k_per_token, out, dev_status,
+                    static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, const void* router_w,
+                             const void* w_gate_up, const void* w_down,
+                             const int32_t* k_per_token, void* out, int32_t* dev_status,
+                             void* workspace, void* stream) {
+  MOE_TRY(validate(desc));
+  if (desc->T == 0) return MOE_OK;
+  MOE_TRY(check_ptrs({x, router_w, w_gate_up, w_down, out}));
+  MOE_TRY(check_ptrs4({k_per_token, dev_status}));
+  MOE_TRY(check_ws(workspace));
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Layout l = layout_of(*desc);
+  int32_t* topk_idx = at<int32_t>(workspace, l.topk_idx);
+  float* topk_w = at<float>(workspace, l.topk_w);
+  int32_t* counts = at<int32_t>(workspace, l.counts);
+  int32_t* offsets = at<int32_t>(workspace, l.offsets);
+  int32_t* sorted_token = at<int32_t>(workspace, l.sorted_token);
+  int32_t* inv_row = at<int32_t>(workspace, l.inv_row);
+  void* act = at<void>(workspace, l.act);
+  void* yperm = at<void>(workspace, l.yperm);
+  void* ysh = desc->I_shared > 0 ? at<void>(workspace, l.ysh) : nullptr;
+  MOE_TRY(do_route(desc, x, router_w, nullptr, k_per_token, nullptr, topk_idx, topk_w,
+                   dev_status, workspace, s));
+  MOE_TRY(do_permute(desc, topk_idx, k_per_token, counts, offsets, sorted_token, inv_row,
+                     dev_status, workspace, s));
+  if (ysh != nullptr) MOE_TRY(do_shared(desc, x, ysh, dev_status, workspace, s));
+  MOE_TRY(do_gate_up(desc, x, sorted_token, offsets, w_gate_up, act, dev_status, workspace, s));
+  MOE_TRY(do_down(desc, act, offsets, w_down, yperm, dev_status, s));
+  return do_combine(desc, yperm, ysh, inv_row, topk_w, k_per_token, out, dev_status, s);
+}
+
+moe_status moe_get_device_status(const int32_t* dev_status, void* stream) {
+  if (dev_status == nullptr) return MOE_ERR_INVALID_ARGUMENT;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, dev_status, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  return static_cast<moe_status>(v);
+}
+
+const char* moe_status_string(moe_status st) {
+  switch (st) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARGUMENT: return "MOE_ERR_INVALID_ARGUMENT";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "MOE_ERR_UNSUPPORTED_SHAPE";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT";
+    case MOE_ERR_NONFINITE: return "MOE_ERR_NONFINITE";
+    case MOE_ERR_K_RANGE: return "MOE_ERR_K_RANGE";
+    case MOE_ERR_BAD_INDEX: return "MOE_ERR_BAD_INDEX";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+}  // extern "C"

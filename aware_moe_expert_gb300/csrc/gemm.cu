@@ -1,0 +1,512 @@
+// Grouped GEMM on the 5th-generation tensor cores (tcgen05 + TMEM), fed by
+// TMA, for the expert FFN of the k-aware MoE layer.
+//
+//   D[r, n] = sum_k A[r, k] * B[b_row(g, n), k]      r in the rows of group g
+//
+// Groups are routing units (rows of unit u are offsets[u] .. offsets[u+1]),
+// or one dense group (router logits, shared expert).  Three epilogues:
+//   EPI_SWIGLU  the B tile is a gate slab and the matching up slab of one
+//               sub-expert; act = SiLU(gate) * up, stored bf16
+//               (MoE-Prism, arXiv 2510.19366, §III-B1 Eq. (1))
+//   EPI_BF16    plain bf16 store (down projection, X' = A Wdown)
+//   EPI_F32     fp32 store plus a per-expert bias (router logits, §III-B2)
+//
+// Structure: persistent CTAs (one per SM), 6 warps.
+//   warp 0      TMA producer: one elected thread streams A and B k-blocks
+//               (64 bf16 = 128 B wide, 128-byte swizzle) into a STAGES-deep
+//               shared-memory ring, completion counted on `full` mbarriers
+//   warp 1      allocates TMEM; one elected thread issues tcgen05.mma
+//               (M = 128, N = BN_MMA, K = 16) into one of two fp32 TMEM
+//               accumulators, and commits to `empty` (ring slot free) and
+//               `tfull` (accumulator ready) mbarriers
+//   warps 2..5  epilogue: tcgen05.ld of their 32-lane TMEM quadrant (one
+//               output row per thread), math, 16-byte global stores; then
+//               release the accumulator on `tempty`
+// Work items are (m-tile, n-tile) pairs, m-tile major, handed out
+// round-robin; the m-tile -> (unit, first row) map is rebuilt in shared
+// memory from `offsets` at kernel start, so no host sync is needed.
+// Every wait is bounded (MOE_ERR_DEVICE_TIMEOUT), loads in flight are
+// drained and TMEM is freed before the CTA exits.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int kThreads = 192;
+constexpr uint32_t kABytes = BM * BK * 2;
+constexpr int kMaxGroups = 256;
+
+struct KParams {
+  const int32_t* offsets;
+  int n_groups;
+  int dense_rows;
+  int K;
+  int n_tiles;       // n-tiles per group
+  int bn_out;        // output columns per n-tile
+  int b_group_rows;  // rows of B per group
+  int b_up_offset;   // SWIGLU: rows between a gate row and its up row
+  void* out;
+  long long ld_out;
+  long long out_rows;
+  int out_cols;      // EPI_F32: valid output columns
+  const float* bias;
+  int bias_div;
+  int32_t* status;
+  uint32_t debug_flags;
+};
+
+template <int BN_MMA, int STAGES>
+struct Cfg {
+  static constexpr uint32_t kBBytes = BN_MMA * BK * 2;
+  static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  static constexpr uint32_t kTmemCols = (2 * BN_MMA <= 32)    ? 32
+                                        : (2 * BN_MMA <= 64)  ? 64
+                                        : (2 * BN_MMA <= 128) ? 128
+                                        : (2 * BN_MMA <= 256) ? 256
+                                                              : 512;
+  static constexpr uint32_t kOffA = 0;
+  static constexpr uint32_t kOffB = STAGES * kABytes;
+  static constexpr uint32_t kOffBar = STAGES * kStageBytes;
+  static constexpr uint32_t kNumBars = 2 * STAGES + 5;
+  static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr uint32_t kOffPrefix = kOffMisc + 16;
+  static constexpr uint32_t kOffOffs = kOffPrefix + (kMaxGroups + 1) * 4;
+  static constexpr uint32_t kSmemUsed = kOffOffs + (kMaxGroups + 1) * 4;
+  static constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // 1024-B alignment slack
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  static_assert(BN_MMA % 16 == 0 && BN_MMA >= 16 && BN_MMA <= 256, "tcgen05 N for M = 128");
+};
+
+struct Tile {
+  int g, row0, rows, nt;
+};
+
+__device__ __forceinline__ Tile decode_tile(int w, int n_tiles, int n_groups, const int* prefix,
+                                            const int* offs) {
+  Tile t;
+  const int mt = w / n_tiles;
+  t.nt = w - mt * n_tiles;
+  // largest g in [0, n_groups) with prefix[g] <= mt
+  int lo = 0, hi = n_groups;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (prefix[mid] <= mt)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  t.g = lo;
+  t.row0 = offs[lo] + (mt - prefix[lo]) * BM;
+  t.rows = min(BM, offs[lo + 1] - t.row0);
+  return t;
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
+__device__ __forceinline__ void fail(volatile int* abort, int32_t* status) {
+  *abort = 1;
+  report(status, MOE_ERR_DEVICE_TIMEOUT);
+}
+
+template <int BN_MMA, int EPI, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, const KParams p) {
+  using C = Cfg<BN_MMA, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* tfull = bars + 2 * STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* done = tempty + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+  int* s_total = reinterpret_cast<int*>(smem + C::kOffMisc + 8);
+  int* s_prefix = reinterpret_cast<int*>(smem + C::kOffPrefix);
+  int* s_offs = reinterpret_cast<int*>(smem + C::kOffOffs);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&tfull[0], 1);
+    mbar_init(&tfull[1], 1);
+    mbar_init(&tempty[0], 4);
+    mbar_init(&tempty[1], 4);
+    mbar_init(done, 1);
+    *s_abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 2) {
+    // m-tile table: s_prefix[g] = first m-tile of group g, s_offs = row offsets
+    if (p.offsets == nullptr) {
+      if (lane == 0) {
+        s_offs[0] = 0;
+        s_offs[1] = p.dense_rows;
+        s_prefix[0] = 0;
+        s_prefix[1] = (p.dense_rows + BM - 1) / BM;
+        *s_total = s_prefix[1];
+      }
+    } else {
+      const int G = p.n_groups;
+      const int per = (G + 31) / 32;
+      const int g0 = lane * per;
+      int local = 0;
+      bool bad = false;
+      for (int i = 0; i < per; ++i) {
+        const int g = g0 + i;
+        if (g < G) {
+          const int a = p.offsets[g], b = p.offsets[g + 1];
+          bad |= (a < 0) || (b < a);
+          s_offs[g] = a;
+          local += b > a ? (b - a + BM - 1) / BM : 0;
+        }
+      }
+      int incl = local;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      int run = incl - local;
+      for (int i = 0; i < per; ++i) {
+        const int g = g0 + i;
+        if (g < G) {
+          s_prefix[g] = run;
+          const int a = p.offsets[g], b = p.offsets[g + 1];
+          run += b > a ? (b - a + BM - 1) / BM : 0;
+        }
+      }
+      if (lane == 31) {
+        const int last = p.offsets[G];
+        bad |= static_cast<long long>(last) > p.out_rows;
+        s_offs[G] = last;
+        s_prefix[G] = incl;
+      }
+      bad = __any_sync(0xffffffffu, bad);
+      if (lane == 31) *s_total = bad ? 0 : incl;
+      if (bad && lane == 0) report(p.status, MOE_ERR_BAD_INDEX);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(s_tmem, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+  const int total_work = *s_total * p.n_tiles;
+  const int KB = p.K / BK;
+  const int G = p.offsets == nullptr ? 1 : p.n_groups;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, issued_par = 0;
+      bool skip = (p.debug_flags & MOE_DEBUG_SKIP_FIRST_LOAD) != 0u;
+      bool ok = true;
+      for (int w = blockIdx.x; ok && w < total_work; w += gridDim.x) {
+        const Tile t = decode_tile(w, p.n_tiles, G, s_prefix, s_offs);
+        const int b_row = t.g * p.b_group_rows + t.nt * p.bn_out;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, s_abort)) {
+            ok = false;
+            break;
+          }
+          if (skip) {
+            skip = false;  // test hook: the consumer of this slot must time out
+          } else {
+            uint8_t* sa = smem + C::kOffA + stage * kABytes;
+            uint8_t* sb = smem + C::kOffB + stage * C::kBBytes;
+            mbar_expect_tx(&full[stage], C::kStageBytes);
+            tma_load_2d(sa, &tmA, &full[stage], kb * BK, t.row0);
+            if (EPI == EPI_SWIGLU) {
+              tma_load_2d(sb, &tmB, &full[stage], kb * BK, b_row);
+              tma_load_2d(sb + (BN_MMA / 2) * BK * 2, &tmB, &full[stage], kb * BK,
+                          b_row + p.b_up_offset);
+            } else {
+              tma_load_2d(sb, &tmB, &full[stage], kb * BK, b_row);
+            }
+            issued |= 1u << stage;
+            issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) fail(s_abort, p.status);
+      // every load issued here must land before the CTA may exit
+      for (int s = 0; s < STAGES; ++s)
+        if ((issued >> s) & 1u) mbar_wait(&full[s], (issued_par >> s) & 1u, nullptr);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN_MMA);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, aphase = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; ok && w < total_work; w += gridDim.x) {
+        if (!mbar_wait(&tempty[acc], aphase ^ 1u, s_abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN_MMA);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&full[stage], phase, s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sdesc_sw128(smem_u32(smem + C::kOffA + stage * kABytes));
+          const uint64_t bd = sdesc_sw128(smem_u32(smem + C::kOffB + stage * C::kBBytes));
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            umma_bf16(d, ad + 2u * k, bd + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
+          umma_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          aphase ^= 1u;
+        }
+      }
+      if (!ok) fail(s_abort, p.status);
+      // all MMAs issued here must be complete before TMEM is released
+      umma_commit(done);
+      mbar_wait(done, 0u, nullptr);
+    }
+    __syncwarp();
+  } else {
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int r_in = q * 32 + lane;
+    int acc = 0;
+    uint32_t aphase = 0;
+    for (int w = blockIdx.x; w < total_work; w += gridDim.x) {
+      const Tile t = decode_tile(w, p.n_tiles, G, s_prefix, s_offs);
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&tfull[acc], aphase, s_abort) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) fail(s_abort, p.status);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tbase =
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN_MMA);
+      const long long grow = static_cast<long long>(t.row0) + r_in;
+      const bool valid = r_in < t.rows && grow < p.out_rows;
+      if (EPI == EPI_SWIGLU) {
+        constexpr int BNH = BN_MMA / 2;
+        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + grow * p.ld_out +
+                              static_cast<long long>(t.nt) * p.bn_out;
+#pragma unroll 1
+        for (int c = 0; c < BNH; c += 32) {
+          uint32_t gv[32], uv[32];
+          tmem_ld32(tbase + c, gv);
+          tmem_ld32(tbase + BNH + c, uv);
+          tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float a0 = silu_f(__uint_as_float(gv[2 * i])) * __uint_as_float(uv[2 * i]);
+            const float a1 =
+                silu_f(__uint_as_float(gv[2 * i + 1])) * __uint_as_float(uv[2 * i + 1]);
+            pk[i] = pack_bf16x2(a0, a1);
+          }
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+        }
+      } else if (EPI == EPI_BF16) {
+        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + grow * p.ld_out +
+                              static_cast<long long>(t.nt) * p.bn_out;
+#pragma unroll 1
+        for (int c = 0; c < BN_MMA; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(tbase + c, v);
+          tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+        }
+      } else {
+        const int col0 = t.nt * p.bn_out;
+        float* orow = static_cast<float*>(p.out) + grow * p.ld_out + col0;
+#pragma unroll 1
+        for (int c = 0; c < BN_MMA; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(tbase + c, v);
+          tmem_ld_wait();
+          if (valid) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              const int col = col0 + c + i;
+              if (col + 4 <= p.out_cols) {
+                float4 f;
+                f.x = __uint_as_float(v[i]);
+                f.y = __uint_as_float(v[i + 1]);
+                f.z = __uint_as_float(v[i + 2]);
+                f.w = __uint_as_float(v[i + 3]);
+                if (p.bias != nullptr) {
+                  f.x += p.bias[(col + 0) / p.bias_div];
+                  f.y += p.bias[(col + 1) / p.bias_div];
+                  f.z += p.bias[(col + 2) / p.bias_div];
+                  f.w += p.bias[(col + 3) / p.bias_div];
+                }
+                *reinterpret_cast<float4*>(orow + c + i) = f;
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        aphase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// bf16 [rows, cols] row-major, box = 64 columns x box_rows rows, 128-B swizzle.
+bool make_tmap(CUtensorMap* m, const void* base, long long rows, int cols, int box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr || rows <= 0) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int BN_MMA, int EPI, int STAGES>
+cudaError_t run_gemm(const GemmArgs& g, cudaStream_t s) {
+  using C = Cfg<BN_MMA, STAGES>;
+  const int box_b = EPI == EPI_SWIGLU ? BN_MMA / 2 : BN_MMA;
+  CUtensorMap ta, tb;
+  if (!make_tmap(&ta, g.a, g.a_rows, g.K, BM)) return cudaErrorInvalidValue;
+  if (!make_tmap(&tb, g.b, g.b_rows, g.K, box_b)) return cudaErrorInvalidValue;
+  KParams kp;
+  kp.offsets = g.offsets;
+  kp.n_groups = g.offsets == nullptr ? 1 : g.n_groups;
+  kp.dense_rows = g.dense_rows;
+  kp.K = g.K;
+  kp.bn_out = box_b;
+  kp.n_tiles = (g.n_out + box_b - 1) / box_b;
+  kp.b_group_rows = g.b_group_rows;
+  kp.b_up_offset = EPI == EPI_SWIGLU ? g.n_out : 0;
+  kp.out = g.out;
+  kp.ld_out = g.ld_out;
+  kp.out_rows = g.out_rows;
+  kp.out_cols = g.n_out;
+  kp.bias = g.bias;
+  kp.bias_div = g.bias_div > 0 ? g.bias_div : 1;
+  kp.status = g.status;
+  kp.debug_flags = g.debug_flags;
+  long long m_tiles;
+  if (g.offsets == nullptr)
+    m_tiles = (g.dense_rows + BM - 1) / BM;
+  else
+    m_tiles = (g.max_rows_hint + BM - 1) / BM + g.n_groups;
+  const long long work = m_tiles * kp.n_tiles;
+  if (work <= 0) return cudaSuccess;
+  const int grid = static_cast<int>(work < g.sm_count ? work : g.sm_count);
+  auto kern = grouped_gemm_kernel<BN_MMA, EPI, STAGES>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(C::kSmemBytes));
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, C::kSmemBytes, s>>>(ta, tb, kp);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool gemm_supports_f32_router(int E_r) { return E_r == 64 || E_r == 128 || E_r == 256; }
+
+cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s) {
+  switch (g.epi) {
+    case EPI_SWIGLU:
+      if (g.n_out % 128 == 0) return run_gemm<256, EPI_SWIGLU, 4>(g, s);
+      return run_gemm<128, EPI_SWIGLU, 6>(g, s);
+    case EPI_BF16:
+      if (g.n_out % 256 == 0) return run_gemm<256, EPI_BF16, 4>(g, s);
+      if (g.n_out % 128 == 0) return run_gemm<128, EPI_BF16, 6>(g, s);
+      return run_gemm<64, EPI_BF16, 8>(g, s);
+    case EPI_F32:
+      if (g.n_out == 256) return run_gemm<256, EPI_F32, 4>(g, s);
+      if (g.n_out == 128) return run_gemm<128, EPI_F32, 6>(g, s);
+      if (g.n_out == 64) return run_gemm<64, EPI_F32, 8>(g, s);
+      return cudaErrorInvalidValue;
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace moe

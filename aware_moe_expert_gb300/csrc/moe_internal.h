@@ -1,0 +1,64 @@
+// Host-side launchers of the libmoe kernels (internal; the public ABI is
+// include/moe.h).  Each launcher enqueues on `stream` and returns the
+// cudaError_t of the launch.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// ---- route.cu
+cudaError_t launch_router_logits_small(const void* x, const void* router_w,
+                                       const float* expert_bias, int T, int H, int E_r,
+                                       int n_sub, float* logits, cudaStream_t s);
+cudaError_t launch_topk_gate(const float* logits, const int32_t* k_per_token, int T, int E_r,
+                             int k_max, int score, int renorm, float route_scale,
+                             int32_t* topk_idx, float* topk_w, int32_t* status,
+                             cudaStream_t s);
+
+// ---- permute.cu
+cudaError_t launch_permute(const int32_t* topk_idx, const int32_t* k_per_token, int T,
+                           int k_max, int E_r, uint32_t* bitmap, int32_t* wprefix,
+                           int32_t* counts, int32_t* offsets, int32_t* sorted_token,
+                           int32_t* inv_row, int32_t* status, cudaStream_t s);
+cudaError_t launch_gather_rows(const void* x, const int32_t* sorted_token,
+                               const int32_t* offsets, int E_r, int T, int H, int n_cap,
+                               void* x_perm, int32_t* status, int sm_count, cudaStream_t s);
+
+// ---- combine.cu
+cudaError_t launch_combine(const void* y_perm, const void* y_shared, const int32_t* inv_row,
+                           const float* topk_w, const int32_t* k_per_token, int T, int H,
+                           int k_max, int n_rows, void* out, int32_t* status, cudaStream_t s);
+
+// ---- gemm.cu
+enum GemmEpi { EPI_SWIGLU = 0, EPI_BF16 = 1, EPI_F32 = 2 };
+
+struct GemmArgs {
+  int epi;                   // GemmEpi
+  const void* a;             // bf16 [a_rows, K]
+  long long a_rows;
+  const void* b;             // bf16 [b_rows, K]
+  long long b_rows;
+  int K;                     // multiple of 64
+  const int32_t* offsets;    // [n_groups + 1] device, or nullptr for one dense group
+  int n_groups;
+  int dense_rows;            // rows of the dense group (offsets == nullptr)
+  int n_out;                 // output columns per group (SWIGLU: I; BF16: H; F32: E_r)
+  int b_group_rows;          // B rows per group (SWIGLU: 2I; BF16: H; F32: 0)
+  void* out;                 // SWIGLU/BF16: bf16, F32: fp32
+  long long ld_out;          // elements
+  long long out_rows;        // rows the output buffer holds (stores beyond are dropped)
+  const float* bias;         // F32 only, nullable
+  int bias_div;
+  int32_t* status;
+  uint32_t debug_flags;
+  int sm_count;
+  int max_rows_hint;         // upper bound of total rows (grid sizing)
+};
+
+cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s);
+bool gemm_supports_f32_router(int E_r);
+
+}  // namespace moe

@@ -1,0 +1,189 @@
+// Permutation of the routed assignments into unit-contiguous rows, and the
+// row gather that feeds the grouped GEMM.
+//
+// MoE-Prism (arXiv 2510.19366) §II-D: grouped-GEMM MoE kernels need the
+// token rows of one expert contiguous.  The order is fixed so the result is
+// bit-reproducible: unit ascending, token ascending inside a unit.
+//
+// Deterministic without position atomics: a membership bitmap
+// bitmap[u][w] (bit b of word w = token 32w+b selected u) is built per
+// 32-token block in shared memory (atomicOr only merges bits, so the result
+// does not depend on order).  One CTA then turns per-word popcounts into
+// per-unit word prefixes and the unit offsets, and the rank of (t, u) inside
+// unit u is offsets[u] + prefix[u][t/32] + popcount(bits of earlier tokens).
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+// One CTA per 32-token word.  bits[u] collects the tokens of this word that
+// selected unit u; invalid or repeated unit indices are reported.
+__global__ void __launch_bounds__(256) bitmap_kernel(const int32_t* __restrict__ topk_idx,
+                                                      const int32_t* __restrict__ kpt, int T,
+                                                      int k_max, int E_r, int W,
+                                                      uint32_t* __restrict__ bitmap,
+                                                      int32_t* status) {
+  __shared__ uint32_t bits[256];
+  for (int u = threadIdx.x; u < E_r; u += blockDim.x) bits[u] = 0u;
+  __syncthreads();
+  const int word = blockIdx.x;
+  for (int i = threadIdx.x; i < 32 * k_max; i += blockDim.x) {
+    const int tl = i / k_max, j = i - tl * k_max;
+    const int t = word * 32 + tl;
+    if (t >= T) continue;
+    int k = kpt[t];
+    if (k < 1 || k > k_max) {
+      if (j == 0) report(status, MOE_ERR_K_RANGE);
+      k = min(max(k, 0), k_max);
+    }
+    if (j >= k) continue;
+    const int u = topk_idx[static_cast<size_t>(t) * k_max + j];
+    if (u < 0 || u >= E_r) {
+      report(status, MOE_ERR_BAD_INDEX);
+      continue;
+    }
+    const uint32_t bit = 1u << tl;
+    const uint32_t old = atomicOr(&bits[u], bit);
+    if (old & bit) report(status, MOE_ERR_BAD_INDEX);
+  }
+  __syncthreads();
+  for (int u = threadIdx.x; u < E_r; u += blockDim.x)
+    bitmap[static_cast<size_t>(u) * W + word] = bits[u];
+}
+
+// Single CTA, 1024 threads: warp w handles units w, w+32, ...; then warp 0
+// scans the unit counts into offsets.
+__global__ void __launch_bounds__(1024) scan_kernel(const uint32_t* __restrict__ bitmap, int E_r,
+                                                     int W, int32_t* __restrict__ wprefix,
+                                                     int32_t* __restrict__ counts,
+                                                     int32_t* __restrict__ offsets) {
+  __shared__ int32_t s_cnt[256];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int u = warp; u < E_r; u += 32) {
+    const uint32_t* row = bitmap + static_cast<size_t>(u) * W;
+    int32_t* pre = wprefix + static_cast<size_t>(u) * W;
+    int running = 0;
+    for (int w0 = 0; w0 < W; w0 += 32) {
+      const int w = w0 + lane;
+      const int c = w < W ? __popc(row[w]) : 0;
+      int incl = c;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      if (w < W) pre[w] = running + incl - c;
+      running += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) s_cnt[u] = running;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // each lane owns a contiguous run of up to 8 units
+    const int per = (E_r + 31) / 32;
+    const int u0 = lane * per;
+    int local = 0;
+    for (int i = 0; i < per; ++i)
+      if (u0 + i < E_r) local += s_cnt[u0 + i];
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    int run = incl - local;
+    for (int i = 0; i < per; ++i) {
+      const int u = u0 + i;
+      if (u < E_r) {
+        offsets[u] = run;
+        counts[u] = s_cnt[u];
+        run += s_cnt[u];
+      }
+    }
+    if (lane == 31) offsets[E_r] = incl;
+  }
+}
+
+// One thread per (t, j) slot.
+__global__ void __launch_bounds__(256) scatter_kernel(
+    const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ kpt, int T, int k_max,
+    int E_r, int W, const uint32_t* __restrict__ bitmap, const int32_t* __restrict__ wprefix,
+    const int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_token,
+    int32_t* __restrict__ inv_row) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= static_cast<long long>(T) * k_max) return;
+  const int t = static_cast<int>(i / k_max), j = static_cast<int>(i - static_cast<long long>(t) * k_max);
+  const int k = min(max(kpt[t], 0), k_max);
+  int pos = -1;
+  if (j < k) {
+    const int u = topk_idx[i];
+    if (u >= 0 && u < E_r) {
+      const int w = t >> 5;
+      const uint32_t below = (1u << (t & 31)) - 1u;
+      const size_t o = static_cast<size_t>(u) * W + w;
+      pos = offsets[u] + wprefix[o] + __popc(bitmap[o] & below);
+      sorted_token[pos] = t;
+    }
+  }
+  inv_row[i] = pos;
+}
+
+// x_perm[r] = x[sorted_token[r]] for r < offsets[E_r]; one warp per row,
+// 16-byte vectors.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x,
+                                                           const int32_t* __restrict__ sorted_token,
+                                                           const int32_t* __restrict__ offsets,
+                                                           int E_r, int T, int nv, int n_cap,
+                                                           uint4* __restrict__ x_perm,
+                                                           int32_t* status) {
+  const int n = min(offsets[E_r], n_cap);
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  for (int r = gw; r < n; r += nw) {
+    const int t = sorted_token[r];
+    uint4* dst = x_perm + static_cast<size_t>(r) * nv;
+    if (t < 0 || t >= T) {
+      if (lane == 0) report(status, MOE_ERR_BAD_INDEX);
+      for (int v = lane; v < nv; v += 32) dst[v] = make_uint4(0u, 0u, 0u, 0u);
+      continue;
+    }
+    const uint4* src = x + static_cast<size_t>(t) * nv;
+    for (int v = lane; v < nv; v += 32) dst[v] = __ldg(src + v);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_permute(const int32_t* topk_idx, const int32_t* k_per_token, int T,
+                           int k_max, int E_r, uint32_t* bitmap, int32_t* wprefix,
+                           int32_t* counts, int32_t* offsets, int32_t* sorted_token,
+                           int32_t* inv_row, int32_t* status, cudaStream_t s) {
+  const int W = (T + 31) / 32;
+  if (W > 0) {
+    bitmap_kernel<<<W, 256, 0, s>>>(topk_idx, k_per_token, T, k_max, E_r, W, bitmap, status);
+  }
+  scan_kernel<<<1, 1024, 0, s>>>(bitmap, E_r, W, wprefix, counts, offsets);
+  const long long slots = static_cast<long long>(T) * k_max;
+  if (slots > 0) {
+    scatter_kernel<<<static_cast<unsigned>((slots + 255) / 256), 256, 0, s>>>(
+        topk_idx, k_per_token, T, k_max, E_r, W, bitmap, wprefix, offsets, sorted_token, inv_row);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const void* x, const int32_t* sorted_token,
+                               const int32_t* offsets, int E_r, int T, int H, int n_cap,
+                               void* x_perm, int32_t* status, int sm_count, cudaStream_t s) {
+  if (n_cap <= 0) return cudaSuccess;
+  const int warps_needed = n_cap;
+  int blocks = (warps_needed + 7) / 8;
+  blocks = blocks < sm_count * 8 ? blocks : sm_count * 8;
+  gather_rows_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint4*>(x), sorted_token, offsets,
+                                             E_r, T, H / 8, n_cap, static_cast<uint4*>(x_perm),
+                                             status);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,213 @@
+// Router: logits on CUDA cores for small token counts, and the warp-per-token
+// top-k_t selection with softmax / sigmoid gates.
+//
+// MoE-Prism (arXiv 2510.19366) §III-B2, expanded linear gate: a linear layer
+// scores every sub-expert and the layer-wide top-k is taken over all of them;
+// §III-C1: the budget k_i belongs to the request, so each token has its own k.
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kTokPerCta = 8;
+
+__device__ __forceinline__ float dot8_bf16(uint4 a, uint4 b, float acc) {
+  const uint32_t av[4] = {a.x, a.y, a.z, a.w};
+  const uint32_t bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    acc = fmaf(bf16lo(av[i]), bf16lo(bv[i]), acc);
+    acc = fmaf(bf16hi(av[i]), bf16hi(bv[i]), acc);
+  }
+  return acc;
+}
+
+// logits[t, u] = x_t . router_w[u] + bias[u / n_sub].  CTA = 8 tokens x 8
+// units, one warp per unit; lanes stride over H in 16-byte vectors.
+__global__ void __launch_bounds__(256) router_logits_small_kernel(
+    const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ rw,
+    const float* __restrict__ bias, int T, int H, int E_r, int n_sub,
+    float* __restrict__ logits) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int u = blockIdx.y * 8 + warp;
+  const int t0 = blockIdx.x * kTokPerCta;
+  if (u >= E_r) return;
+  const int nt = min(kTokPerCta, T - t0);
+  float acc[kTokPerCta];
+#pragma unroll
+  for (int i = 0; i < kTokPerCta; ++i) acc[i] = 0.f;
+  const uint4* wrow = reinterpret_cast<const uint4*>(rw + static_cast<size_t>(u) * H);
+  const int nv = H / 8;
+  for (int v = lane; v < nv; v += 32) {
+    const uint4 wv = __ldg(wrow + v);
+#pragma unroll
+    for (int i = 0; i < kTokPerCta; ++i) {
+      if (i < nt) {
+        const uint4 xv =
+            __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(t0 + i) * H) + v);
+        acc[i] = dot8_bf16(xv, wv, acc[i]);
+      }
+    }
+  }
+  float mine = 0.f;
+#pragma unroll
+  for (int i = 0; i < kTokPerCta; ++i) {
+    float a = acc[i];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+    if (lane == i) mine = a;
+  }
+  if (lane < nt) {
+    const float b = bias != nullptr ? bias[u / n_sub] : 0.f;
+    logits[static_cast<size_t>(t0 + lane) * E_r + u] = mine + b;
+  }
+}
+
+// Total order used for selection: larger logit first; -0 == +0; NaN below
+// every number.  The key is monotone in the logit.
+__device__ __forceinline__ uint32_t order_key(float L) {
+  if (L != L) return 0u;
+  uint32_t b = __float_as_uint(L);
+  if ((b & 0x7fffffffu) == 0u) b = 0u;  // -0 is +0
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// One warp per token.  Lane l holds units l, l+32, ... (IPL per lane).
+// Round j picks the best remaining unit with a 64-bit warp max over
+// (key << 32 | ~u), so equal keys resolve to the lower unit index.
+template <int IPL>
+__global__ void __launch_bounds__(256) topk_gate_kernel(
+    const float* __restrict__ logits, const int32_t* __restrict__ kpt, int T, int E_r,
+    int k_max, int score, int renorm, float route_scale, int32_t* __restrict__ topk_idx,
+    float* __restrict__ topk_w, int32_t* status) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  int k = kpt[t];
+  if (k < 1 || k > k_max) {
+    if (lane == 0) report(status, MOE_ERR_K_RANGE);
+    k = min(max(k, 0), k_max);
+  }
+  k = min(k, E_r);
+
+  float v[IPL];
+  uint32_t key[IPL];
+  bool bad = false;
+  const float* row = logits + static_cast<size_t>(t) * E_r;
+#pragma unroll
+  for (int i = 0; i < IPL; ++i) {
+    const int u = lane + 32 * i;
+    if (u < E_r) {
+      const float L = row[u];
+      bad |= !isfinite(L);
+      v[i] = L;
+      key[i] = order_key(L);
+    } else {
+      v[i] = 0.f;
+      key[i] = 0u;
+    }
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) report(status, MOE_ERR_NONFINITE);
+
+  float mx = -INFINITY, sum = 0.f;
+  if (score == MOE_SCORE_SOFTMAX) {
+#pragma unroll
+    for (int i = 0; i < IPL; ++i)
+      if (lane + 32 * i < E_r) mx = fmaxf(mx, v[i]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+#pragma unroll
+    for (int i = 0; i < IPL; ++i)
+      if (lane + 32 * i < E_r) sum += expf(v[i] - mx);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  }
+
+  uint32_t taken = 0;
+  int my_u = -1;
+  float my_s = 0.f;
+  for (int j = 0; j < k; ++j) {
+    unsigned long long best = 0ull;
+#pragma unroll
+    for (int i = 0; i < IPL; ++i) {
+      const int u = lane + 32 * i;
+      if (u < E_r && !((taken >> i) & 1u)) {
+        const unsigned long long c =
+            (static_cast<unsigned long long>(key[i]) << 32) | static_cast<uint32_t>(~u);
+        best = c > best ? c : best;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
+      best = o > best ? o : best;
+    }
+    const int u = static_cast<int>(~static_cast<uint32_t>(best & 0xffffffffull));
+    const int owner = u & 31, item = u >> 5;
+    float s_local = 0.f;
+    if (lane == owner) {
+      float L = 0.f;
+#pragma unroll
+      for (int i = 0; i < IPL; ++i)
+        if (i == item) L = v[i];
+      taken |= 1u << item;
+      s_local = (score == MOE_SCORE_SOFTMAX) ? expf(L - mx) / sum : 1.f / (1.f + expf(-L));
+    }
+    const float s = __shfl_sync(0xffffffffu, s_local, owner);
+    if (lane == j) {
+      my_u = u;
+      my_s = s;
+    }
+  }
+  float selsum = lane < k ? my_s : 0.f;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) selsum += __shfl_xor_sync(0xffffffffu, selsum, off);
+  if (lane < k_max) {
+    const size_t o = static_cast<size_t>(t) * k_max + lane;
+    if (lane < k) {
+      const float w = renorm ? my_s / selsum : my_s;
+      topk_idx[o] = my_u;
+      topk_w[o] = w * route_scale;
+    } else {
+      topk_idx[o] = -1;
+      topk_w[o] = 0.f;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_router_logits_small(const void* x, const void* router_w,
+                                       const float* expert_bias, int T, int H, int E_r,
+                                       int n_sub, float* logits, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  dim3 grid((T + kTokPerCta - 1) / kTokPerCta, (E_r + 7) / 8);
+  router_logits_small_kernel<<<grid, 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(router_w),
+      expert_bias, T, H, E_r, n_sub, logits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk_gate(const float* logits, const int32_t* k_per_token, int T, int E_r,
+                             int k_max, int score, int renorm, float route_scale,
+                             int32_t* topk_idx, float* topk_w, int32_t* status,
+                             cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  const int grid = (T + 7) / 8;
+  if (E_r <= 32)
+    topk_gate_kernel<1><<<grid, 256, 0, s>>>(logits, k_per_token, T, E_r, k_max, score, renorm,
+                                             route_scale, topk_idx, topk_w, status);
+  else if (E_r <= 64)
+    topk_gate_kernel<2><<<grid, 256, 0, s>>>(logits, k_per_token, T, E_r, k_max, score, renorm,
+                                             route_scale, topk_idx, topk_w, status);
+  else if (E_r <= 128)
+    topk_gate_kernel<4><<<grid, 256, 0, s>>>(logits, k_per_token, T, E_r, k_max, score, renorm,
+                                             route_scale, topk_idx, topk_w, status);
+  else
+    topk_gate_kernel<8><<<grid, 256, 0, s>>>(logits, k_per_token, T, E_r, k_max, score, renorm,
+                                             route_scale, topk_idx, topk_w, status);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

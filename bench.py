@@ -1,0 +1,485 @@
+"""Benchmark of the k-aware MoE layer forward on GB300 (prints ONE JSON line).
+
+A step is one pass of the whole hot path over one batch: router logits and
+top-k_t (moe_route), permutation (moe_permute), grouped gate|up + SwiGLU
+(moe_gate_up), grouped down (moe_down), weighted combine (moe_combine), plus
+the shared expert where the workload has one.  Inputs are seeded synthetic
+tensors already resident in HBM.  The default workload is the
+Mixtral-8x7B-shaped decode step (H 4096, 8 experts x 4 sub-experts of 3584,
+64 one-token requests, k in {2,4,6,8}); its metric is microseconds per layer.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload.  Under torchrun (N > 1) every rank runs an
+independent replica (the layer has no exchange step); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("MoE-layer tokens/s (prefill), µs/layer (decode), % of roofline, 1×GB300")
+THROTTLE_BITS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+                 0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+                 0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+                 0x100: "display_clock_setting"}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=30)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--workload", default="mixtral_decode")
+    p.add_argument("--T", type=int, default=None, help="override the token count")
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--cpu-budget-s", type=float, default=30.0)
+    return p.parse_args()
+
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0,
+                source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    def __init__(self, index: int, out_path: str):
+        self.path = out_path
+        self.proc = None
+        self.index = index
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active")
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], [], 0
+        for line in open(self.path):
+            parts = [s.strip() for s in line.split(",")]
+            if len(parts) < 5:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+                reasons |= int(parts[4], 16)
+            except ValueError:
+                continue
+        if not sm:
+            return None
+        names = [n for b, n in THROTTLE_BITS.items() if reasons & b and n != "gpu_idle"]
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "reasons": names,
+                "samples": len(sm)}
+
+
+def source_hash(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "aware_moe_expert_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(workload_name: str, kernel: str, per_launch_units: float):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        table = json.load(f)
+    e = table.get(f"{workload_name}:{kernel}")
+    if not e or e.get("source_hash") != source_hash(*e.get("sources", ["gemm.cu"])):
+        return None
+    return float(e["dram_bytes_per_launch"]) * per_launch_units / float(e.get("units", per_launch_units))
+
+
+def run_ours(args, wl, rank, world, local):
+    import torch
+    from aware_moe_expert_gb300 import binding as B
+    from aware_moe_expert_gb300.inputs import make_layer_inputs
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    d = make_layer_inputs(wl, dev, seed=wl.seed + 1000 * rank)
+    desc = B.desc_for(wl, expert_bias=d["expert_bias"], w_shared_gate_up=d.get("w_shared_gate_up"),
+                      w_shared_down=d.get("w_shared_down"))
+    T, H, E_r, k_max, I_sub = wl.T, wl.H, wl.E_r, wl.k_max, wl.I_sub
+    ws = torch.empty(B.moe_workspace_size(desc), dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    idx = torch.empty(T, k_max, dtype=torch.int32, device=dev)
+    w = torch.empty(T, k_max, dtype=torch.float32, device=dev)
+    counts = torch.empty(E_r, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E_r + 1, dtype=torch.int32, device=dev)
+    st_tok = torch.empty(T * k_max, dtype=torch.int32, device=dev)
+    inv = torch.empty(T * k_max, dtype=torch.int32, device=dev)
+    act = torch.empty(T * k_max, I_sub, dtype=torch.bfloat16, device=dev)
+    y = torch.empty(T * k_max, H, dtype=torch.bfloat16, device=dev)
+    ysh = torch.empty(T, H, dtype=torch.bfloat16, device=dev) if wl.I_shared else None
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    sp = stream.cuda_stream
+
+    def step(ev=None):
+        def rec(i):
+            if ev is not None:
+                ev[i].record(stream)
+        rec(0)
+        B.check(B.moe_route(desc, d["x"], d["router_w"], None, d["k_per_token"], None, idx, w,
+                            st, ws, sp), "moe_route")
+        rec(1)
+        B.check(B.moe_permute(desc, idx, d["k_per_token"], counts, offsets, st_tok, inv, st, ws,
+                              sp), "moe_permute")
+        rec(2)
+        if ysh is not None:
+            B.check(B.moe_shared_ffn(desc, d["x"], ysh, st, ws, sp), "moe_shared_ffn")
+        rec(3)
+        B.check(B.moe_gate_up(desc, d["x"], st_tok, offsets, d["w_gate_up"], act, st, ws, sp),
+                "moe_gate_up")
+        rec(4)
+        B.check(B.moe_down(desc, act, offsets, d["w_down"], y, st, ws, sp), "moe_down")
+        rec(5)
+        B.check(B.moe_combine(desc, y, ysh, inv, w, d["k_per_token"], out, st, sp), "moe_combine")
+        rec(6)
+
+    # realised routing statistics (one untimed pass)
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize(dev)
+    code = B.moe_get_device_status(st, sp)
+    if code != 0:
+        raise RuntimeError(f"device status {B.STATUS_NAMES.get(code, code)}")
+    cnt = counts.cpu().numpy()
+    n_assign = int(cnt.sum())
+    D = int(np.count_nonzero(cnt))
+
+    # L2 handling: flush with a 2x-L2 write between steps unless the step
+    # streams far more than L2 anyway.
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    w_active = D * 3 * H * I_sub * 2 + (3 * H * wl.I_shared * 2 if wl.I_shared else 0)
+    flush = w_active < 4 * l2
+    flush_buf = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev) if flush else None
+
+    n_ev = 7
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+    for _ in range(args.warmup):
+        if flush:
+            with torch.cuda.stream(stream):
+                flush_buf.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    smi_path = os.path.join(ROOT, "gpurun_out", f"bench_clocks_r{rank}.csv")
+    os.makedirs(os.path.dirname(smi_path), exist_ok=True)
+    with ClockSampler(local, smi_path) as cs:
+        t_wall0 = time.perf_counter()
+        for i in range(args.steps):
+            if flush:
+                with torch.cuda.stream(stream):
+                    flush_buf.zero_()
+            step(evs[i])
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall0
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    code = B.moe_get_device_status(st, sp)
+    if code != 0:
+        raise RuntimeError(f"device status {B.STATUS_NAMES.get(code, code)}")
+    per = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(n_ev - 1)]
+                    for i in range(args.steps)])  # ms
+    step_ms = per.sum(axis=1)
+    ms = float(step_ms.mean())
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    parts = {n: float(per[:, j].mean() * 1000.0) for j, n in
+             enumerate(["route", "permute", "shared_ffn", "gate_up", "down", "combine"])}
+
+    # end to end through the public call with host buffers
+    e2e = None
+    if not args.no_e2e:
+        layer = B.MoeLayer(desc, dev)
+        hx = d["x"].cpu().pin_memory()
+        hk = d["k_per_token"].cpu().pin_memory()
+        hout = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+        dx = torch.empty_like(d["x"])
+        dk = torch.empty_like(d["k_per_token"])
+        dout = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        e0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        e1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+
+        def e2e_step(i=None):
+            with torch.cuda.stream(stream):
+                if i is not None:
+                    e0[i].record(stream)
+                dx.copy_(hx, non_blocking=True)
+                dk.copy_(hk, non_blocking=True)
+                B.check(B.moe_layer_forward(desc, dx, d["router_w"], d["w_gate_up"], d["w_down"],
+                                            dk, dout, layer.status, layer.workspace, sp))
+                hout.copy_(dout, non_blocking=True)
+                if i is not None:
+                    e1[i].record(stream)
+        for _ in range(args.warmup):
+            if flush:
+                with torch.cuda.stream(stream):
+                    flush_buf.zero_()
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        for i in range(args.steps):
+            if flush:
+                with torch.cuda.stream(stream):
+                    flush_buf.zero_()
+            e2e_step(i)
+        torch.cuda.synchronize(dev)
+        e2e_ms = float(np.mean([e0[i].elapsed_time(e1[i]) for i in range(args.steps)]))
+        h2d = T * H * 2 + T * 4
+        d2h = T * H * 2
+        e2e = (e2e_ms, h2d, d2h)
+        if layer.device_status(sp) != 0:
+            raise RuntimeError("device status after e2e")
+
+    peaks = load_peaks()
+    # algorithmic work (spec formulas)
+    F_routed = 6.0 * H * I_sub * n_assign
+    F_shared = 6.0 * H * wl.I_shared * T
+    F_router = 2.0 * T * H * E_r
+    F = F_routed + F_shared + F_router
+    Bytes = 2.0 * (D * 3 * H * I_sub + 3 * H * wl.I_shared + E_r * H + 2 * T * H)
+    t_roof_us = max(F / (peaks["bf16_tflops"] * 1e12), Bytes / (peaks["hbm_gbs"] * 1e9)) * 1e6
+    bound = "tensor" if F / (peaks["bf16_tflops"] * 1e12) > Bytes / (peaks["hbm_gbs"] * 1e9) else "hbm"
+
+    # dominant kernel: the grouped gate|up call (2/3 of the routed work)
+    gu_us = parts["gate_up"]
+    if wl.phase == "decode":
+        alg = 2.0 * (D * 2 * I_sub * H + n_assign * H + n_assign * I_sub)  # weights + x rows + act
+        achieved = alg / (gu_us * 1e-6) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": traffic_for(wl.name, "gate_up", 1.0),
+                "kernel": "moe_gate_up (row gather + grouped gate|up GEMM, SwiGLU epilogue)",
+                "algorithmic_bytes": alg, "peak_source": peaks["source"] + " hbm_gbs"}
+    else:
+        alg = 4.0 * H * I_sub * n_assign
+        achieved = alg / (gu_us * 1e-6) / 1e12
+        pk = peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk, "unit": "TFLOP/s",
+                "frac": round(achieved / pk, 4), "traffic": traffic_for(wl.name, "gate_up", 1.0),
+                "kernel": "moe_gate_up (row gather + grouped gate|up GEMM, SwiGLU epilogue)",
+                "algorithmic_flops": alg, "peak_source": peaks["source"] + " bf16_tflops (burst)"}
+
+    n_launch = launches_per_step(wl, T)
+    us = ms * 1000.0
+    res = {
+        "metric": METRIC,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+    }
+    if wl.phase == "decode":
+        res.update({"value": round(us, 2), "unit": "µs/layer", "higher_is_better": False})
+    else:
+        res.update({"value": round(T * world / (ms * 1e-3), 1), "unit": "tokens/s",
+                    "higher_is_better": True})
+    res["config"] = {"workload": wl.name, "T": T, "H": H, "experts": wl.n_experts,
+                     "n_sub": wl.n_sub, "E_r": E_r, "I_sub": I_sub, "I_shared": wl.I_shared,
+                     "k_choices": list(wl.k_choices), "k_per": wl.k_per, "score": wl.score,
+                     "parallelism": f"replicas{world}",
+                     "l2": (f"flushed between steps ({2 * l2 >> 20} MiB write)" if flush else
+                            f"inputs larger than L2 ({w_active / 2**20:.0f} MiB of active weights "
+                            f"per step vs {l2 >> 20} MiB L2)")}
+    res["realised"] = {"n_assign": n_assign, "distinct_units": D, "k_mean": n_assign / T}
+    res["roofline_layer"] = {"t_roof_us": round(t_roof_us, 2), "bound": bound,
+                             "frac": round(t_roof_us / us, 4), "flops": F, "bytes": Bytes}
+    res["roofline"] = roof
+    res["breakdown_us"] = {k: round(v, 2) for k, v in parts.items()}
+    res["gpu_launches"] = n_launch * args.steps
+    if e2e is not None:
+        e2e_ms, h2d, d2h = e2e
+        if wl.phase == "decode":
+            res["e2e"] = {"value": round(e2e_ms * 1000.0, 2), "unit": "µs/layer",
+                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        else:
+            res["e2e"] = {"value": round(T / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    clocks = cs.summary()
+    res["clocks"] = clocks
+    res["wall_s_timed"] = round(t_wall, 4)
+    return res, d
+
+
+def launches_per_step(wl, T):
+    """Kernels libmoe enqueues per step (mirrors the host sequencing)."""
+    n = 0
+    tensor_router = T >= 128 and wl.E_r in (64, 128, 256)
+    n += 1 + 1                 # logits (GEMM or CUDA-core) + top-k
+    n += (1 if T > 0 else 0) + 1 + (1 if T > 0 else 0)   # bitmap, scan, scatter
+    n += 2 if wl.I_shared else 0
+    n += 2                     # gather + gate|up GEMM
+    n += 1                     # down GEMM
+    n += 1                     # combine
+    del tensor_router
+    return n
+
+
+def oracle_sample(wl, d_host, budget_s):
+    """Time the fp64 oracle on a bounded sample of the workload's tokens.
+    Returns (seconds, n_tokens, description)."""
+    from oracle import moe_oracle as O
+    T = wl.T
+    spec_full = dict(H=wl.H, n_experts=wl.n_experts, n_sub=wl.n_sub, I_sub=wl.I_sub,
+                     k_max=wl.k_max, score=wl.score, renorm=wl.renorm,
+                     route_scale=wl.route_scale, I_shared=wl.I_shared)
+    n = T if wl.phase == "decode" else min(T, 64)
+    spec = O.LayerSpec(T=n, **spec_full)
+    t0 = time.perf_counter()
+    O.layer_forward(spec, d_host["x"][:n], d_host["router_w"], d_host["w_gate_up"],
+                    d_host["w_down"], d_host["k"][:n], expert_bias=d_host["bias"],
+                    w_shared_gate_up=d_host.get("sgu"), w_shared_down=d_host.get("sd"))
+    dt = time.perf_counter() - t0
+    return dt, n
+
+
+def host_copy(d, wl):
+    from aware_moe_expert_gb300.inputs import bf16_bits
+    h = {"x": bf16_bits(d["x"]), "router_w": bf16_bits(d["router_w"]),
+         "w_gate_up": (lambda u, w=d["w_gate_up"]: bf16_bits(w[u])),
+         "w_down": (lambda u, w=d["w_down"]: bf16_bits(w[u])),
+         "k": d["k_per_token"].cpu().numpy(),
+         "bias": None if d["expert_bias"] is None else d["expert_bias"].cpu().numpy()}
+    if wl.I_shared:
+        h["sgu"] = bf16_bits(d["w_shared_gate_up"])
+        h["sd"] = bf16_bits(d["w_shared_down"])
+    return h
+
+
+def cpu_baseline_entry(wl, d, budget_s):
+    h = host_copy(d, wl)
+    dt, n = oracle_sample(wl, h, budget_s)
+    cores = os.cpu_count()
+    if wl.phase == "decode":
+        value, unit = dt * 1e6, "µs/layer"
+        sample = f"the whole {wl.T}-token decode batch, one layer"
+    else:
+        value, unit = n / dt, "tokens/s"
+        sample = f"first {n} of {wl.T} tokens (tokens are independent), one layer"
+    return {"value": round(value, 3), "unit": unit, "cores": cores, "kind": "oracle",
+            "sample": sample + "; float64 numpy, BLAS matmuls on all host cores, "
+                      "element-wise steps single-threaded", "seconds": round(dt, 3)}
+
+
+def run_reference(args, wl, rank, world):
+    """--impl reference: the oracle, as it stands, timed on the host cores."""
+    if rank != 0:
+        return None
+    import torch
+    from aware_moe_expert_gb300.inputs import make_layer_inputs
+    d = make_layer_inputs(wl, "cpu") if wl.T * wl.H < 1 << 26 and wl.E_r * wl.H * wl.I_sub < 1 << 31 \
+        else make_layer_inputs(wl, "cpu")
+    h = host_copy(d, wl)
+    times = []
+    for i in range(args.warmup + args.steps):
+        dt, n = oracle_sample(wl, h, args.cpu_budget_s)
+        if i >= args.warmup:
+            times.append(dt)
+        if sum(times) > 240:
+            break
+    dt = float(np.mean(times))
+    if wl.phase == "decode":
+        value, unit, hib = dt * 1e6, "µs/layer", False
+        sample = f"the whole {wl.T}-token decode batch, one layer"
+    else:
+        value, unit, hib = n / dt, "tokens/s", True
+        sample = f"first {n} of {wl.T} tokens, one layer"
+    del torch
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": unit,
+            "n_gpus": world, "steps": len(times), "warmup": args.warmup,
+            "ms_per_step": round(dt * 1e3, 3), "higher_is_better": hib, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "T": wl.T, "parallelism": "host cores"},
+            "cpu_baseline": {"value": round(value, 3), "unit": unit, "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": unit, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    from aware_moe_expert_gb300 import workloads as WL
+    wl = WL.ALL[args.workload]
+    if args.T is not None:
+        wl = wl.with_T(args.T)
+    rank, world, local = dist_info()
+    if args.impl == "reference":
+        res = run_reference(args, wl, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    res, d = run_ours(args, wl, rank, world, local)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline_entry(wl, d, args.cpu_budget_s)
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

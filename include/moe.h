@@ -1,0 +1,175 @@
+/*
+ * moe.h - C ABI of libmoe.so: one k-aware Mixture-of-Experts layer forward
+ * on an NVIDIA GB300 (sm_103a).
+ *
+ * The layer (MoE-Prism, arXiv 2510.19366, §III-B and §III-C1): every token t
+ * carries its own routing budget k_t.  The router scores E_r = n_experts *
+ * n_sub routing units (an expert's intermediate neurons split into n_sub equal
+ * sub-experts, §III-B1 Eq. (3)); token t runs the k_t best units through a
+ * SwiGLU FFN (§III-B1 Eq. (1)) and sums their outputs weighted by the gate
+ * (§III-B2, expanded linear gate).
+ *
+ * Conventions for every call below
+ *  - Tensor pointers are DEVICE memory owned by the caller; bf16 tensors are
+ *    passed as const void*, row-major, contiguous, 16-byte aligned.  The
+ *    library never allocates, frees, or synchronises inside these calls.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *    NULL is the legacy default stream) and returns a moe_status for errors
+ *    the host can see (bad arguments, unsupported shapes, launch failures).
+ *  - Errors the device finds (k_t out of range, non-finite logits, bad unit
+ *    indices, a device wait that gave up) are written to `dev_status`, a
+ *    caller-owned int32 in device memory that the caller zeroes; the first
+ *    error wins.  Read it with moe_get_device_status (the only call that
+ *    synchronises).
+ *  - `workspace` is caller-owned device memory of at least
+ *    moe_workspace_size(desc) bytes, 256-byte aligned.  Calls on the same
+ *    workspace must not overlap in time.
+ *  - Weight layout (routing unit u = e * n_sub + n):
+ *      w_gate_up [E_r, 2*I_sub, H]  rows 0..I_sub-1 gate, I_sub..2*I_sub-1 up
+ *                                   (out x in, as a linear layer)
+ *      w_down    [E_r, H, I_sub]
+ *      router_w  [E_r, H]
+ *  - Supported shapes: H % 64 == 0, I_sub % 64 == 0, I_shared % 64 == 0,
+ *    1 <= E_r <= 256, 1 <= k_max <= min(E_r, 32), T >= 0.  Anything else
+ *    returns MOE_ERR_UNSUPPORTED_SHAPE; there is no fallback path.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARGUMENT = 1,  /* null / misaligned / inconsistent argument       */
+  MOE_ERR_UNSUPPORTED_SHAPE = 2, /* shape outside the supported set above          */
+  MOE_ERR_WORKSPACE = 3,         /* workspace pointer null or misaligned           */
+  MOE_ERR_CUDA = 4,              /* a CUDA runtime/driver call or launch failed     */
+  MOE_ERR_DEVICE_TIMEOUT = 5,    /* device: a bounded wait gave up                  */
+  MOE_ERR_NONFINITE = 6,         /* device: a router logit is NaN or infinite       */
+  MOE_ERR_K_RANGE = 7,           /* device: some k_t outside [1, k_max]             */
+  MOE_ERR_BAD_INDEX = 8          /* device: unit index out of range or repeated     */
+} moe_status;
+
+typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_fn;
+typedef enum { MOE_PATH_AUTO = 0, MOE_PATH_PREFILL = 1, MOE_PATH_DECODE = 2 } moe_path;
+
+/* debug_flags bits (tests only; 0 in normal use) */
+#define MOE_DEBUG_SKIP_FIRST_LOAD 1u /* the FFN producer skips its first load, so the
+                                        consumer's bounded wait must give up and report
+                                        MOE_ERR_DEVICE_TIMEOUT (about 2 s)            */
+
+typedef struct {
+  int32_t T;          /* tokens                                                  */
+  int32_t H;          /* hidden size                                             */
+  int32_t n_experts;  /* original experts                                        */
+  int32_t n_sub;      /* sub-experts per expert (MoE-Prism's N); E_r = n_experts*n_sub */
+  int32_t I_sub;      /* intermediate size of one sub-expert (C / N)             */
+  int32_t k_max;      /* upper bound of every k_t; sizes the [T, k_max] outputs   */
+  moe_score_fn score; /* softmax over all units, or sigmoid                      */
+  int32_t renorm;     /* 1: divide the selected units' scores by their sum        */
+  float route_scale;  /* multiplies every gate weight                            */
+  const float* expert_bias;       /* nullable fp32 [n_experts], added to the logits
+                                     of the expert's n_sub units                  */
+  int32_t I_shared;               /* 0: no shared expert                         */
+  const void* w_shared_gate_up;   /* bf16 [2*I_shared, H] (gate rows, then up)   */
+  const void* w_shared_down;      /* bf16 [H, I_shared]                          */
+  moe_path path;                  /* reserved: AUTO/PREFILL/DECODE give the same
+                                     result; the library picks launch shapes     */
+  uint32_t debug_flags;           /* MOE_DEBUG_* bits, tests only                 */
+} moe_layer_desc;
+
+/* Bytes of workspace every call below needs for this desc (0 on a bad desc). */
+size_t moe_workspace_size(const moe_layer_desc* desc);
+
+/* Steps 1-3 of the layer: router logits, per-token top-k_t, gate weights.
+ * MoE-Prism §III-B2 (expanded linear gate scores every sub-expert and takes
+ * the top-k) with the per-request budget k_i of §III-C1.
+ *   x            bf16 [T, H]            (ignored when logits_in is given)
+ *   router_w     bf16 [E_r, H]          (ignored when logits_in is given)
+ *   logits_in    nullable fp32 [T, E_r]: route these logits instead of x.router_w
+ *   k_per_token  int32 [T], each in [1, k_max] (else MOE_ERR_K_RANGE on device;
+ *                the offending row is clamped into [0, k_max])
+ *   logits_out   nullable fp32 [T, E_r]: receives x.router_w^T + bias
+ *   topk_idx     int32 [T, k_max]: selected units, best first; -1 after k_t.
+ *                Order: logit descending, lower index first on ties, -0 == +0,
+ *                NaN last (and MOE_ERR_NONFINITE).
+ *   topk_w       fp32 [T, k_max]: gate weight of each selected unit, 0 after k_t.
+ *                softmax: exp(L_u - max L) / sum over ALL units; sigmoid:
+ *                1/(1+exp(-L_u)); renorm divides by the selected sum; then
+ *                times route_scale. */
+moe_status moe_route(const moe_layer_desc* desc, const void* x, const void* router_w,
+                     const float* logits_in, const int32_t* k_per_token, float* logits_out,
+                     int32_t* topk_idx, float* topk_w, int32_t* dev_status, void* workspace,
+                     void* stream);
+
+/* Step 4: group the assignments by routing unit (MoE-Prism §II-D: grouped
+ * GEMMs need one unit's rows contiguous).  Deterministic: unit ascending,
+ * token ascending inside a unit.
+ *   topk_idx, k_per_token  as produced by moe_route
+ *   counts        int32 [E_r]       assignments per unit
+ *   offsets       int32 [E_r + 1]   exclusive prefix sum of counts
+ *   sorted_token  int32 [T * k_max] token of each permuted row (first offsets[E_r] valid)
+ *   inv_row       int32 [T, k_max]  permuted row of assignment (t, j); -1 after k_t
+ * A unit index outside [0, E_r) or repeated within a token -> MOE_ERR_BAD_INDEX. */
+moe_status moe_permute(const moe_layer_desc* desc, const int32_t* topk_idx,
+                       const int32_t* k_per_token, int32_t* counts, int32_t* offsets,
+                       int32_t* sorted_token, int32_t* inv_row, int32_t* dev_status,
+                       void* workspace, void* stream);
+
+/* Step 5a: for every unit u, act[r] = SiLU(x_t Wg_u^T) * (x_t Wu_u^T) for the
+ * permuted rows r of u (t = sorted_token[r]).  MoE-Prism §III-B1 Eq. (1).
+ *   act  bf16 [T * k_max, I_sub]; rows >= offsets[E_r] are left untouched.
+ * Accumulation in fp32 on the tensor cores; act is rounded to bf16. */
+moe_status moe_gate_up(const moe_layer_desc* desc, const void* x, const int32_t* sorted_token,
+                       const int32_t* offsets, const void* w_gate_up, void* act,
+                       int32_t* dev_status, void* workspace, void* stream);
+
+/* Step 5b: y_perm[r] = act[r] Wd_u^T for the permuted rows r of unit u
+ * (MoE-Prism §III-B1 Eq. (1), X' = A Wdown).
+ *   y_perm  bf16 [T * k_max, H]; rows >= offsets[E_r] untouched. */
+moe_status moe_down(const moe_layer_desc* desc, const void* act, const int32_t* offsets,
+                    const void* w_down, void* y_perm, int32_t* dev_status, void* workspace,
+                    void* stream);
+
+/* Steps 5a + 5b with act kept in the workspace. */
+moe_status moe_grouped_ffn(const moe_layer_desc* desc, const void* x,
+                           const int32_t* sorted_token, const int32_t* offsets,
+                           const void* w_gate_up, const void* w_down, void* y_perm,
+                           int32_t* dev_status, void* workspace, void* stream);
+
+/* The always-on shared expert of every token (weight 1, not counted in k):
+ * y_shared = SwiGLU_shared(x), bf16 [T, H].  Requires desc->I_shared > 0. */
+moe_status moe_shared_ffn(const moe_layer_desc* desc, const void* x, void* y_shared,
+                          int32_t* dev_status, void* workspace, void* stream);
+
+/* Step 6: out_t = sum_{j < k_t} topk_w[t,j] * y_perm[inv_row[t,j]] (+ y_shared[t]),
+ * accumulated in fp32 in j order, rounded once to bf16 [T, H].
+ * MoE-Prism §III-B2: the routed output is sum_j w_j FFN_j(x). */
+moe_status moe_combine(const moe_layer_desc* desc, const void* y_perm, const void* y_shared,
+                       const int32_t* inv_row, const float* topk_w, const int32_t* k_per_token,
+                       void* out, int32_t* dev_status, void* stream);
+
+/* The whole layer: route -> permute -> [shared FFN] -> grouped FFN -> combine,
+ * every intermediate in the workspace.  out bf16 [T, H]. */
+moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, const void* router_w,
+                             const void* w_gate_up, const void* w_down,
+                             const int32_t* k_per_token, void* out, int32_t* dev_status,
+                             void* workspace, void* stream);
+
+/* Synchronises `stream`, then returns the code stored in *dev_status
+ * (MOE_OK if zero), or MOE_ERR_CUDA if the synchronisation itself failed. */
+moe_status moe_get_device_status(const int32_t* dev_status, void* stream);
+
+/* Static string naming a status code. */
+const char* moe_status_string(moe_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

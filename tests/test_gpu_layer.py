@@ -1,0 +1,116 @@
+"""End-to-end parity of moe_layer_forward on the five synthetic workloads.
+
+The GPU computes router logits in fp32 and the oracle in float64, so a token
+whose k-th and (k+1)-th logits nearly tie may legitimately select a
+different unit; such tokens must be genuine near ties (checked) and are left
+out of the element comparison.  Small workloads compare every token; the two
+large prefill workloads compare a seeded sample of tokens (the oracle runs
+on that sample: tokens are independent) plus properties that hold at any
+size (routing and permutation bit-exact from generator-given logits).
+"""
+import numpy as np
+import pytest
+import torch
+
+from aware_moe_expert_gb300 import binding as B
+from aware_moe_expert_gb300 import workloads as WL
+from aware_moe_expert_gb300.inputs import make_layer_inputs, make_logits, bf16_bits
+from oracle import moe_oracle as O
+from parity_utils import assert_close_layer, spec_of, unit_fetch, tie_safe_tokens
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _run_layer(wl, T=None):
+    wl = wl if T is None else wl.with_T(T)
+    d = make_layer_inputs(wl, DEV)
+    desc = B.desc_for(wl, expert_bias=d["expert_bias"], w_shared_gate_up=d.get("w_shared_gate_up"),
+                      w_shared_down=d.get("w_shared_down"))
+    layer = B.MoeLayer(desc, DEV)
+    out = layer.forward(d["x"], d["router_w"], d["w_gate_up"], d["w_down"], d["k_per_token"])
+    code = layer.device_status()
+    assert code == 0, B.STATUS_NAMES[code]
+    # the GPU's own logits and selection (same kernels as inside the layer)
+    Lg = torch.empty(wl.T, wl.E_r, dtype=torch.float32, device=DEV)
+    idx = torch.empty(wl.T, wl.k_max, dtype=torch.int32, device=DEV)
+    w = torch.empty(wl.T, wl.k_max, dtype=torch.float32, device=DEV)
+    B.check(B.moe_route(desc, d["x"], d["router_w"], None, d["k_per_token"], Lg, idx, w,
+                        layer.status, layer.workspace))
+    assert layer.device_status() == 0
+    return wl, d, desc, out, Lg, idx
+
+
+def _compare(wl, d, desc, out, Lg, idx, tokens):
+    tokens = np.asarray(tokens)
+    x_s = bf16_bits(d["x"][torch.as_tensor(tokens, device=DEV)])
+    k_s = d["k_per_token"].cpu().numpy()[tokens]
+    bias = None if d["expert_bias"] is None else d["expert_bias"].cpu().numpy()
+    spec = spec_of(desc, T=len(tokens))
+    ref = O.layer_forward(spec, x_s, bf16_bits(d["router_w"]), unit_fetch(d["w_gate_up"]),
+                          unit_fetch(d["w_down"]), k_s, expert_bias=bias,
+                          w_shared_gate_up=(bf16_bits(d["w_shared_gate_up"])
+                                            if wl.I_shared else None),
+                          w_shared_down=(bf16_bits(d["w_shared_down"]) if wl.I_shared else None))
+    L64 = ref["logits"]
+    Lg_s = Lg.cpu().numpy()[tokens].astype(np.float64)
+    delta = 2.0 * np.abs(Lg_s - L64).max(axis=1) + 1e-7
+    ok, n_tied = tie_safe_tokens(L64, idx.cpu().numpy()[tokens], k_s, delta)
+    assert n_tied <= max(2, len(tokens) // 100), f"{n_tied} near-tie tokens"
+    got = out.to(torch.float64).cpu().numpy()[tokens]
+    fro = assert_close_layer(got[ok], ref["out"][ok], wl.name)
+    return fro, n_tied
+
+
+@pytest.mark.parametrize("name", ["tiny", "mixtral_decode"])
+def test_layer_all_tokens(name):
+    wl, d, desc, out, Lg, idx = _run_layer(WL.ALL[name])
+    _compare(wl, d, desc, out, Lg, idx, np.arange(wl.T))
+
+
+@pytest.mark.parametrize("T", WL.QWEN_DECODE_T)
+def test_layer_qwen_decode_sweep(T):
+    wl, d, desc, out, Lg, idx = _run_layer(WL.QWEN_DECODE, T=T)
+    tokens = np.arange(T) if T <= 256 else np.random.default_rng(T).choice(T, 256, replace=False)
+    _compare(wl, d, desc, out, Lg, idx, np.sort(tokens))
+
+
+@pytest.mark.parametrize("name,n_sample", [("qwen_prefill", 96), ("deepseek_prefill", 24)])
+def test_layer_prefill_sampled(name, n_sample):
+    wl, d, desc, out, Lg, idx = _run_layer(WL.ALL[name])
+    rng = np.random.default_rng(12345)
+    tokens = np.sort(rng.choice(wl.T, n_sample, replace=False))
+    # always include the first and the last token (ragged tail of the batch)
+    tokens = np.unique(np.concatenate([[0, wl.T - 1], tokens]))
+    _compare(wl, d, desc, out, Lg, idx, tokens)
+
+
+@pytest.mark.parametrize("name", ["qwen_prefill", "deepseek_prefill"])
+def test_full_size_routing_and_permutation_bit_exact(name):
+    """At full size: top-k, gates and the permutation from generator-given
+    logits (the layer's own launch shapes for these steps)."""
+    wl = WL.ALL[name]
+    desc = B.desc_for(wl)
+    desc.I_shared = 0          # routing and permutation do not involve the shared expert
+    L = make_logits(wl.T, wl.E_r, DEV, seed=wl.seed)
+    from aware_moe_expert_gb300.inputs import draw_k
+    k = draw_k(wl, DEV)
+    ws = torch.empty(B.moe_workspace_size(desc), dtype=torch.uint8, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    idx = torch.empty(wl.T, wl.k_max, dtype=torch.int32, device=DEV)
+    w = torch.empty(wl.T, wl.k_max, dtype=torch.float32, device=DEV)
+    counts = torch.empty(wl.E_r, dtype=torch.int32, device=DEV)
+    offsets = torch.empty(wl.E_r + 1, dtype=torch.int32, device=DEV)
+    st_tok = torch.empty(wl.T * wl.k_max, dtype=torch.int32, device=DEV)
+    inv = torch.empty(wl.T * wl.k_max, dtype=torch.int32, device=DEV)
+    B.check(B.moe_route(desc, None, None, L, k, None, idx, w, st, ws))
+    B.check(B.moe_permute(desc, idx, k, counts, offsets, st_tok, inv, st, ws))
+    assert B.moe_get_device_status(st) == 0
+    Ln, kn = L.cpu().numpy(), k.cpu().numpy()
+    want_idx, _ = O.select_topk(Ln, kn, wl.k_max)
+    np.testing.assert_array_equal(idx.cpu().numpy(), want_idx)
+    wc, wo, wst, winv = O.permute(want_idx, kn, wl.E_r)
+    np.testing.assert_array_equal(offsets.cpu().numpy(), wo)
+    np.testing.assert_array_equal(st_tok.cpu().numpy()[: int(wo[-1])], wst)
+    np.testing.assert_array_equal(inv.cpu().numpy().reshape(wl.T, wl.k_max), winv)
+    assert int(wo[-1]) == int(kn.sum())

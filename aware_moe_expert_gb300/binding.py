@@ -23,6 +23,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARGUMENT", 2: "MOE_ERR_UNSUPPOR
                 3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_TIMEOUT",
                 6: "MOE_ERR_NONFINITE", 7: "MOE_ERR_K_RANGE", 8: "MOE_ERR_BAD_INDEX"}
 SCORE = {"softmax": 0, "sigmoid": 1}
+PATH_AUTO, PATH_PREFILL, PATH_DECODE = 0, 1, 2
 DEBUG_SKIP_FIRST_LOAD = 1
 
 EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_gate_up", "moe_down",
@@ -97,6 +98,7 @@ class LayerDesc:
     w_shared_gate_up: Optional[torch.Tensor] = None
     w_shared_down: Optional[torch.Tensor] = None
     debug_flags: int = 0
+    path: int = 0              # MOE_PATH_AUTO / PREFILL (1) / DECODE (2)
 
     @property
     def E_r(self) -> int:
@@ -113,7 +115,7 @@ class LayerDesc:
         d.I_shared = self.I_shared
         d.w_shared_gate_up = _ptr(self.w_shared_gate_up)
         d.w_shared_down = _ptr(self.w_shared_down)
-        d.path = 0
+        d.path = int(self.path)
         d.debug_flags = int(self.debug_flags)
         return d
 

@@ -23,8 +23,13 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 // Byte offsets of every workspace region for one desc.
 struct Layout {
   size_t logits, topk_idx, topk_w, counts, offsets, sorted_token, inv_row, bitmap, wprefix, xperm,
-      act, yperm, act_sh, ysh, total;
+      act, yperm, act_sh, ysh, split_word, partial, total;
+  int max_split;  // K splits the decode gate|up kernel may use (1: no partial buffer)
 };
+
+// Budget of the decode kernel's fp32 split-K partial buffer.
+constexpr size_t kPartialBudget = size_t(256) << 20;
+constexpr int kMaxSplit = 8;
 
 Layout layout_of(const moe_layer_desc& d) {
   const size_t T = static_cast<size_t>(d.T), E_r = static_cast<size_t>(d.n_experts) * d.n_sub;
@@ -50,6 +55,11 @@ Layout layout_of(const moe_layer_desc& d) {
   l.yperm = take(n_cap * d.H * 2);
   l.act_sh = take(T * static_cast<size_t>(d.I_shared) * 2);
   l.ysh = take(T * static_cast<size_t>(d.H) * 2);
+  l.split_word = take(16);
+  const size_t per_split = n_cap * 2 * static_cast<size_t>(d.I_sub) * 4;
+  size_t ms = per_split > 0 ? kPartialBudget / per_split : 1;
+  l.max_split = static_cast<int>(ms < 1 ? 1 : (ms > kMaxSplit ? kMaxSplit : ms));
+  l.partial = take(l.max_split > 1 ? l.max_split * per_split : 0);
   l.total = o;
   return l;
 }
@@ -118,6 +128,15 @@ inline moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK 
 
 inline int E_r_of(const moe_layer_desc* d) { return d->n_experts * d->n_sub; }
 
+// Decode-shaped batches (at most 64 rows per routing unit on average, from
+// the T * k_max bound) run the swap-AB kernels; desc->path forces either.
+bool use_decode_path(const moe_layer_desc* d, int n_out) {
+  if (!moe::decode_gemm_supports(n_out)) return false;
+  if (d->path == MOE_PATH_DECODE) return true;
+  if (d->path == MOE_PATH_PREFILL) return false;
+  return static_cast<long long>(d->T) * d->k_max <= 64ll * E_r_of(d);
+}
+
 // ---- the steps, without argument checks (callers check)
 
 moe_status do_route(const moe_layer_desc* d, const void* x, const void* router_w,
@@ -181,6 +200,28 @@ moe_status do_gate_up(const moe_layer_desc* d, const void* x, const int32_t* sor
   MOE_TRY(cuda_status(moe::launch_gather_rows(x, sorted_token, offsets, E_r, d->T, d->H,
                                               static_cast<int>(n_cap), xperm, status,
                                               sm_count(), s)));
+  if (use_decode_path(d, d->I_sub)) {
+    moe::DecodeGemmArgs a{};
+    a.gate_up = true;
+    a.w = w_gate_up;
+    a.w_rows = static_cast<long long>(E_r) * 2 * d->I_sub;
+    a.x = xperm;
+    a.x_rows = n_cap;
+    a.K = d->H;
+    a.offsets = offsets;
+    a.n_groups = E_r;
+    a.n_out = d->I_sub;
+    a.w_group_rows = 2 * d->I_sub;
+    a.out = act;
+    a.out_rows = n_cap;
+    a.partial = at<float>(ws, l.partial);
+    a.split_word = at<int32_t>(ws, l.split_word);
+    a.max_split = l.max_split;
+    a.status = status;
+    a.debug_flags = d->debug_flags;
+    a.sm_count = sm_count();
+    return cuda_status(moe::launch_decode_gemm(a, s));
+  }
   GemmArgs g{};
   g.epi = moe::EPI_SWIGLU;
   g.a = xperm;
@@ -207,6 +248,26 @@ moe_status do_down(const moe_layer_desc* d, const void* act, const int32_t* offs
   const int E_r = E_r_of(d);
   const long long n_cap = static_cast<long long>(d->T) * d->k_max;
   if (n_cap == 0) return MOE_OK;
+  if (use_decode_path(d, d->H)) {
+    moe::DecodeGemmArgs a{};
+    a.gate_up = false;
+    a.w = w_down;
+    a.w_rows = static_cast<long long>(E_r) * d->H;
+    a.x = act;
+    a.x_rows = n_cap;
+    a.K = d->I_sub;
+    a.offsets = offsets;
+    a.n_groups = E_r;
+    a.n_out = d->H;
+    a.w_group_rows = d->H;
+    a.out = y_perm;
+    a.out_rows = n_cap;
+    a.max_split = 1;
+    a.status = status;
+    a.debug_flags = 0;
+    a.sm_count = sm_count();
+    return cuda_status(moe::launch_decode_gemm(a, s));
+  }
   GemmArgs g{};
   g.epi = moe::EPI_BF16;
   g.a = act;

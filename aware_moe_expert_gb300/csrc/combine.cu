@@ -8,59 +8,73 @@
 namespace moe {
 namespace {
 
-// One warp per token; lanes stride over H in 16-byte (8 x bf16) vectors.
-// Lane j caches (row, weight) of slot j and broadcasts it in the j loop.
+__device__ __forceinline__ void fma8(float (&acc)[8], float w, uint4 y) {
+  const uint32_t yv[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    acc[2 * i] = fmaf(w, bf16lo(yv[i]), acc[2 * i]);
+    acc[2 * i + 1] = fmaf(w, bf16hi(yv[i]), acc[2 * i + 1]);
+  }
+}
+
+// One thread per (token, 16-byte column vector).  The k_t rows a thread
+// reads are independent, so they are loaded four at a time before they are
+// accumulated (in j order); the grid spans T * H/8 threads so enough loads
+// are in flight even for a handful of tokens.
 __global__ void __launch_bounds__(256) combine_kernel(
     const uint4* __restrict__ y_perm, const uint4* __restrict__ y_shared,
     const int32_t* __restrict__ inv_row, const float* __restrict__ topk_w,
     const int32_t* __restrict__ kpt, int T, int nv, int k_max, int n_rows,
     uint4* __restrict__ out, int32_t* status) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + warp;
+  const long long gid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int t = static_cast<int>(gid / nv);
+  const int v = static_cast<int>(gid - static_cast<long long>(t) * nv);
   if (t >= T) return;
   const int k = min(max(kpt[t], 0), k_max);
-  int my_r = -1;
-  float my_w = 0.f;
-  if (lane < k) {
-    my_r = inv_row[static_cast<size_t>(t) * k_max + lane];
-    my_w = topk_w[static_cast<size_t>(t) * k_max + lane];
-    if (my_r < 0 || my_r >= n_rows) {
-      report(status, MOE_ERR_BAD_INDEX);
-      my_r = -1;
-    }
-  }
-  for (int v = lane; v < nv; v += 32) {
-    float acc[8];
+  const int32_t* ir = inv_row + static_cast<size_t>(t) * k_max;
+  const float* tw = topk_w + static_cast<size_t>(t) * k_max;
+  float acc[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-    for (int j = 0; j < k; ++j) {
-      const int r = __shfl_sync(0xffffffffu, my_r, j);
-      const float w = __shfl_sync(0xffffffffu, my_w, j);
-      if (r < 0) continue;
-      const uint4 y = __ldg(y_perm + static_cast<size_t>(r) * nv + v);
-      const uint32_t yv[4] = {y.x, y.y, y.z, y.w};
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  bool bad = false;
+  for (int j0 = 0; j0 < k; j0 += 4) {
+    int r[4];
+    float w[4];
+    uint4 y[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        acc[2 * i] = fmaf(w, bf16lo(yv[i]), acc[2 * i]);
-        acc[2 * i + 1] = fmaf(w, bf16hi(yv[i]), acc[2 * i + 1]);
+    for (int q = 0; q < 4; ++q) {
+      const int j = j0 + q;
+      r[q] = j < k ? __ldg(ir + j) : -1;
+      w[q] = j < k ? __ldg(tw + j) : 0.f;
+      if (j < k && (r[q] < 0 || r[q] >= n_rows)) {
+        bad = true;
+        r[q] = -1;
       }
     }
-    if (y_shared != nullptr) {
-      const uint4 y = __ldg(y_shared + static_cast<size_t>(t) * nv + v);
-      const uint32_t yv[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        acc[2 * i] += bf16lo(yv[i]);
-        acc[2 * i + 1] += bf16hi(yv[i]);
-      }
-    }
-    uint4 o;
-    o.x = pack_bf16x2(acc[0], acc[1]);
-    o.y = pack_bf16x2(acc[2], acc[3]);
-    o.z = pack_bf16x2(acc[4], acc[5]);
-    o.w = pack_bf16x2(acc[6], acc[7]);
-    out[static_cast<size_t>(t) * nv + v] = o;
+    for (int q = 0; q < 4; ++q)
+      y[q] = r[q] >= 0 ? __ldg(y_perm + static_cast<size_t>(r[q]) * nv + v)
+                       : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (r[q] >= 0) fma8(acc, w[q], y[q]);
   }
+  if (bad && v == 0) report(status, MOE_ERR_BAD_INDEX);
+  if (y_shared != nullptr) {
+    const uint4 s = __ldg(y_shared + static_cast<size_t>(t) * nv + v);
+    const uint32_t sv[4] = {s.x, s.y, s.z, s.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc[2 * i] += bf16lo(sv[i]);
+      acc[2 * i + 1] += bf16hi(sv[i]);
+    }
+  }
+  uint4 o;
+  o.x = pack_bf16x2(acc[0], acc[1]);
+  o.y = pack_bf16x2(acc[2], acc[3]);
+  o.z = pack_bf16x2(acc[4], acc[5]);
+  o.w = pack_bf16x2(acc[6], acc[7]);
+  out[static_cast<size_t>(t) * nv + v] = o;
 }
 
 }  // namespace
@@ -69,7 +83,8 @@ cudaError_t launch_combine(const void* y_perm, const void* y_shared, const int32
                            const float* topk_w, const int32_t* k_per_token, int T, int H,
                            int k_max, int n_rows, void* out, int32_t* status, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  combine_kernel<<<(T + 7) / 8, 256, 0, s>>>(
+  const long long threads = static_cast<long long>(T) * (H / 8);
+  combine_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(
       static_cast<const uint4*>(y_perm), static_cast<const uint4*>(y_shared), inv_row, topk_w,
       k_per_token, T, H / 8, k_max, n_rows, static_cast<uint4*>(out), status);
   return cudaGetLastError();

@@ -31,17 +31,19 @@
 
 #include <mutex>
 
-#include "moe_common.cuh"
+#include "gemm_common.cuh"
 #include "moe_internal.h"
 
 namespace moe {
+
+bool make_tmap_bf16(CUtensorMap* m, const void* base, long long rows, int cols, int box_rows);
+
 namespace {
 
-constexpr int BM = 128;
+constexpr int BM = kTileRows;
 constexpr int BK = 64;
 constexpr int kThreads = 192;
 constexpr uint32_t kABytes = BM * BK * 2;
-constexpr int kMaxGroups = 256;
 
 struct KParams {
   const int32_t* offsets;
@@ -84,37 +86,6 @@ struct Cfg {
   static_assert(BN_MMA % 16 == 0 && BN_MMA >= 16 && BN_MMA <= 256, "tcgen05 N for M = 128");
 };
 
-struct Tile {
-  int g, row0, rows, nt;
-};
-
-__device__ __forceinline__ Tile decode_tile(int w, int n_tiles, int n_groups, const int* prefix,
-                                            const int* offs) {
-  Tile t;
-  const int mt = w / n_tiles;
-  t.nt = w - mt * n_tiles;
-  // largest g in [0, n_groups) with prefix[g] <= mt
-  int lo = 0, hi = n_groups;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (prefix[mid] <= mt)
-      lo = mid;
-    else
-      hi = mid;
-  }
-  t.g = lo;
-  t.row0 = offs[lo] + (mt - prefix[lo]) * BM;
-  t.rows = min(BM, offs[lo + 1] - t.row0);
-  return t;
-}
-
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
-
-__device__ __forceinline__ void fail(volatile int* abort, int32_t* status) {
-  *abort = 1;
-  report(status, MOE_ERR_DEVICE_TIMEOUT);
-}
-
 template <int BN_MMA, int EPI, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -154,57 +125,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
   }
-  if (warp == 2) {
-    // m-tile table: s_prefix[g] = first m-tile of group g, s_offs = row offsets
-    if (p.offsets == nullptr) {
-      if (lane == 0) {
-        s_offs[0] = 0;
-        s_offs[1] = p.dense_rows;
-        s_prefix[0] = 0;
-        s_prefix[1] = (p.dense_rows + BM - 1) / BM;
-        *s_total = s_prefix[1];
-      }
-    } else {
-      const int G = p.n_groups;
-      const int per = (G + 31) / 32;
-      const int g0 = lane * per;
-      int local = 0;
-      bool bad = false;
-      for (int i = 0; i < per; ++i) {
-        const int g = g0 + i;
-        if (g < G) {
-          const int a = p.offsets[g], b = p.offsets[g + 1];
-          bad |= (a < 0) || (b < a);
-          s_offs[g] = a;
-          local += b > a ? (b - a + BM - 1) / BM : 0;
-        }
-      }
-      int incl = local;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
-      }
-      int run = incl - local;
-      for (int i = 0; i < per; ++i) {
-        const int g = g0 + i;
-        if (g < G) {
-          s_prefix[g] = run;
-          const int a = p.offsets[g], b = p.offsets[g + 1];
-          run += b > a ? (b - a + BM - 1) / BM : 0;
-        }
-      }
-      if (lane == 31) {
-        const int last = p.offsets[G];
-        bad |= static_cast<long long>(last) > p.out_rows;
-        s_offs[G] = last;
-        s_prefix[G] = incl;
-      }
-      bad = __any_sync(0xffffffffu, bad);
-      if (lane == 31) *s_total = bad ? 0 : incl;
-      if (bad && lane == 0) report(p.status, MOE_ERR_BAD_INDEX);
-    }
-  }
+  if (warp == 2) build_tile_table(p.offsets, p.n_groups, p.dense_rows, p.out_rows, s_prefix, s_offs,
+                                  s_total, p.status, lane);
   if (warp == 1) {
     tmem_alloc(s_tmem, C::kTmemCols);
     tmem_relinquish();
@@ -417,42 +339,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  });
-  return fn;
-}
-
-// bf16 [rows, cols] row-major, box = 64 columns x box_rows rows, 128-B swizzle.
-bool make_tmap(CUtensorMap* m, const void* base, long long rows, int cols, int box_rows) {
-  auto fn = encode_fn();
-  if (fn == nullptr || rows <= 0) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
-  cuuint32_t estr[2] = {1, 1};
-  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 template <int BN_MMA, int EPI, int STAGES>
 cudaError_t run_gemm(const GemmArgs& g, cudaStream_t s) {
   using C = Cfg<BN_MMA, STAGES>;
   const int box_b = EPI == EPI_SWIGLU ? BN_MMA / 2 : BN_MMA;
   CUtensorMap ta, tb;
-  if (!make_tmap(&ta, g.a, g.a_rows, g.K, BM)) return cudaErrorInvalidValue;
-  if (!make_tmap(&tb, g.b, g.b_rows, g.K, box_b)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&ta, g.a, g.a_rows, g.K, BM)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&tb, g.b, g.b_rows, g.K, box_b)) return cudaErrorInvalidValue;
   KParams kp;
   kp.offsets = g.offsets;
   kp.n_groups = g.offsets == nullptr ? 1 : g.n_groups;
@@ -479,14 +372,53 @@ cudaError_t run_gemm(const GemmArgs& g, cudaStream_t s) {
   if (work <= 0) return cudaSuccess;
   const int grid = static_cast<int>(work < g.sm_count ? work : g.sm_count);
   auto kern = grouped_gemm_kernel<BN_MMA, EPI, STAGES>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(C::kSmemBytes));
+  // The shared-memory opt-in is set once per device, so that launches made
+  // while a stream is being captured into a CUDA graph issue no other call.
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_done[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(C::kSmemBytes));
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
   kern<<<grid, kThreads, C::kSmemBytes, s>>>(ta, tb, kp);
   return cudaGetLastError();
 }
 
 }  // namespace
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// bf16 [rows, cols] row-major, box = 64 columns x box_rows rows, 128-B swizzle.
+bool make_tmap_bf16(CUtensorMap* m, const void* base, long long rows, int cols, int box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr || rows <= 0) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
 
 bool gemm_supports_f32_router(int E_r) { return E_r == 64 || E_r == 128 || E_r == 256; }
 

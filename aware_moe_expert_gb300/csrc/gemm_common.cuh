@@ -1,0 +1,101 @@
+// Pieces shared by the grouped GEMM kernels: the m-tile table built from the
+// unit offsets, tile decoding, SiLU, and the timeout report.
+#pragma once
+
+#include "moe_common.cuh"
+
+namespace moe {
+
+constexpr int kTileRows = 128;   // rows of one m-tile (tokens of one unit)
+constexpr int kMaxGroups = 256;
+
+struct Tile {
+  int g, row0, rows, nt;
+};
+
+__device__ __forceinline__ Tile decode_tile(int w, int n_tiles, int n_groups, const int* prefix,
+                                            const int* offs) {
+  Tile t;
+  const int mt = w / n_tiles;
+  t.nt = w - mt * n_tiles;
+  // largest g in [0, n_groups) with prefix[g] <= mt
+  int lo = 0, hi = n_groups;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (prefix[mid] <= mt)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  t.g = lo;
+  t.row0 = offs[lo] + (mt - prefix[lo]) * kTileRows;
+  t.rows = min(kTileRows, offs[lo + 1] - t.row0);
+  return t;
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
+__device__ __forceinline__ void fail(volatile int* abort, int32_t* status) {
+  *abort = 1;
+  report(status, MOE_ERR_DEVICE_TIMEOUT);
+}
+
+
+// Built by one warp: s_prefix[g] = first m-tile of group g (s_prefix[G] =
+// total), s_offs = row offsets, *s_total = number of m-tiles.  offsets ==
+// nullptr means one dense group of dense_rows rows.  Offsets that decrease,
+// are negative, or end past out_rows are reported (MOE_ERR_BAD_INDEX) and
+// give zero tiles.
+__device__ __forceinline__ void build_tile_table(const int32_t* offsets, int G, int dense_rows,
+                                                 long long out_rows, int* s_prefix, int* s_offs,
+                                                 int* s_total, int32_t* status, int lane) {
+  if (offsets == nullptr) {
+    if (lane == 0) {
+      s_offs[0] = 0;
+      s_offs[1] = dense_rows;
+      s_prefix[0] = 0;
+      s_prefix[1] = (dense_rows + kTileRows - 1) / kTileRows;
+      *s_total = s_prefix[1];
+    }
+    return;
+  }
+  const int per = (G + 31) / 32;
+  const int g0 = lane * per;
+  int local = 0;
+  bool bad = false;
+  for (int i = 0; i < per; ++i) {
+    const int g = g0 + i;
+    if (g < G) {
+      const int a = offsets[g], b = offsets[g + 1];
+      bad |= (a < 0) || (b < a);
+      s_offs[g] = a;
+      local += b > a ? (b - a + kTileRows - 1) / kTileRows : 0;
+    }
+  }
+  int incl = local;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  int run = incl - local;
+  for (int i = 0; i < per; ++i) {
+    const int g = g0 + i;
+    if (g < G) {
+      s_prefix[g] = run;
+      const int a = offsets[g], b = offsets[g + 1];
+      run += b > a ? (b - a + kTileRows - 1) / kTileRows : 0;
+    }
+  }
+  if (lane == 31) {
+    const int last = offsets[G];
+    bad |= static_cast<long long>(last) > out_rows;
+    s_offs[G] = last;
+    s_prefix[G] = incl;
+  }
+  bad = __any_sync(0xffffffffu, bad);
+  if (lane == 31) *s_total = bad ? 0 : incl;
+  if (bad && lane == 0) report(status, MOE_ERR_BAD_INDEX);
+}
+
+}  // namespace moe

@@ -59,6 +59,35 @@ struct GemmArgs {
 };
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s);
+
+// ---- gemm_decode.cu
+struct DecodeGemmArgs {
+  bool gate_up;              // true: gate|up + SwiGLU; false: down
+  const void* w;             // bf16 weights [w_rows, K]
+  long long w_rows;
+  const void* x;             // bf16 rows [x_rows, K] (x_perm or act)
+  long long x_rows;
+  int K;
+  const int32_t* offsets;    // [n_groups + 1]
+  int n_groups;
+  int n_out;                 // gate|up: I_sub; down: H (multiple of 128)
+  int w_group_rows;          // gate|up: 2 I_sub; down: H
+  void* out;                 // bf16 [out_rows, n_out]
+  long long out_rows;
+  float* partial;            // fp32 [max_split][out_rows][2 n_out] (gate|up, max_split > 1)
+  int32_t* split_word;
+  int max_split;
+  int32_t* status;
+  uint32_t debug_flags;
+  int sm_count;
+};
+
+cudaError_t launch_decode_gemm(const DecodeGemmArgs& a, cudaStream_t s);
+bool decode_gemm_supports(int n_out);
+
+// bf16 [rows, cols] row-major tensor map: box of 64 columns x box_rows rows,
+// 128-byte swizzle, zero fill out of bounds.
+bool make_tmap_bf16(CUtensorMap* m, const void* base, long long rows, int cols, int box_rows);
 bool gemm_supports_f32_router(int E_r);
 
 }  // namespace moe

@@ -154,6 +154,92 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
   }
 }
 
+// Decode-sized batches in one CTA (1024 threads): bitmap, word prefixes,
+// offsets and scatter all in shared memory (W = ceil(T/32) <= 32 words per
+// unit).  Same result as bitmap_kernel + scan_kernel + scatter_kernel.
+__global__ void __launch_bounds__(1024) permute_small_kernel(
+    const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ kpt, int T, int k_max,
+    int E_r, int W, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ sorted_token, int32_t* __restrict__ inv_row, int32_t* status) {
+  extern __shared__ uint32_t sm[];
+  uint32_t* bits = sm;
+  int32_t* pre = reinterpret_cast<int32_t*>(sm + E_r * W);
+  int32_t* s_cnt = pre + E_r * W;
+  int32_t* s_off = s_cnt + 256;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int i = tid; i < E_r * W; i += blockDim.x) bits[i] = 0u;
+  __syncthreads();
+  const int slots = T * k_max;
+  for (int i = tid; i < slots; i += blockDim.x) {
+    const int t = i / k_max, j = i - (i / k_max) * k_max;
+    int k = kpt[t];
+    if (k < 1 || k > k_max) {
+      if (j == 0) report(status, MOE_ERR_K_RANGE);
+      k = min(max(k, 0), k_max);
+    }
+    if (j >= k) continue;
+    const int u = topk_idx[i];
+    if (u < 0 || u >= E_r) {
+      report(status, MOE_ERR_BAD_INDEX);
+      continue;
+    }
+    const uint32_t bit = 1u << (t & 31);
+    if (atomicOr(&bits[u * W + (t >> 5)], bit) & bit) report(status, MOE_ERR_BAD_INDEX);
+  }
+  __syncthreads();
+  for (int u = warp; u < E_r; u += 32) {
+    const int c = lane < W ? __popc(bits[u * W + lane]) : 0;
+    int incl = c;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    if (lane < W) pre[u * W + lane] = incl - c;
+    if (lane == 31) s_cnt[u] = incl;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int per = (E_r + 31) / 32;
+    const int u0 = lane * per;
+    int local = 0;
+    for (int i = 0; i < per; ++i)
+      if (u0 + i < E_r) local += s_cnt[u0 + i];
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    int run = incl - local;
+    for (int i = 0; i < per; ++i) {
+      const int u = u0 + i;
+      if (u < E_r) {
+        s_off[u] = run;
+        offsets[u] = run;
+        counts[u] = s_cnt[u];
+        run += s_cnt[u];
+      }
+    }
+    if (lane == 31) offsets[E_r] = incl;
+  }
+  __syncthreads();
+  for (int i = tid; i < slots; i += blockDim.x) {
+    const int t = i / k_max, j = i - (i / k_max) * k_max;
+    const int k = min(max(kpt[t], 0), k_max);
+    int pos = -1;
+    if (j < k) {
+      const int u = topk_idx[i];
+      if (u >= 0 && u < E_r) {
+        const int o = u * W + (t >> 5);
+        pos = s_off[u] + pre[o] + __popc(bits[o] & ((1u << (t & 31)) - 1u));
+        sorted_token[pos] = t;
+      }
+    }
+    inv_row[i] = pos;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_permute(const int32_t* topk_idx, const int32_t* k_per_token, int T,
@@ -161,6 +247,23 @@ cudaError_t launch_permute(const int32_t* topk_idx, const int32_t* k_per_token, 
                            int32_t* counts, int32_t* offsets, int32_t* sorted_token,
                            int32_t* inv_row, int32_t* status, cudaStream_t s) {
   const int W = (T + 31) / 32;
+  if (W > 0 && W <= 32 && E_r * W <= 8192) {
+    const int smem = (2 * E_r * W + 256 + 257) * 4;
+    static bool attr_done[64] = {false};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_done[dev]) {
+      e = cudaFuncSetAttribute(permute_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (2 * 8192 + 256 + 257) * 4);
+      if (e != cudaSuccess) return e;
+      attr_done[dev] = true;
+    }
+    permute_small_kernel<<<1, 1024, smem, s>>>(topk_idx, k_per_token, T, k_max, E_r, W, counts,
+                                                offsets, sorted_token, inv_row, status);
+    return cudaGetLastError();
+  }
   if (W > 0) {
     bitmap_kernel<<<W, 256, 0, s>>>(topk_idx, k_per_token, T, k_max, E_r, W, bitmap, status);
   }

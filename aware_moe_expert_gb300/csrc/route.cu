@@ -39,14 +39,22 @@ __global__ void __launch_bounds__(256) router_logits_small_kernel(
   for (int i = 0; i < kTokPerCta; ++i) acc[i] = 0.f;
   const uint4* wrow = reinterpret_cast<const uint4*>(rw + static_cast<size_t>(u) * H);
   const int nv = H / 8;
-  for (int v = lane; v < nv; v += 32) {
-    const uint4 wv = __ldg(wrow + v);
+  // four 16-byte vectors per lane per pass, all loads issued before the math
+  for (int v0 = lane; v0 < nv; v0 += 128) {
+    uint4 wv[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      wv[q] = v0 + 32 * q < nv ? __ldg(wrow + v0 + 32 * q) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
     for (int i = 0; i < kTokPerCta; ++i) {
       if (i < nt) {
-        const uint4 xv =
-            __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(t0 + i) * H) + v);
-        acc[i] = dot8_bf16(xv, wv, acc[i]);
+        const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t0 + i) * H);
+        uint4 xv[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          xv[q] = v0 + 32 * q < nv ? __ldg(xr + v0 + 32 * q) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[i] = dot8_bf16(xv[q], wv[q], acc[i]);
       }
     }
   }

@@ -171,31 +171,39 @@ def run_ours(args, wl, rank, world, local):
     stream = torch.cuda.Stream(device=dev)
     sp = stream.cuda_stream
 
-    def step(ev=None):
-        def rec(i):
-            if ev is not None:
-                ev[i].record(stream)
-        rec(0)
+    def call_route(sp):
         B.check(B.moe_route(desc, d["x"], d["router_w"], None, d["k_per_token"], None, idx, w,
                             st, ws, sp), "moe_route")
-        rec(1)
+
+    def call_permute(sp):
         B.check(B.moe_permute(desc, idx, d["k_per_token"], counts, offsets, st_tok, inv, st, ws,
                               sp), "moe_permute")
-        rec(2)
-        if ysh is not None:
-            B.check(B.moe_shared_ffn(desc, d["x"], ysh, st, ws, sp), "moe_shared_ffn")
-        rec(3)
+
+    def call_shared(sp):
+        B.check(B.moe_shared_ffn(desc, d["x"], ysh, st, ws, sp), "moe_shared_ffn")
+
+    def call_gate_up(sp):
         B.check(B.moe_gate_up(desc, d["x"], st_tok, offsets, d["w_gate_up"], act, st, ws, sp),
                 "moe_gate_up")
-        rec(4)
-        B.check(B.moe_down(desc, act, offsets, d["w_down"], y, st, ws, sp), "moe_down")
-        rec(5)
-        B.check(B.moe_combine(desc, y, ysh, inv, w, d["k_per_token"], out, st, sp), "moe_combine")
-        rec(6)
 
-    # realised routing statistics (one untimed pass)
+    def call_down(sp):
+        B.check(B.moe_down(desc, act, offsets, d["w_down"], y, st, ws, sp), "moe_down")
+
+    def call_combine(sp):
+        B.check(B.moe_combine(desc, y, ysh, inv, w, d["k_per_token"], out, st, sp), "moe_combine")
+
+    calls = [("route", call_route), ("permute", call_permute)]
+    if ysh is not None:
+        calls.append(("shared_ffn", call_shared))
+    calls += [("gate_up", call_gate_up), ("down", call_down), ("combine", call_combine)]
+
+    def step(sp):
+        for _, f in calls:
+            f(sp)
+
+    # one eager pass: realised routing statistics, per-device set-up
     with torch.cuda.stream(stream):
-        step()
+        step(sp)
     torch.cuda.synchronize(dev)
     code = B.moe_get_device_status(st, sp)
     if code != 0:
@@ -204,6 +212,17 @@ def run_ours(args, wl, rank, world, local):
     n_assign = int(cnt.sum())
     D = int(np.count_nonzero(cnt))
 
+    # The step is replayed from CUDA graphs so that the device timeline is
+    # not stretched by host enqueue time: one graph of the whole step (the
+    # timed value) and one graph per call (the per-call breakdown).
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+            fn(torch.cuda.current_stream().cuda_stream)
+        return g
+    g_full = capture(step)
+    g_parts = [(n, capture(f)) for n, f in calls]
+
     # L2 handling: flush with a 2x-L2 write between steps unless the step
     # streams far more than L2 anyway.
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -211,13 +230,19 @@ def run_ours(args, wl, rank, world, local):
     flush = w_active < 4 * l2
     flush_buf = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev) if flush else None
 
-    n_ev = 7
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
-    for _ in range(args.warmup):
+    def maybe_flush():
         if flush:
-            with torch.cuda.stream(stream):
-                flush_buf.zero_()
-        step()
+            flush_buf.zero_()
+
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    n_parts = len(g_parts)
+    evp = [[torch.cuda.Event(enable_timing=True) for _ in range(n_parts + 1)]
+           for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            maybe_flush()
+            g_full.replay()
     torch.cuda.synchronize(dev)
     if world > 1:
         import torch.distributed as dist
@@ -227,31 +252,49 @@ def run_ours(args, wl, rank, world, local):
     os.makedirs(os.path.dirname(smi_path), exist_ok=True)
     with ClockSampler(local, smi_path) as cs:
         t_wall0 = time.perf_counter()
-        for i in range(args.steps):
-            if flush:
-                with torch.cuda.stream(stream):
-                    flush_buf.zero_()
-            step(evs[i])
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                maybe_flush()
+                ev0[i].record(stream)
+                g_full.replay()
+                ev1[i].record(stream)
         torch.cuda.synchronize(dev)
         t_wall = time.perf_counter() - t_wall0
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
-    torch.cuda.synchronize(dev)
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        # per-call breakdown, same number of steps
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                maybe_flush()
+                evp[i][0].record(stream)
+                for j, (_, g) in enumerate(g_parts):
+                    g.replay()
+                    evp[i][j + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        # identical untimed steps so that the clock record covers >= ~1.5 s of load
+        t_extra = time.perf_counter()
+        with torch.cuda.stream(stream):
+            while time.perf_counter() - t_extra < 1.5:
+                for _ in range(20):
+                    maybe_flush()
+                    g_full.replay()
+                torch.cuda.synchronize(dev)
     code = B.moe_get_device_status(st, sp)
     if code != 0:
         raise RuntimeError(f"device status {B.STATUS_NAMES.get(code, code)}")
-    per = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(n_ev - 1)]
-                    for i in range(args.steps)])  # ms
-    step_ms = per.sum(axis=1)
+    step_ms = np.array([ev0[i].elapsed_time(ev1[i]) for i in range(args.steps)])
     ms = float(step_ms.mean())
     if world > 1:
         import torch.distributed as dist
         tt = torch.tensor([ms], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         ms = float(tt.item())
-    parts = {n: float(per[:, j].mean() * 1000.0) for j, n in
-             enumerate(["route", "permute", "shared_ffn", "gate_up", "down", "combine"])}
+    per = np.array([[evp[i][j].elapsed_time(evp[i][j + 1]) for j in range(n_parts)]
+                    for i in range(args.steps)])
+    parts = {n: float(per[:, j].mean() * 1000.0) for j, (n, _) in enumerate(g_parts)}
+    del g_full, g_parts
 
     # end to end through the public call with host buffers
     e2e = None

@@ -30,14 +30,19 @@ def _weights(E_r, H, I_sub, n_sub, seed):
     return x, wgu, wd
 
 
+@pytest.mark.parametrize("path", [B.PATH_PREFILL, B.PATH_DECODE])
 @pytest.mark.parametrize("T,H,n_experts,n_sub,I_sub,k_max,skew", [
     (64, 256, 16, 4, 128, 8, 0.0),      # tiny layer shape
     (300, 512, 8, 1, 192, 4, 3.0),      # 3 m-tiles on hot units, I_sub % 128 != 0
     (257, 384, 4, 2, 256, 3, 0.0),      # H % 256 != 0 (down uses 128-wide tiles)
     (130, 320, 6, 1, 64, 2, 6.0),       # H % 128 != 0 (64-wide tiles), empty units
-    (1, 2048, 128, 2, 384, 16, 0.0),    # one token
+    (1, 2048, 128, 2, 384, 16, 0.0),    # one token (decode: split-K over few items)
+    (8, 2048, 128, 2, 384, 16, 0.0),    # eight tokens
+    (400, 512, 4, 2, 256, 4, 4.0),      # > 128 rows on a unit: decode chunks of 128 tokens
 ])
-def test_grouped_ffn_rows_match_oracle(T, H, n_experts, n_sub, I_sub, k_max, skew):
+def test_grouped_ffn_rows_match_oracle(T, H, n_experts, n_sub, I_sub, k_max, skew, path):
+    """Both kernel families (prefill tiles, decode swap-AB) on the same inputs;
+    shapes a family does not support fall back to the other one."""
     E_r = n_experts * n_sub
     x, wgu, wd = _weights(E_r, H, I_sub, n_sub, seed=T * 31 + H)
     x = x[:T].contiguous()
@@ -46,7 +51,8 @@ def test_grouped_ffn_rows_match_oracle(T, H, n_experts, n_sub, I_sub, k_max, ske
         L = L + (-skew * torch.log(torch.arange(1, E_r + 1, device=DEV, dtype=torch.float32)))
     g = torch.Generator().manual_seed(T)
     k = torch.randint(1, k_max + 1, (T,), generator=g, dtype=torch.int32).to(DEV)
-    desc = B.LayerDesc(T=T, H=H, n_experts=n_experts, n_sub=n_sub, I_sub=I_sub, k_max=k_max)
+    desc = B.LayerDesc(T=T, H=H, n_experts=n_experts, n_sub=n_sub, I_sub=I_sub, k_max=k_max,
+                       path=path)
     ws = torch.empty(B.moe_workspace_size(desc), dtype=torch.uint8, device=DEV)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
     idx = torch.empty(T, k_max, dtype=torch.int32, device=DEV)

@@ -22,11 +22,12 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def _run_layer(wl, T=None):
+def _run_layer(wl, T=None, path=B.PATH_AUTO):
     wl = wl if T is None else wl.with_T(T)
     d = make_layer_inputs(wl, DEV)
     desc = B.desc_for(wl, expert_bias=d["expert_bias"], w_shared_gate_up=d.get("w_shared_gate_up"),
                       w_shared_down=d.get("w_shared_down"))
+    desc.path = path
     layer = B.MoeLayer(desc, DEV)
     out = layer.forward(d["x"], d["router_w"], d["w_gate_up"], d["w_down"], d["k_per_token"])
     code = layer.device_status()
@@ -65,6 +66,14 @@ def _compare(wl, d, desc, out, Lg, idx, tokens):
 @pytest.mark.parametrize("name", ["tiny", "mixtral_decode"])
 def test_layer_all_tokens(name):
     wl, d, desc, out, Lg, idx = _run_layer(WL.ALL[name])
+    _compare(wl, d, desc, out, Lg, idx, np.arange(wl.T))
+
+
+@pytest.mark.parametrize("path", [B.PATH_PREFILL, B.PATH_DECODE])
+@pytest.mark.parametrize("name,T", [("tiny", None), ("qwen_decode", 64), ("mixtral_decode", None)])
+def test_layer_both_gemm_paths(name, T, path):
+    """The prefill-tile and decode swap-AB kernels both match the oracle."""
+    wl, d, desc, out, Lg, idx = _run_layer(WL.ALL[name], T=T, path=path)
     _compare(wl, d, desc, out, Lg, idx, np.arange(wl.T))
 
 

@@ -24,7 +24,8 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 struct Layout {
   size_t logits, topk_idx, topk_w, counts, offsets, sorted_token, inv_row, bitmap, wprefix, xperm,
       act, yperm, act_sh, ysh, split_word, partial, total;
-  int max_split;  // K splits the decode gate|up kernel may use (1: no partial buffer)
+  int max_split;       // K splits the decode gate|up kernel may use (1: none)
+  int max_split_down;  // K splits the decode down kernel may use
 };
 
 // Budget of the decode kernel's fp32 split-K partial buffer.
@@ -56,10 +57,17 @@ Layout layout_of(const moe_layer_desc& d) {
   l.act_sh = take(T * static_cast<size_t>(d.I_shared) * 2);
   l.ysh = take(T * static_cast<size_t>(d.H) * 2);
   l.split_word = take(16);
-  const size_t per_split = n_cap * 2 * static_cast<size_t>(d.I_sub) * 4;
-  size_t ms = per_split > 0 ? kPartialBudget / per_split : 1;
-  l.max_split = static_cast<int>(ms < 1 ? 1 : (ms > kMaxSplit ? kMaxSplit : ms));
-  l.partial = take(l.max_split > 1 ? l.max_split * per_split : 0);
+  auto splits = [](size_t per_split) {
+    size_t ms = per_split > 0 ? kPartialBudget / per_split : 1;
+    return static_cast<int>(ms < 1 ? 1 : (ms > kMaxSplit ? kMaxSplit : ms));
+  };
+  const size_t per_gu = n_cap * 2 * static_cast<size_t>(d.I_sub) * 4;
+  const size_t per_dn = n_cap * static_cast<size_t>(d.H) * 4;
+  l.max_split = splits(per_gu);
+  l.max_split_down = splits(per_dn);
+  const size_t need_gu = l.max_split > 1 ? l.max_split * per_gu : 0;
+  const size_t need_dn = l.max_split_down > 1 ? l.max_split_down * per_dn : 0;
+  l.partial = take(need_gu > need_dn ? need_gu : need_dn);
   l.total = o;
   return l;
 }
@@ -78,6 +86,7 @@ moe_status validate(const moe_layer_desc* d) {
     return MOE_ERR_INVALID_ARGUMENT;
   const long long E_r = static_cast<long long>(d->n_experts) * d->n_sub;
   if (d->H % 64 != 0 || d->I_sub % 64 != 0 || d->I_shared % 64 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (d->H > 49152) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (E_r > 256 || d->k_max > E_r || d->k_max > 32) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (static_cast<long long>(d->T) * d->k_max > (1ll << 30)) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (d->I_shared > 0 && (d->w_shared_gate_up == nullptr || d->w_shared_down == nullptr))
@@ -244,7 +253,7 @@ moe_status do_gate_up(const moe_layer_desc* d, const void* x, const int32_t* sor
 }
 
 moe_status do_down(const moe_layer_desc* d, const void* act, const int32_t* offsets,
-                   const void* w_down, void* y_perm, int32_t* status, cudaStream_t s) {
+                   const void* w_down, void* y_perm, int32_t* status, void* ws, cudaStream_t s) {
   const int E_r = E_r_of(d);
   const long long n_cap = static_cast<long long>(d->T) * d->k_max;
   if (n_cap == 0) return MOE_OK;
@@ -260,9 +269,12 @@ moe_status do_down(const moe_layer_desc* d, const void* act, const int32_t* offs
     a.n_groups = E_r;
     a.n_out = d->H;
     a.w_group_rows = d->H;
+    const Layout l = layout_of(*d);
     a.out = y_perm;
     a.out_rows = n_cap;
-    a.max_split = 1;
+    a.partial = at<float>(ws, l.partial);
+    a.split_word = at<int32_t>(ws, l.split_word) + 1;
+    a.max_split = l.max_split_down;
     a.status = status;
     a.debug_flags = 0;
     a.sm_count = sm_count();
@@ -399,12 +411,12 @@ moe_status moe_gate_up(const moe_layer_desc* desc, const void* x, const int32_t*
 moe_status moe_down(const moe_layer_desc* desc, const void* act, const int32_t* offsets,
                     const void* w_down, void* y_perm, int32_t* dev_status, void* workspace,
                     void* stream) {
-  (void)workspace;
   MOE_TRY(validate(desc));
   if (desc->T == 0) return MOE_OK;
   MOE_TRY(check_ptrs({act, w_down, y_perm}));
   MOE_TRY(check_ptrs4({offsets, dev_status}));
-  return do_down(desc, act, offsets, w_down, y_perm, dev_status,
+  MOE_TRY(check_ws(workspace));
+  return do_down(desc, act, offsets, w_down, y_perm, dev_status, workspace,
                  static_cast<cudaStream_t>(stream));
 }
 
@@ -420,7 +432,7 @@ moe_status moe_grouped_ffn(const moe_layer_desc* desc, const void* x,
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   void* act = at<void>(workspace, layout_of(*desc).act);
   MOE_TRY(do_gate_up(desc, x, sorted_token, offsets, w_gate_up, act, dev_status, workspace, s));
-  return do_down(desc, act, offsets, w_down, y_perm, dev_status, s);
+  return do_down(desc, act, offsets, w_down, y_perm, dev_status, workspace, s);
 }
 
 moe_status moe_shared_ffn(const moe_layer_desc* desc, const void* x, void* y_shared,
@@ -472,7 +484,7 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, const vo
                      dev_status, workspace, s));
   if (ysh != nullptr) MOE_TRY(do_shared(desc, x, ysh, dev_status, workspace, s));
   MOE_TRY(do_gate_up(desc, x, sorted_token, offsets, w_gate_up, act, dev_status, workspace, s));
-  MOE_TRY(do_down(desc, act, offsets, w_down, yperm, dev_status, s));
+  MOE_TRY(do_down(desc, act, offsets, w_down, yperm, dev_status, workspace, s));
   return do_combine(desc, yperm, ysh, inv_row, topk_w, k_per_token, out, dev_status, s);
 }
 

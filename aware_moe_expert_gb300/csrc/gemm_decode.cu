@@ -14,8 +14,9 @@
 // Work items are (token chunk of one unit (<= 128 rows), weight slice, K
 // split).  The split count S is chosen on the device from the real number of
 // items so that the persistent grid runs close to whole waves; with S > 1 the
-// gate|up kernel writes fp32 partial sums and moe::launch_split_swiglu adds
-// them in split order (deterministic) and applies SiLU * up.
+// kernel writes fp32 partial sums, and split_swiglu_kernel (gate|up: adds
+// the splits, then SiLU * up) or split_sum_kernel (down) adds them in split
+// order, so the result does not depend on scheduling.
 //
 // Roles as in the prefill kernel: warp 0 TMA producer, warp 1 TMEM owner and
 // MMA issuer, warps 2-5 epilogue (TMEM lane = weight row = output column).
@@ -42,8 +43,8 @@ struct DParams {
   int w_up_offset;      // gate|up: rows from a gate row to its up row
   int n_out;            // output columns (gate|up: I_sub, down: H)
   void* out;            // bf16 [out_rows, n_out]
-  float* partial;       // fp32 [max_split][out_rows][2 * n_out] (gate|up, S > 1)
-  int32_t* split_word;  // receives the chosen S (gate|up)
+  float* partial;       // fp32 [max_split][out_rows][w * n_out], w = 2 (gate|up) or 1
+  int32_t* split_word;  // receives the chosen S
   long long out_rows;
   int max_split;
   int32_t* status;
@@ -75,8 +76,8 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 }
 
 // Split count for `items1` unsplit items on a grid of G CTAs: the smallest
-// S <= max_split (and <= k-blocks) whose last wave is at least 85% full, else
-// the one with the fullest waves.
+// S <= max_split (and <= k-blocks) whose waves are at least 93% full on
+// average, else the one with the fullest waves.
 __device__ __forceinline__ int choose_split(int items1, int G, int max_split, int KB) {
   if (items1 <= 0) return 1;
   int best_s = 1;
@@ -86,7 +87,7 @@ __device__ __forceinline__ int choose_split(int items1, int G, int max_split, in
     const long long it = static_cast<long long>(items1) * s;
     const long long waves = (it + G - 1) / G;
     const float e = static_cast<float>(it) / static_cast<float>(waves * G);
-    if (e >= 0.85f) return s;
+    if (e >= 0.93f) return s;
     if (e > best_e + 0.02f) {
       best_e = e;
       best_s = s;
@@ -146,9 +147,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *s_tmem;
   const int KB = p.K / kBK;
   const int items1 = *s_total * p.m_tiles;
-  const int S = GATE_UP ? choose_split(items1, gridDim.x, p.max_split, KB) : 1;
-  if (GATE_UP && blockIdx.x == 0 && threadIdx.x == 0 && p.split_word != nullptr)
-    *p.split_word = S;
+  const int S = choose_split(items1, gridDim.x, p.max_split, KB);
+  if (blockIdx.x == 0 && threadIdx.x == 0 && p.split_word != nullptr) *p.split_word = S;
   const int per_mt = p.m_tiles * S;
   const int total_work = items1 * S;
 
@@ -293,8 +293,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 prow[col] = g;
                 prow[p.n_out + col] = u;
               }
-            } else {
+            } else if (S == 1) {
               static_cast<__nv_bfloat16*>(p.out)[r * p.n_out + col] = __float2bfloat16_rn(g);
+            } else {
+              p.partial[(static_cast<long long>(s) * p.out_rows + r) * p.n_out + col] = g;
             }
           }
         }
@@ -348,6 +350,34 @@ __global__ void __launch_bounds__(256) split_swiglu_kernel(const float* __restri
   }
 }
 
+// y[r, c] = sum_s Y_s[r, c] (split order) rounded to bf16, for r < offsets[E_r].
+__global__ void __launch_bounds__(256) split_sum_kernel(const float* __restrict__ partial,
+                                                        const int32_t* __restrict__ split_word,
+                                                        const int32_t* __restrict__ offsets,
+                                                        int E_r, int N, long long out_rows,
+                                                        __nv_bfloat16* __restrict__ y) {
+  const int S = *split_word;
+  if (S <= 1) return;
+  const long long n = min(static_cast<long long>(offsets[E_r]), out_rows);
+  const int nq = N / 4;
+  const long long total = n * nq;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long r = i / nq;
+    const int c = static_cast<int>(i - r * nq) * 4;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < S; ++s) {
+      const float4 b =
+          __ldcg(reinterpret_cast<const float4*>(partial + (static_cast<long long>(s) * out_rows + r) * N + c));
+      a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+    }
+    uint2 o;
+    o.x = pack_bf16x2(a.x, a.y);
+    o.y = pack_bf16x2(a.z, a.w);
+    *reinterpret_cast<uint2*>(y + r * N + c) = o;
+  }
+}
+
 template <bool GATE_UP, int STAGES>
 cudaError_t run_decode(const DecodeGemmArgs& a, cudaStream_t s) {
   using C = DCfg<GATE_UP, STAGES>;
@@ -366,7 +396,7 @@ cudaError_t run_decode(const DecodeGemmArgs& a, cudaStream_t s) {
   p.partial = a.partial;
   p.split_word = a.split_word;
   p.out_rows = a.out_rows;
-  p.max_split = GATE_UP ? a.max_split : 1;
+  p.max_split = a.max_split;
   p.status = a.status;
   p.debug_flags = a.debug_flags;
   auto kern = decode_gemm_kernel<GATE_UP, STAGES>;
@@ -400,7 +430,12 @@ cudaError_t launch_decode_gemm(const DecodeGemmArgs& a, cudaStream_t s) {
                                                static_cast<__nv_bfloat16*>(a.out));
     return cudaGetLastError();
   }
-  return run_decode<false, 6>(a, s);
+  cudaError_t e = run_decode<false, 6>(a, s);
+  if (e != cudaSuccess || a.max_split <= 1) return e;
+  split_sum_kernel<<<a.sm_count * 4, 256, 0, s>>>(a.partial, a.split_word, a.offsets, a.n_groups,
+                                                  a.n_out, a.out_rows,
+                                                  static_cast<__nv_bfloat16*>(a.out));
+  return cudaGetLastError();
 }
 
 }  // namespace moe

@@ -23,38 +23,39 @@ __device__ __forceinline__ float dot8_bf16(uint4 a, uint4 b, float acc) {
   return acc;
 }
 
-// logits[t, u] = x_t . router_w[u] + bias[u / n_sub].  CTA = 8 tokens x 8
-// units, one warp per unit; lanes stride over H in 16-byte vectors.
+// logits[t, u] = x_t . router_w[u] + bias[u / n_sub].  CTA = up to 8
+// tokens x 8 units.  The CTA's x rows are first staged in shared memory
+// (every thread's loads in flight at once); then one warp per unit streams
+// its router row with eight independent 16-byte loads per lane per pass.
 __global__ void __launch_bounds__(256) router_logits_small_kernel(
     const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ rw,
-    const float* __restrict__ bias, int T, int H, int E_r, int n_sub,
+    const float* __restrict__ bias, int T, int H, int E_r, int n_sub, int tok_per_cta,
     float* __restrict__ logits) {
+  extern __shared__ uint4 xs[];  // [tok_per_cta][H / 8]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u = blockIdx.y * 8 + warp;
-  const int t0 = blockIdx.x * kTokPerCta;
+  const int t0 = blockIdx.x * tok_per_cta;
+  const int nt = min(tok_per_cta, T - t0);
+  const int nv = H / 8;
+  const uint4* xg = reinterpret_cast<const uint4*>(x) + static_cast<size_t>(t0) * nv;
+  for (int i = threadIdx.x; i < nt * nv; i += blockDim.x) xs[i] = __ldg(xg + i);
+  __syncthreads();
   if (u >= E_r) return;
-  const int nt = min(kTokPerCta, T - t0);
   float acc[kTokPerCta];
 #pragma unroll
   for (int i = 0; i < kTokPerCta; ++i) acc[i] = 0.f;
   const uint4* wrow = reinterpret_cast<const uint4*>(rw + static_cast<size_t>(u) * H);
-  const int nv = H / 8;
-  // four 16-byte vectors per lane per pass, all loads issued before the math
-  for (int v0 = lane; v0 < nv; v0 += 128) {
-    uint4 wv[4];
+  for (int v0 = lane; v0 < nv; v0 += 256) {
+    uint4 wv[8];
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
+    for (int q = 0; q < 8; ++q)
       wv[q] = v0 + 32 * q < nv ? __ldg(wrow + v0 + 32 * q) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-    for (int i = 0; i < kTokPerCta; ++i) {
-      if (i < nt) {
-        const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t0 + i) * H);
-        uint4 xv[4];
+    for (int q = 0; q < 8; ++q) {
+      if (v0 + 32 * q < nv) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          xv[q] = v0 + 32 * q < nv ? __ldg(xr + v0 + 32 * q) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) acc[i] = dot8_bf16(xv[q], wv[q], acc[i]);
+        for (int i = 0; i < kTokPerCta; ++i)
+          if (i < nt) acc[i] = dot8_bf16(xs[i * nv + v0 + 32 * q], wv[q], acc[i]);
       }
     }
   }
@@ -190,10 +191,27 @@ cudaError_t launch_router_logits_small(const void* x, const void* router_w,
                                        const float* expert_bias, int T, int H, int E_r,
                                        int n_sub, float* logits, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  dim3 grid((T + kTokPerCta - 1) / kTokPerCta, (E_r + 7) / 8);
-  router_logits_small_kernel<<<grid, 256, 0, s>>>(
+  // staged x rows: at most 96 KB of shared memory per CTA
+  const int row_bytes = H * 2;
+  int tpc = (96 * 1024) / row_bytes;
+  tpc = tpc < 1 ? 1 : (tpc > kTokPerCta ? kTokPerCta : tpc);
+  const int smem = tpc * row_bytes;
+  if (smem > 96 * 1024) return cudaErrorInvalidValue;
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_done[dev]) {
+    e = cudaFuncSetAttribute(router_logits_small_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  dim3 grid((T + tpc - 1) / tpc, (E_r + 7) / 8);
+  router_logits_small_kernel<<<grid, 256, smem, s>>>(
       static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(router_w),
-      expert_bias, T, H, E_r, n_sub, logits);
+      expert_bias, T, H, E_r, n_sub, tpc, logits);
   return cudaGetLastError();
 }
 

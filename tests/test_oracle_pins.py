@@ -450,3 +450,12 @@ def test_bf16_bit_conversion_exact():
     v = O.bf16_to_f64(bits)
     assert v[0] == 1.0 and v[1] == -1.0 and v[2] == 0.0 and math.copysign(1, v[3]) < 0
     assert math.isinf(v[4]) and v[5] == 3.140625 and v[6] == 2.0 ** -133
+
+
+def test_distinct_units_counts_nonzero_units():
+    assert O.distinct_units(np.array([0, 3, 0, 1, 7])) == 3
+    assert O.distinct_units(np.zeros(5, dtype=np.int32)) == 0
+    # from a permutation: every selected unit is counted once
+    idx = np.array([[2, 0, -1], [2, 5, 1]], dtype=np.int32)
+    counts, *_ = O.permute(idx, [2, 3], 6)
+    assert O.distinct_units(counts) == 4

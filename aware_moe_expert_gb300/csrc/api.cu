@@ -146,6 +146,12 @@ bool use_decode_path(const moe_layer_desc* d, int n_out) {
   return static_cast<long long>(d->T) * d->k_max <= 64ll * E_r_of(d);
 }
 
+// Tokens per weight-stationary item: 64 when units hold few rows (decode),
+// else larger chunks so each weight tile is reused across more tokens.
+int decode_chunk(const moe_layer_desc* d) {
+  return static_cast<long long>(d->T) * d->k_max <= 64ll * E_r_of(d) ? 64 : 128;
+}
+
 // ---- the steps, without argument checks (callers check)
 
 moe_status do_route(const moe_layer_desc* d, const void* x, const void* router_w,
@@ -229,6 +235,7 @@ moe_status do_gate_up(const moe_layer_desc* d, const void* x, const int32_t* sor
     a.status = status;
     a.debug_flags = d->debug_flags;
     a.sm_count = sm_count();
+    a.chunk = decode_chunk(d);
     return cuda_status(moe::launch_decode_gemm(a, s));
   }
   GemmArgs g{};
@@ -278,6 +285,7 @@ moe_status do_down(const moe_layer_desc* d, const void* act, const int32_t* offs
     a.status = status;
     a.debug_flags = 0;
     a.sm_count = sm_count();
+    a.chunk = decode_chunk(d);
     return cuda_status(moe::launch_decode_gemm(a, s));
   }
   GemmArgs g{};

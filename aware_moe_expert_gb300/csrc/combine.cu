@@ -26,6 +26,7 @@ __global__ void __launch_bounds__(256) combine_kernel(
     const int32_t* __restrict__ inv_row, const float* __restrict__ topk_w,
     const int32_t* __restrict__ kpt, int T, int nv, int k_max, int n_rows,
     uint4* __restrict__ out, int32_t* status) {
+  pdl_wait_and_trigger();
   const long long gid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int t = static_cast<int>(gid / nv);
   const int v = static_cast<int>(gid - static_cast<long long>(t) * nv);
@@ -84,10 +85,10 @@ cudaError_t launch_combine(const void* y_perm, const void* y_shared, const int32
                            int k_max, int n_rows, void* out, int32_t* status, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   const long long threads = static_cast<long long>(T) * (H / 8);
-  combine_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(
-      static_cast<const uint4*>(y_perm), static_cast<const uint4*>(y_shared), inv_row, topk_w,
-      k_per_token, T, H / 8, k_max, n_rows, static_cast<uint4*>(out), status);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3(static_cast<unsigned>((threads + 255) / 256)), dim3(256),
+                    0, s, static_cast<const uint4*>(y_perm), static_cast<const uint4*>(y_shared),
+                    inv_row, topk_w, k_per_token, T, H / 8, k_max, n_rows,
+                    static_cast<uint4*>(out), status);
 }
 
 }  // namespace moe

@@ -107,6 +107,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* s_offs = reinterpret_cast<int*>(smem + C::kOffOffs);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_wait_and_trigger();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -375,18 +376,9 @@ cudaError_t run_gemm(const GemmArgs& g, cudaStream_t s) {
   // The shared-memory opt-in is set once per device, so that launches made
   // while a stream is being captured into a CUDA graph issue no other call.
   static bool attr_done[64] = {false};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  cudaError_t e = set_smem_once(kern, static_cast<int>(C::kSmemBytes), attr_done);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_done[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(C::kSmemBytes));
-    if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
-  }
-  kern<<<grid, kThreads, C::kSmemBytes, s>>>(ta, tb, kp);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), C::kSmemBytes, s, ta, tb, kp);
 }
 
 }  // namespace

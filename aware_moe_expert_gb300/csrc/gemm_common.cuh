@@ -13,6 +13,8 @@ struct Tile {
   int g, row0, rows, nt;
 };
 
+// Work item w -> (group, first row, rows, n-tile) for m-tiles of TR rows.
+template <int TR = kTileRows>
 __device__ __forceinline__ Tile decode_tile(int w, int n_tiles, int n_groups, const int* prefix,
                                             const int* offs) {
   Tile t;
@@ -28,8 +30,8 @@ __device__ __forceinline__ Tile decode_tile(int w, int n_tiles, int n_groups, co
       hi = mid;
   }
   t.g = lo;
-  t.row0 = offs[lo] + (mt - prefix[lo]) * kTileRows;
-  t.rows = min(kTileRows, offs[lo + 1] - t.row0);
+  t.row0 = offs[lo] + (mt - prefix[lo]) * TR;
+  t.rows = min(TR, offs[lo + 1] - t.row0);
   return t;
 }
 
@@ -41,11 +43,12 @@ __device__ __forceinline__ void fail(volatile int* abort, int32_t* status) {
 }
 
 
-// Built by one warp: s_prefix[g] = first m-tile of group g (s_prefix[G] =
+// Built by one warp (m-tiles of TR rows): s_prefix[g] = first m-tile of group g (s_prefix[G] =
 // total), s_offs = row offsets, *s_total = number of m-tiles.  offsets ==
 // nullptr means one dense group of dense_rows rows.  Offsets that decrease,
 // are negative, or end past out_rows are reported (MOE_ERR_BAD_INDEX) and
 // give zero tiles.
+template <int TR = kTileRows>
 __device__ __forceinline__ void build_tile_table(const int32_t* offsets, int G, int dense_rows,
                                                  long long out_rows, int* s_prefix, int* s_offs,
                                                  int* s_total, int32_t* status, int lane) {
@@ -54,7 +57,7 @@ __device__ __forceinline__ void build_tile_table(const int32_t* offsets, int G, 
       s_offs[0] = 0;
       s_offs[1] = dense_rows;
       s_prefix[0] = 0;
-      s_prefix[1] = (dense_rows + kTileRows - 1) / kTileRows;
+      s_prefix[1] = (dense_rows + TR - 1) / TR;
       *s_total = s_prefix[1];
     }
     return;
@@ -69,7 +72,7 @@ __device__ __forceinline__ void build_tile_table(const int32_t* offsets, int G, 
       const int a = offsets[g], b = offsets[g + 1];
       bad |= (a < 0) || (b < a);
       s_offs[g] = a;
-      local += b > a ? (b - a + kTileRows - 1) / kTileRows : 0;
+      local += b > a ? (b - a + TR - 1) / TR : 0;
     }
   }
   int incl = local;
@@ -84,7 +87,7 @@ __device__ __forceinline__ void build_tile_table(const int32_t* offsets, int G, 
     if (g < G) {
       s_prefix[g] = run;
       const int a = offsets[g], b = offsets[g + 1];
-      run += b > a ? (b - a + kTileRows - 1) / kTileRows : 0;
+      run += b > a ? (b - a + TR - 1) / TR : 0;
     }
   }
   if (lane == 31) {

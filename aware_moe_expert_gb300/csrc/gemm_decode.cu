@@ -1,6 +1,6 @@
 // Decode-shaped grouped GEMM ("swap AB"): when every routing unit holds only
 // a few token rows, the weights are the 128-row tcgen05 M operand and the
-// unit's tokens the small N operand (16..128), so each activated sub-expert's
+// unit's tokens the small N operand (16..64), so each activated sub-expert's
 // weights stream from HBM once per step while the tensor cores do no padded
 // work on the weight side.  Decode is bound by the bytes of the activated
 // experts' weights (MoE-Prism, arXiv 2510.19366, §II-A: work is linear in the
@@ -11,7 +11,7 @@
 //            128-neuron slice; act[c, n] = SiLU(D_g) * D_u   (§III-B1 Eq. (1))
 //   down     D[h, c] = sum_k Wd_u[h, k] act_c[k], h in a 128-row slice of H
 //
-// Work items are (token chunk of one unit (<= 128 rows), weight slice, K
+// Work items are (token chunk of one unit (<= 64 rows), weight slice, K
 // split).  The split count S is chosen on the device from the real number of
 // items so that the persistent grid runs close to whole waves; with S > 1 the
 // kernel writes fp32 partial sums, and split_swiglu_kernel (gate|up: adds
@@ -26,13 +26,12 @@
 namespace moe {
 namespace {
 
-constexpr int kBK = 64;
+constexpr int kBK = 64;           // columns of one 128-byte swizzled sub-block
 constexpr int kM = 128;           // weight rows per item (MMA M)
 constexpr int kTokBox = 16;       // token rows per TMA box
 constexpr int kThreads = 192;
-constexpr uint32_t kWBytes = kM * kBK * 2;                 // one weight tile: 16 KB
-constexpr uint32_t kTokBytes = kTileRows * kBK * 2;        // token tile capacity: 16 KB
-constexpr uint32_t kTmemCols = 512;                        // 2 slots x (gate 128 | up 128)
+constexpr uint32_t kWBytes = kM * kBK * 2;  // one weight sub-block: 16 KB
+constexpr uint32_t kTmemCols = 512;         // 2 accumulator slots
 
 struct DParams {
   const int32_t* offsets;
@@ -49,11 +48,19 @@ struct DParams {
   int max_split;
   int32_t* status;
   uint32_t debug_flags;
+  float item_bytes;     // weight bytes of one unsplit item
+  float total_scale;    // 1 / (HBM bytes per ns) for the whole grid
 };
 
-template <bool GATE_UP, int STAGES>
+// GATE_UP: two weight tiles (gate, up) per stage; CHUNK: tokens per item
+// (MMA N <= CHUNK); KSUB: 64-column sub-blocks per pipeline stage.
+template <bool GATE_UP, int STAGES, int CHUNK, int KSUB>
 struct DCfg {
-  static constexpr uint32_t kA = GATE_UP ? 2 * kWBytes : kWBytes;
+  static constexpr uint32_t kW = kWBytes * KSUB;                        // one weight tile
+  static constexpr uint32_t kA = GATE_UP ? 2 * kW : kW;
+  static constexpr uint32_t kTokSub = CHUNK * kBK * 2;                  // tokens, one sub-block
+  static constexpr uint32_t kTokBytes = kTokSub * KSUB;
+  static constexpr uint32_t kSlot = GATE_UP ? 2 * CHUNK : CHUNK;        // TMEM columns per slot
   static constexpr uint32_t kStage = kA + kTokBytes;
   static constexpr uint32_t kOffB = STAGES * kA;
   static constexpr uint32_t kOffBar = STAGES * kStage;
@@ -63,6 +70,8 @@ struct DCfg {
   static constexpr uint32_t kOffOffs = kOffPrefix + (kMaxGroups + 1) * 4;
   static constexpr uint32_t kSmemBytes = kOffOffs + (kMaxGroups + 1) * 4 + 1024;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  static_assert(2 * kSlot <= kTmemCols, "two accumulator slots in TMEM");
+  static_assert(CHUNK % 16 == 0 && CHUNK <= 256, "tcgen05 N for M = 128");
 };
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
@@ -75,32 +84,36 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr));
 }
 
-// Split count for `items1` unsplit items on a grid of G CTAs: the smallest
-// S <= max_split (and <= k-blocks) whose waves are at least 93% full on
-// average, else the one with the fullest waves.
-__device__ __forceinline__ int choose_split(int items1, int G, int max_split, int KB) {
+// Split count for `items1` unsplit items of `item_bytes` weight bytes on a
+// grid of G CTAs.  Estimated time of split S: the larger of the whole-grid
+// HBM time and the per-CTA streaming time of the busiest CTA (waves x bytes
+// per split item at the rate one SM sustains), plus a reduction launch when
+// S > 1.  The smallest S within 3% of the best estimate wins.
+__device__ __forceinline__ int choose_split(int items1, int G, int max_split, int KB,
+                                            float item_bytes, float hbm_ns_per_byte) {
   if (items1 <= 0) return 1;
-  int best_s = 1;
-  float best_e = 0.f;
+  constexpr float kSmBytesPerNs = 100.f;   // one SM streaming alone, ~100 GB/s
+  constexpr float kReduceNs = 3000.f;      // extra launch + partial traffic
+  const float total_ns = static_cast<float>(items1) * item_bytes * hbm_ns_per_byte;
   const int smax = min(max_split, KB);
-  for (int s = 1; s <= smax; ++s) {
-    const long long it = static_cast<long long>(items1) * s;
-    const long long waves = (it + G - 1) / G;
-    const float e = static_cast<float>(it) / static_cast<float>(waves * G);
-    if (e >= 0.93f) return s;
-    if (e > best_e + 0.02f) {
-      best_e = e;
-      best_s = s;
-    }
+  float t[9];
+  float best = 3.4e38f;
+  for (int s = 1; s <= smax && s <= 8; ++s) {
+    const long long waves = (static_cast<long long>(items1) * s + G - 1) / G;
+    const float per_cta = static_cast<float>(waves) * item_bytes / s / kSmBytesPerNs;
+    t[s] = fmaxf(total_ns, per_cta) + (s > 1 ? kReduceNs : 0.f);
+    best = fminf(best, t[s]);
   }
-  return best_s;
+  for (int s = 1; s <= smax && s <= 8; ++s)
+    if (t[s] <= best * 1.03f) return s;
+  return 1;
 }
 
-template <bool GATE_UP, int STAGES>
+template <bool GATE_UP, int STAGES, int CHUNK, int KSUB>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
                        const __grid_constant__ CUtensorMap tmX, const DParams p) {
-  using C = DCfg<GATE_UP, STAGES>;
+  using C = DCfg<GATE_UP, STAGES, CHUNK, KSUB>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -116,6 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* s_prefix = reinterpret_cast<int*>(smem + C::kOffPrefix);
   int* s_offs = reinterpret_cast<int*>(smem + C::kOffOffs);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_wait_and_trigger();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -135,8 +149,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmX);
   }
   if (warp == 2)
-    build_tile_table(p.offsets, p.n_groups, 0, p.out_rows, s_prefix, s_offs, s_total, p.status,
-                     lane);
+    build_tile_table<CHUNK>(p.offsets, p.n_groups, 0, p.out_rows, s_prefix, s_offs, s_total,
+                             p.status, lane);
   if (warp == 1) {
     tmem_alloc(s_tmem, kTmemCols);
     tmem_relinquish();
@@ -145,9 +159,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
-  const int KB = p.K / kBK;
+  const int KB = p.K / (kBK * KSUB);
   const int items1 = *s_total * p.m_tiles;
-  const int S = choose_split(items1, gridDim.x, p.max_split, KB);
+  const int S = choose_split(items1, gridDim.x, p.max_split, KB, p.item_bytes, p.total_scale);
   if (blockIdx.x == 0 && threadIdx.x == 0 && p.split_word != nullptr) *p.split_word = S;
   const int per_mt = p.m_tiles * S;
   const int total_work = items1 * S;
@@ -162,9 +176,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int mt = w / per_mt;
         const int rem = w - mt * per_mt;
         const int m = rem / S, s = rem - (rem / S) * S;
-        const Tile t = decode_tile(mt, 1, p.n_groups, s_prefix, s_offs);
+        const Tile t = decode_tile<CHUNK>(mt, 1, p.n_groups, s_prefix, s_offs);
         const int nb = (t.rows + kTokBox - 1) / kTokBox;
-        const uint32_t bytes = C::kA + static_cast<uint32_t>(nb) * kTokBox * kBK * 2;
+        const uint32_t bytes = C::kA + static_cast<uint32_t>(KSUB * nb) * kTokBox * kBK * 2;
         const int wrow = t.g * p.w_group_rows + m * kM;
         const int kb0 = s * KB / S, kb1 = (s + 1) * KB / S;
         for (int kb = kb0; kb < kb1; ++kb) {
@@ -176,13 +190,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             skip = false;  // test hook: the consumer of this slot must time out
           } else {
             uint8_t* sa = smem + stage * C::kA;
-            uint8_t* sb = smem + C::kOffB + stage * kTokBytes;
+            uint8_t* sb = smem + C::kOffB + stage * C::kTokBytes;
             mbar_expect_tx(&full[stage], bytes);
-            tma_load_2d(sa, &tmW, &full[stage], kb * kBK, wrow);
-            if (GATE_UP) tma_load_2d(sa + kWBytes, &tmW, &full[stage], kb * kBK, wrow + p.w_up_offset);
-            for (int b = 0; b < nb; ++b)
-              tma_load_2d(sb + b * kTokBox * kBK * 2, &tmX, &full[stage], kb * kBK,
-                          t.row0 + b * kTokBox);
+#pragma unroll
+            for (int j = 0; j < KSUB; ++j) {
+              const int kc = (kb * KSUB + j) * kBK;
+              tma_load_2d(sa + j * kWBytes, &tmW, &full[stage], kc, wrow);
+              if (GATE_UP)
+                tma_load_2d(sa + C::kW + j * kWBytes, &tmW, &full[stage], kc, wrow + p.w_up_offset);
+              for (int b = 0; b < nb; ++b)
+                tma_load_2d(sb + j * C::kTokSub + b * kTokBox * kBK * 2, &tmX, &full[stage], kc,
+                            t.row0 + b * kTokBox);
+            }
             issued |= 1u << stage;
             issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
           }
@@ -206,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int mt = w / per_mt;
         const int rem = w - mt * per_mt;
         const int s = rem - (rem / S) * S;
-        const Tile t = decode_tile(mt, 1, p.n_groups, s_prefix, s_offs);
+        const Tile t = decode_tile<CHUNK>(mt, 1, p.n_groups, s_prefix, s_offs);
         const int n = ((t.rows + 15) / 16) * 16;
         const uint32_t idesc = idesc_bf16_f32(kM, n);
         const int kb0 = s * KB / S, kb1 = (s + 1) * KB / S;
@@ -215,22 +234,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t dg = tmem_base + static_cast<uint32_t>(acc * 256);
-        const uint32_t du = dg + 128u;
+        const uint32_t dg = tmem_base + static_cast<uint32_t>(acc) * C::kSlot;
+        const uint32_t du = dg + static_cast<uint32_t>(CHUNK);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full[stage], phase, s_abort)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t ag = sdesc_sw128(smem_u32(smem + stage * C::kA));
-          const uint64_t au = sdesc_sw128(smem_u32(smem + stage * C::kA + kWBytes));
-          const uint64_t bx = sdesc_sw128(smem_u32(smem + C::kOffB + stage * kTokBytes));
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k) {
-            const uint32_t accum = (kb != kb0 || k != 0) ? 1u : 0u;
-            umma_bf16(dg, ag + 2u * k, bx + 2u * k, idesc, accum);
-            if (GATE_UP) umma_bf16(du, au + 2u * k, bx + 2u * k, idesc, accum);
+          for (int j = 0; j < KSUB; ++j) {
+            const uint64_t ag = sdesc_sw128(smem_u32(smem + stage * C::kA + j * kWBytes));
+            const uint64_t au = sdesc_sw128(smem_u32(smem + stage * C::kA + C::kW + j * kWBytes));
+            const uint64_t bx =
+                sdesc_sw128(smem_u32(smem + C::kOffB + stage * C::kTokBytes + j * C::kTokSub));
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k) {
+              const uint32_t accum = (kb != kb0 || j != 0 || k != 0) ? 1u : 0u;
+              umma_bf16(dg, ag + 2u * k, bx + 2u * k, idesc, accum);
+              if (GATE_UP) umma_bf16(du, au + 2u * k, bx + 2u * k, idesc, accum);
+            }
           }
           umma_commit(&empty[stage]);
           if (++stage == STAGES) {
@@ -259,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int mt = w / per_mt;
       const int rem = w - mt * per_mt;
       const int m = rem / S, s = rem - (rem / S) * S;
-      const Tile t = decode_tile(mt, 1, p.n_groups, s_prefix, s_offs);
+      const Tile t = decode_tile<CHUNK>(mt, 1, p.n_groups, s_prefix, s_offs);
       int ok = 1;
       if (lane == 0) ok = mbar_wait(&tfull[acc], aphase, s_abort) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -269,12 +292,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const uint32_t tg = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                          static_cast<uint32_t>(acc * 256);
+                          static_cast<uint32_t>(acc) * C::kSlot;
       const int col = m * kM + r_in;  // output column of this thread
       for (int c0 = 0; c0 < t.rows; c0 += 16) {
         uint32_t gv[16], uv[16];
         tmem_ld16(tg + c0, gv);
-        if (GATE_UP) tmem_ld16(tg + 128u + c0, uv);
+        if (GATE_UP) tmem_ld16(tg + static_cast<uint32_t>(CHUNK) + c0, uv);
         tmem_ld_wait();
 #pragma unroll
         for (int cc = 0; cc < 16; ++cc) {
@@ -326,6 +349,7 @@ __global__ void __launch_bounds__(256) split_swiglu_kernel(const float* __restri
                                                            const int32_t* __restrict__ offsets,
                                                            int E_r, int I, long long out_rows,
                                                            __nv_bfloat16* __restrict__ act) {
+  pdl_wait_and_trigger();
   const int S = *split_word;
   if (S <= 1) return;
   const long long n = min(static_cast<long long>(offsets[E_r]), out_rows);
@@ -356,6 +380,7 @@ __global__ void __launch_bounds__(256) split_sum_kernel(const float* __restrict_
                                                         const int32_t* __restrict__ offsets,
                                                         int E_r, int N, long long out_rows,
                                                         __nv_bfloat16* __restrict__ y) {
+  pdl_wait_and_trigger();
   const int S = *split_word;
   if (S <= 1) return;
   const long long n = min(static_cast<long long>(offsets[E_r]), out_rows);
@@ -378,9 +403,9 @@ __global__ void __launch_bounds__(256) split_sum_kernel(const float* __restrict_
   }
 }
 
-template <bool GATE_UP, int STAGES>
+template <bool GATE_UP, int STAGES, int CHUNK, int KSUB>
 cudaError_t run_decode(const DecodeGemmArgs& a, cudaStream_t s) {
-  using C = DCfg<GATE_UP, STAGES>;
+  using C = DCfg<GATE_UP, STAGES, CHUNK, KSUB>;
   CUtensorMap tw, tx;
   if (!make_tmap_bf16(&tw, a.w, a.w_rows, a.K, kM)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tx, a.x, a.x_rows, a.K, kTokBox)) return cudaErrorInvalidValue;
@@ -399,20 +424,13 @@ cudaError_t run_decode(const DecodeGemmArgs& a, cudaStream_t s) {
   p.max_split = a.max_split;
   p.status = a.status;
   p.debug_flags = a.debug_flags;
-  auto kern = decode_gemm_kernel<GATE_UP, STAGES>;
+  p.item_bytes = static_cast<float>(GATE_UP ? 2 * kM : kM) * a.K * 2.f;
+  p.total_scale = 1.f / 6200.f;  // ~6.2 TB/s sustained weight streaming
+  auto kern = decode_gemm_kernel<GATE_UP, STAGES, CHUNK, KSUB>;
   static bool attr_done[64] = {false};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  cudaError_t e = set_smem_once(kern, static_cast<int>(C::kSmemBytes), attr_done);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_done[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(C::kSmemBytes));
-    if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
-  }
-  kern<<<a.sm_count, kThreads, C::kSmemBytes, s>>>(tw, tx, p);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(a.sm_count), dim3(kThreads), C::kSmemBytes, s, tw, tx, p);
 }
 
 }  // namespace
@@ -422,20 +440,26 @@ bool decode_gemm_supports(int n_out) { return n_out % kM == 0; }
 cudaError_t launch_decode_gemm(const DecodeGemmArgs& a, cudaStream_t s) {
   if (a.x_rows <= 0) return cudaSuccess;
   if (a.gate_up) {
-    cudaError_t e = run_decode<true, 4>(a, s);
+    cudaError_t e = a.chunk <= 64 ? run_decode<true, 5, 64, 1>(a, s)
+                                  : run_decode<true, 4, 128, 1>(a, s);
     if (e != cudaSuccess || a.max_split <= 1) return e;
-    int blocks = a.sm_count * 4;
-    split_swiglu_kernel<<<blocks, 256, 0, s>>>(a.partial, a.split_word, a.offsets, a.n_groups,
-                                               a.n_out, a.out_rows,
-                                               static_cast<__nv_bfloat16*>(a.out));
-    return cudaGetLastError();
+    return launch_pdl(split_swiglu_kernel, dim3(a.sm_count * 4), dim3(256), 0, s,
+                      static_cast<const float*>(a.partial),
+                      static_cast<const int32_t*>(a.split_word), a.offsets, a.n_groups, a.n_out,
+                      a.out_rows, static_cast<__nv_bfloat16*>(a.out));
   }
-  cudaError_t e = run_decode<false, 6>(a, s);
+  cudaError_t e;
+  if (a.chunk > 64)
+    e = run_decode<false, 4, 256, 1>(a, s);
+  else if (a.K % 128 == 0)
+    e = run_decode<false, 4, 64, 2>(a, s);
+  else
+    e = run_decode<false, 8, 64, 1>(a, s);
   if (e != cudaSuccess || a.max_split <= 1) return e;
-  split_sum_kernel<<<a.sm_count * 4, 256, 0, s>>>(a.partial, a.split_word, a.offsets, a.n_groups,
-                                                  a.n_out, a.out_rows,
-                                                  static_cast<__nv_bfloat16*>(a.out));
-  return cudaGetLastError();
+  return launch_pdl(split_sum_kernel, dim3(a.sm_count * 4), dim3(256), 0, s,
+                    static_cast<const float*>(a.partial), static_cast<const int32_t*>(a.split_word),
+                    a.offsets, a.n_groups, a.n_out, a.out_rows,
+                    static_cast<__nv_bfloat16*>(a.out));
 }
 
 }  // namespace moe

@@ -80,6 +80,7 @@ struct DecodeGemmArgs {
   int32_t* status;
   uint32_t debug_flags;
   int sm_count;
+  int chunk;                 // tokens per item: 64 (decode-sized units) or more (prefill)
 };
 
 cudaError_t launch_decode_gemm(const DecodeGemmArgs& a, cudaStream_t s);

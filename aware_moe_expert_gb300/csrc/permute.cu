@@ -25,6 +25,7 @@ __global__ void __launch_bounds__(256) bitmap_kernel(const int32_t* __restrict__
                                                       uint32_t* __restrict__ bitmap,
                                                       int32_t* status) {
   __shared__ uint32_t bits[256];
+  pdl_wait_and_trigger();
   for (int u = threadIdx.x; u < E_r; u += blockDim.x) bits[u] = 0u;
   __syncthreads();
   const int word = blockIdx.x;
@@ -59,6 +60,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(const uint32_t* __restrict__
                                                      int32_t* __restrict__ counts,
                                                      int32_t* __restrict__ offsets) {
   __shared__ int32_t s_cnt[256];
+  pdl_wait_and_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int u = warp; u < E_r; u += 32) {
     const uint32_t* row = bitmap + static_cast<size_t>(u) * W;
@@ -111,6 +113,7 @@ __global__ void __launch_bounds__(256) scatter_kernel(
     int E_r, int W, const uint32_t* __restrict__ bitmap, const int32_t* __restrict__ wprefix,
     const int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_token,
     int32_t* __restrict__ inv_row) {
+  pdl_wait_and_trigger();
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= static_cast<long long>(T) * k_max) return;
   const int t = static_cast<int>(i / k_max), j = static_cast<int>(i - static_cast<long long>(t) * k_max);
@@ -137,6 +140,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
                                                            int E_r, int T, int nv, int n_cap,
                                                            uint4* __restrict__ x_perm,
                                                            int32_t* status) {
+  pdl_wait_and_trigger();
   const int n = min(offsets[E_r], n_cap);
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -155,8 +159,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
 }
 
 // Decode-sized batches in one CTA (1024 threads): bitmap, word prefixes,
-// offsets and scatter all in shared memory (W = ceil(T/32) <= 32 words per
-// unit).  Same result as bitmap_kernel + scan_kernel + scatter_kernel.
+// offsets and scatter all in shared memory (W = ceil(T/32) <= 8 words per
+// unit, T <= 256).  Same result as bitmap_kernel + scan_kernel + scatter_kernel.
 __global__ void __launch_bounds__(1024) permute_small_kernel(
     const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ kpt, int T, int k_max,
     int E_r, int W, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
@@ -166,6 +170,7 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(
   int32_t* pre = reinterpret_cast<int32_t*>(sm + E_r * W);
   int32_t* s_cnt = pre + E_r * W;
   int32_t* s_off = s_cnt + 256;
+  pdl_wait_and_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   for (int i = tid; i < E_r * W; i += blockDim.x) bits[i] = 0u;
   __syncthreads();
@@ -247,31 +252,30 @@ cudaError_t launch_permute(const int32_t* topk_idx, const int32_t* k_per_token, 
                            int32_t* counts, int32_t* offsets, int32_t* sorted_token,
                            int32_t* inv_row, int32_t* status, cudaStream_t s) {
   const int W = (T + 31) / 32;
-  if (W > 0 && W <= 32 && E_r * W <= 8192) {
+  if (W > 0 && W <= 8) {
     const int smem = (2 * E_r * W + 256 + 257) * 4;
     static bool attr_done[64] = {false};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    cudaError_t e = set_smem_once(permute_small_kernel, (2 * 256 * 8 + 256 + 257) * 4, attr_done);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_done[dev]) {
-      e = cudaFuncSetAttribute(permute_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (2 * 8192 + 256 + 257) * 4);
-      if (e != cudaSuccess) return e;
-      attr_done[dev] = true;
-    }
-    permute_small_kernel<<<1, 1024, smem, s>>>(topk_idx, k_per_token, T, k_max, E_r, W, counts,
-                                                offsets, sorted_token, inv_row, status);
-    return cudaGetLastError();
+    return launch_pdl(permute_small_kernel, dim3(1), dim3(1024), smem, s, topk_idx, k_per_token,
+                      T, k_max, E_r, W, counts, offsets, sorted_token, inv_row, status);
   }
   if (W > 0) {
-    bitmap_kernel<<<W, 256, 0, s>>>(topk_idx, k_per_token, T, k_max, E_r, W, bitmap, status);
+    cudaError_t e = launch_pdl(bitmap_kernel, dim3(W), dim3(256), 0, s, topk_idx, k_per_token, T,
+                               k_max, E_r, W, bitmap, status);
+    if (e != cudaSuccess) return e;
   }
-  scan_kernel<<<1, 1024, 0, s>>>(bitmap, E_r, W, wprefix, counts, offsets);
+  cudaError_t e = launch_pdl(scan_kernel, dim3(1), dim3(1024), 0, s,
+                             static_cast<const uint32_t*>(bitmap), E_r, W, wprefix, counts,
+                             offsets);
+  if (e != cudaSuccess) return e;
   const long long slots = static_cast<long long>(T) * k_max;
   if (slots > 0) {
-    scatter_kernel<<<static_cast<unsigned>((slots + 255) / 256), 256, 0, s>>>(
-        topk_idx, k_per_token, T, k_max, E_r, W, bitmap, wprefix, offsets, sorted_token, inv_row);
+    e = launch_pdl(scatter_kernel, dim3(static_cast<unsigned>((slots + 255) / 256)), dim3(256), 0,
+                   s, topk_idx, k_per_token, T, k_max, E_r, W,
+                   static_cast<const uint32_t*>(bitmap), static_cast<const int32_t*>(wprefix),
+                   static_cast<const int32_t*>(offsets), sorted_token, inv_row);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }
@@ -283,10 +287,9 @@ cudaError_t launch_gather_rows(const void* x, const int32_t* sorted_token,
   const int warps_needed = n_cap;
   int blocks = (warps_needed + 7) / 8;
   blocks = blocks < sm_count * 8 ? blocks : sm_count * 8;
-  gather_rows_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint4*>(x), sorted_token, offsets,
-                                             E_r, T, H / 8, n_cap, static_cast<uint4*>(x_perm),
-                                             status);
-  return cudaGetLastError();
+  return launch_pdl(gather_rows_kernel, dim3(blocks), dim3(256), 0, s,
+                    static_cast<const uint4*>(x), sorted_token, offsets, E_r, T, H / 8, n_cap,
+                    static_cast<uint4*>(x_perm), status);
 }
 
 }  // namespace moe

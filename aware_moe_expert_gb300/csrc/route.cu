@@ -32,6 +32,7 @@ __global__ void __launch_bounds__(256) router_logits_small_kernel(
     const float* __restrict__ bias, int T, int H, int E_r, int n_sub, int tok_per_cta,
     float* __restrict__ logits) {
   extern __shared__ uint4 xs[];  // [tok_per_cta][H / 8]
+  pdl_wait_and_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u = blockIdx.y * 8 + warp;
   const int t0 = blockIdx.x * tok_per_cta;
@@ -90,6 +91,7 @@ __global__ void __launch_bounds__(256) topk_gate_kernel(
     const float* __restrict__ logits, const int32_t* __restrict__ kpt, int T, int E_r,
     int k_max, int score, int renorm, float route_scale, int32_t* __restrict__ topk_idx,
     float* __restrict__ topk_w, int32_t* status) {
+  pdl_wait_and_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
@@ -198,21 +200,13 @@ cudaError_t launch_router_logits_small(const void* x, const void* router_w,
   const int smem = tpc * row_bytes;
   if (smem > 96 * 1024) return cudaErrorInvalidValue;
   static bool attr_done[64] = {false};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  cudaError_t e = set_smem_once(router_logits_small_kernel, 96 * 1024, attr_done);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_done[dev]) {
-    e = cudaFuncSetAttribute(router_logits_small_kernel,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
-    if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
-  }
   dim3 grid((T + tpc - 1) / tpc, (E_r + 7) / 8);
-  router_logits_small_kernel<<<grid, 256, smem, s>>>(
-      static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(router_w),
-      expert_bias, T, H, E_r, n_sub, tpc, logits);
-  return cudaGetLastError();
+  return launch_pdl(router_logits_small_kernel, grid, dim3(256), smem, s,
+                    static_cast<const __nv_bfloat16*>(x),
+                    static_cast<const __nv_bfloat16*>(router_w), expert_bias, T, H, E_r, n_sub,
+                    tpc, logits);
 }
 
 cudaError_t launch_topk_gate(const float* logits, const int32_t* k_per_token, int T, int E_r,
@@ -222,18 +216,17 @@ cudaError_t launch_topk_gate(const float* logits, const int32_t* k_per_token, in
   if (T <= 0) return cudaSuccess;
   const int grid = (T + 7) / 8;
   if (E_r <= 32)
-    topk_gate_kernel<1><<<grid, 256, 0, s>>>(logits, k_per_token, T, E_r, k_max, score, renorm,
-                                             route_scale, topk_idx, topk_w, status);
+    return launch_pdl(topk_gate_kernel<1>, dim3(grid), dim3(256), 0, s, logits, k_per_token, T,
+                      E_r, k_max, score, renorm, route_scale, topk_idx, topk_w, status);
   else if (E_r <= 64)
-    topk_gate_kernel<2><<<grid, 256, 0, s>>>(logits, k_per_token, T, E_r, k_max, score, renorm,
-                                             route_scale, topk_idx, topk_w, status);
+    return launch_pdl(topk_gate_kernel<2>, dim3(grid), dim3(256), 0, s, logits, k_per_token, T,
+                      E_r, k_max, score, renorm, route_scale, topk_idx, topk_w, status);
   else if (E_r <= 128)
-    topk_gate_kernel<4><<<grid, 256, 0, s>>>(logits, k_per_token, T, E_r, k_max, score, renorm,
-                                             route_scale, topk_idx, topk_w, status);
+    return launch_pdl(topk_gate_kernel<4>, dim3(grid), dim3(256), 0, s, logits, k_per_token, T,
+                      E_r, k_max, score, renorm, route_scale, topk_idx, topk_w, status);
   else
-    topk_gate_kernel<8><<<grid, 256, 0, s>>>(logits, k_per_token, T, E_r, k_max, score, renorm,
-                                             route_scale, topk_idx, topk_w, status);
-  return cudaGetLastError();
+    return launch_pdl(topk_gate_kernel<8>, dim3(grid), dim3(256), 0, s, logits, k_per_token, T,
+                      E_r, k_max, score, renorm, route_scale, topk_idx, topk_w, status);
 }
 
 }  // namespace moe

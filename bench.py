@@ -49,6 +49,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-budget-s", type=float, default=30.0)
+    p.add_argument("--path", type=int, default=0,
+                   help="GEMM family: 0 auto, 1 token tiles, 2 weight-stationary (swap-AB)")
     return p.parse_args()
 
 
@@ -155,6 +157,7 @@ def run_ours(args, wl, rank, world, local):
     d = make_layer_inputs(wl, dev, seed=wl.seed + 1000 * rank)
     desc = B.desc_for(wl, expert_bias=d["expert_bias"], w_shared_gate_up=d.get("w_shared_gate_up"),
                       w_shared_down=d.get("w_shared_down"))
+    desc.path = args.path
     T, H, E_r, k_max, I_sub = wl.T, wl.H, wl.E_r, wl.k_max, wl.I_sub
     ws = torch.empty(B.moe_workspace_size(desc), dtype=torch.uint8, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)

@@ -154,6 +154,42 @@ int decode_chunk(const moe_layer_desc* d) {
 
 // ---- the steps, without argument checks (callers check)
 
+// Router logits into dst: tcgen05 GEMM for T >= 128 with E_r in {64,128,256},
+// else the CUDA-core kernel.
+moe_status do_logits(const moe_layer_desc* d, const void* x, const void* router_w, float* dst,
+                     int32_t* status, cudaStream_t s) {
+  const int E_r = E_r_of(d);
+  if (d->T >= 128 && moe::gemm_supports_f32_router(E_r)) {
+    GemmArgs g{};
+    g.epi = moe::EPI_F32;
+    g.a = x;
+    g.a_rows = d->T;
+    g.b = router_w;
+    g.b_rows = E_r;
+    g.K = d->H;
+    g.offsets = nullptr;
+    g.n_groups = 1;
+    g.dense_rows = d->T;
+    g.n_out = E_r;
+    g.b_group_rows = 0;
+    g.out = dst;
+    g.ld_out = E_r;
+    g.out_rows = d->T;
+    g.bias = d->expert_bias;
+    g.bias_div = d->n_sub;
+    g.status = status;
+    g.debug_flags = 0;
+    g.sm_count = sm_count();
+    g.max_rows_hint = d->T;
+    // small batches: 64-column tiles for more CTAs; large ones: one n-tile,
+    // so x is read once
+    g.bn_hint = d->T < 4096 ? 64 : 0;
+    return cuda_status(moe::launch_gemm(g, s));
+  }
+  return cuda_status(moe::launch_router_logits_small(x, router_w, d->expert_bias, d->T, d->H,
+                                                     E_r, d->n_sub, dst, s));
+}
+
 moe_status do_route(const moe_layer_desc* d, const void* x, const void* router_w,
                     const float* logits_in, const int32_t* kpt, float* logits_out,
                     int32_t* topk_idx, float* topk_w, int32_t* status, void* ws,
@@ -162,33 +198,7 @@ moe_status do_route(const moe_layer_desc* d, const void* x, const void* router_w
   const float* L = logits_in;
   if (L == nullptr) {
     float* dst = logits_out != nullptr ? logits_out : at<float>(ws, layout_of(*d).logits);
-    if (d->T >= 128 && moe::gemm_supports_f32_router(E_r)) {
-      GemmArgs g{};
-      g.epi = moe::EPI_F32;
-      g.a = x;
-      g.a_rows = d->T;
-      g.b = router_w;
-      g.b_rows = E_r;
-      g.K = d->H;
-      g.offsets = nullptr;
-      g.n_groups = 1;
-      g.dense_rows = d->T;
-      g.n_out = E_r;
-      g.b_group_rows = 0;
-      g.out = dst;
-      g.ld_out = E_r;
-      g.out_rows = d->T;
-      g.bias = d->expert_bias;
-      g.bias_div = d->n_sub;
-      g.status = status;
-      g.debug_flags = 0;
-      g.sm_count = sm_count();
-      g.max_rows_hint = d->T;
-      MOE_TRY(cuda_status(moe::launch_gemm(g, s)));
-    } else {
-      MOE_TRY(cuda_status(moe::launch_router_logits_small(x, router_w, d->expert_bias, d->T,
-                                                          d->H, E_r, d->n_sub, dst, s)));
-    }
+    MOE_TRY(do_logits(d, x, router_w, dst, status, s));
     L = dst;
   }
   return cuda_status(moe::launch_topk_gate(L, kpt, d->T, E_r, d->k_max, d->score, d->renorm,

@@ -343,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int BN_MMA, int EPI, int STAGES>
 cudaError_t run_gemm(const GemmArgs& g, cudaStream_t s) {
   using C = Cfg<BN_MMA, STAGES>;
-  const int box_b = EPI == EPI_SWIGLU ? BN_MMA / 2 : BN_MMA;
+  const int box_b = EPI == EPI_SWIGLU ? BN_MMA / 2 : BN_MMA;  // output columns per n-tile
   CUtensorMap ta, tb;
   if (!make_tmap_bf16(&ta, g.a, g.a_rows, g.K, BM)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tb, g.b, g.b_rows, g.K, box_b)) return cudaErrorInvalidValue;
@@ -423,11 +423,14 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s) {
       if (g.n_out % 256 == 0) return run_gemm<256, EPI_BF16, 4>(g, s);
       if (g.n_out % 128 == 0) return run_gemm<128, EPI_BF16, 6>(g, s);
       return run_gemm<64, EPI_BF16, 8>(g, s);
-    case EPI_F32:
-      if (g.n_out == 256) return run_gemm<256, EPI_F32, 4>(g, s);
-      if (g.n_out == 128) return run_gemm<128, EPI_F32, 6>(g, s);
-      if (g.n_out == 64) return run_gemm<64, EPI_F32, 8>(g, s);
+    case EPI_F32: {
+      const int bn = g.bn_hint > 0 && g.bn_hint < g.n_out ? g.bn_hint : g.n_out;
+      if (g.n_out % bn != 0) return cudaErrorInvalidValue;
+      if (bn == 256) return run_gemm<256, EPI_F32, 4>(g, s);
+      if (bn == 128) return run_gemm<128, EPI_F32, 6>(g, s);
+      if (bn == 64) return run_gemm<64, EPI_F32, 8>(g, s);
       return cudaErrorInvalidValue;
+    }
     default:
       return cudaErrorInvalidValue;
   }

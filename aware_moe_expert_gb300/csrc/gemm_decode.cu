@@ -71,7 +71,7 @@ struct DCfg {
   static constexpr uint32_t kSmemBytes = kOffOffs + (kMaxGroups + 1) * 4 + 1024;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
   static_assert(2 * kSlot <= kTmemCols, "two accumulator slots in TMEM");
-  static_assert(CHUNK % 16 == 0 && CHUNK <= 256, "tcgen05 N for M = 128");
+  static_assert(CHUNK % 16 == 0 && CHUNK <= 256 && CHUNK >= 64, "tcgen05 N for M = 128");
 };
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
@@ -112,7 +112,8 @@ __device__ __forceinline__ int choose_split(int items1, int G, int max_split, in
 template <bool GATE_UP, int STAGES, int CHUNK, int KSUB>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
-                       const __grid_constant__ CUtensorMap tmX, const DParams p) {
+                       const __grid_constant__ CUtensorMap tmX,
+                       const __grid_constant__ CUtensorMap tmX64, const DParams p) {
   using C = DCfg<GATE_UP, STAGES, CHUNK, KSUB>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -147,6 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
+    tma_prefetch_desc(&tmX64);
   }
   if (warp == 2)
     build_tile_table<CHUNK>(p.offsets, p.n_groups, 0, p.out_rows, s_prefix, s_offs, s_total,
@@ -177,8 +179,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int rem = w - mt * per_mt;
         const int m = rem / S, s = rem - (rem / S) * S;
         const Tile t = decode_tile<CHUNK>(mt, 1, p.n_groups, s_prefix, s_offs);
+        // token rows: up to two 16-row boxes, else 64-row boxes, per sub-block
         const int nb = (t.rows + kTokBox - 1) / kTokBox;
-        const uint32_t bytes = C::kA + static_cast<uint32_t>(KSUB * nb) * kTokBox * kBK * 2;
+        const bool wide = nb > 2;
+        const int nb64 = (t.rows + 63) / 64;
+        const uint32_t tok_rows = wide ? 64u * nb64 : static_cast<uint32_t>(nb * kTokBox);
+        const uint32_t bytes = C::kA + KSUB * tok_rows * kBK * 2;
         const int wrow = t.g * p.w_group_rows + m * kM;
         const int kb0 = s * KB / S, kb1 = (s + 1) * KB / S;
         for (int kb = kb0; kb < kb1; ++kb) {
@@ -198,9 +204,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_2d(sa + j * kWBytes, &tmW, &full[stage], kc, wrow);
               if (GATE_UP)
                 tma_load_2d(sa + C::kW + j * kWBytes, &tmW, &full[stage], kc, wrow + p.w_up_offset);
-              for (int b = 0; b < nb; ++b)
-                tma_load_2d(sb + j * C::kTokSub + b * kTokBox * kBK * 2, &tmX, &full[stage], kc,
-                            t.row0 + b * kTokBox);
+              if (wide) {
+                for (int b = 0; b < nb64; ++b)
+                  tma_load_2d(sb + j * C::kTokSub + b * 64 * kBK * 2, &tmX64, &full[stage], kc,
+                              t.row0 + b * 64);
+              } else {
+                for (int b = 0; b < nb; ++b)
+                  tma_load_2d(sb + j * C::kTokSub + b * kTokBox * kBK * 2, &tmX, &full[stage], kc,
+                              t.row0 + b * kTokBox);
+              }
             }
             issued |= 1u << stage;
             issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
@@ -406,9 +418,11 @@ __global__ void __launch_bounds__(256) split_sum_kernel(const float* __restrict_
 template <bool GATE_UP, int STAGES, int CHUNK, int KSUB>
 cudaError_t run_decode(const DecodeGemmArgs& a, cudaStream_t s) {
   using C = DCfg<GATE_UP, STAGES, CHUNK, KSUB>;
-  CUtensorMap tw, tx;
+  CUtensorMap tw, tx, tx64;
   if (!make_tmap_bf16(&tw, a.w, a.w_rows, a.K, kM)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tx, a.x, a.x_rows, a.K, kTokBox)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&tx64, a.x, a.x_rows, a.K, 64))
+    return cudaErrorInvalidValue;
   DParams p;
   p.offsets = a.offsets;
   p.n_groups = a.n_groups;
@@ -430,7 +444,7 @@ cudaError_t run_decode(const DecodeGemmArgs& a, cudaStream_t s) {
   static bool attr_done[64] = {false};
   cudaError_t e = set_smem_once(kern, static_cast<int>(C::kSmemBytes), attr_done);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(a.sm_count), dim3(kThreads), C::kSmemBytes, s, tw, tx, p);
+  return launch_pdl(kern, dim3(a.sm_count), dim3(kThreads), C::kSmemBytes, s, tw, tx, tx64, p);
 }
 
 }  // namespace

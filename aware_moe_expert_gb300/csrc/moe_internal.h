@@ -56,6 +56,7 @@ struct GemmArgs {
   uint32_t debug_flags;
   int sm_count;
   int max_rows_hint;         // upper bound of total rows (grid sizing)
+  int bn_hint;               // EPI_F32: output columns per tile (64/128/256), 0 = all
 };
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s);

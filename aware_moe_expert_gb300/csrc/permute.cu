@@ -53,67 +53,72 @@ __global__ void __launch_bounds__(256) bitmap_kernel(const int32_t* __restrict__
     bitmap[static_cast<size_t>(u) * W + word] = bits[u];
 }
 
-// Single CTA, 1024 threads: warp w handles units w, w+32, ...; then warp 0
-// scans the unit counts into offsets.
-__global__ void __launch_bounds__(1024) scan_kernel(const uint32_t* __restrict__ bitmap, int E_r,
-                                                     int W, int32_t* __restrict__ wprefix,
-                                                     int32_t* __restrict__ counts,
-                                                     int32_t* __restrict__ offsets) {
-  __shared__ int32_t s_cnt[256];
+// One warp per unit: per-word popcounts of the unit's bitmap row turned
+// into exclusive word prefixes, and the unit's count.
+__global__ void __launch_bounds__(256) unit_scan_kernel(const uint32_t* __restrict__ bitmap,
+                                                         int E_r, int W,
+                                                         int32_t* __restrict__ wprefix,
+                                                         int32_t* __restrict__ counts) {
   pdl_wait_and_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int u = warp; u < E_r; u += 32) {
-    const uint32_t* row = bitmap + static_cast<size_t>(u) * W;
-    int32_t* pre = wprefix + static_cast<size_t>(u) * W;
-    int running = 0;
-    for (int w0 = 0; w0 < W; w0 += 32) {
-      const int w = w0 + lane;
-      const int c = w < W ? __popc(row[w]) : 0;
-      int incl = c;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
-      }
-      if (w < W) pre[w] = running + incl - c;
-      running += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) s_cnt[u] = running;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    // each lane owns a contiguous run of up to 8 units
-    const int per = (E_r + 31) / 32;
-    const int u0 = lane * per;
-    int local = 0;
-    for (int i = 0; i < per; ++i)
-      if (u0 + i < E_r) local += s_cnt[u0 + i];
-    int incl = local;
+  const int u = blockIdx.x * 8 + warp;
+  if (u >= E_r) return;
+  const uint32_t* row = bitmap + static_cast<size_t>(u) * W;
+  int32_t* pre = wprefix + static_cast<size_t>(u) * W;
+  int running = 0;
+  for (int w0 = 0; w0 < W; w0 += 32) {
+    const int w = w0 + lane;
+    const int c = w < W ? __popc(row[w]) : 0;
+    int incl = c;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const int o = __shfl_up_sync(0xffffffffu, incl, off);
       if (lane >= off) incl += o;
     }
-    int run = incl - local;
-    for (int i = 0; i < per; ++i) {
-      const int u = u0 + i;
-      if (u < E_r) {
-        offsets[u] = run;
-        counts[u] = s_cnt[u];
-        run += s_cnt[u];
-      }
-    }
-    if (lane == 31) offsets[E_r] = incl;
+    if (w < W) pre[w] = running + incl - c;
+    running += __shfl_sync(0xffffffffu, incl, 31);
   }
+  if (lane == 0) counts[u] = running;
 }
 
-// One thread per (t, j) slot.
+// Exclusive scan of counts[0..E_r) by warp 0 into s_off[0..E_r].
+__device__ __forceinline__ void scan_counts(const int32_t* counts, int E_r, int32_t* s_off,
+                                            int lane) {
+  const int per = (E_r + 31) / 32;
+  const int u0 = lane * per;
+  int local = 0;
+  for (int i = 0; i < per; ++i)
+    if (u0 + i < E_r) local += counts[u0 + i];
+  int incl = local;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  int run = incl - local;
+  for (int i = 0; i < per; ++i) {
+    const int u = u0 + i;
+    if (u < E_r) {
+      s_off[u] = run;
+      run += counts[u];
+    }
+  }
+  if (lane == 31) s_off[E_r] = incl;
+}
+
+// One thread per (t, j) slot.  Every CTA rebuilds the unit offsets from the
+// counts (E_r <= 256) in shared memory; CTA 0 also stores them.
 __global__ void __launch_bounds__(256) scatter_kernel(
     const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ kpt, int T, int k_max,
     int E_r, int W, const uint32_t* __restrict__ bitmap, const int32_t* __restrict__ wprefix,
-    const int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_token,
-    int32_t* __restrict__ inv_row) {
+    const int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ sorted_token, int32_t* __restrict__ inv_row) {
+  __shared__ int32_t s_off[257];
   pdl_wait_and_trigger();
+  if (threadIdx.x < 32) scan_counts(counts, E_r, s_off, threadIdx.x);
+  __syncthreads();
+  if (blockIdx.x == 0)
+    for (int u = threadIdx.x; u <= E_r; u += blockDim.x) offsets[u] = s_off[u];
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= static_cast<long long>(T) * k_max) return;
   const int t = static_cast<int>(i / k_max), j = static_cast<int>(i - static_cast<long long>(t) * k_max);
@@ -125,7 +130,7 @@ __global__ void __launch_bounds__(256) scatter_kernel(
       const int w = t >> 5;
       const uint32_t below = (1u << (t & 31)) - 1u;
       const size_t o = static_cast<size_t>(u) * W + w;
-      pos = offsets[u] + wprefix[o] + __popc(bitmap[o] & below);
+      pos = s_off[u] + wprefix[o] + __popc(bitmap[o] & below);
       sorted_token[pos] = t;
     }
   }
@@ -265,18 +270,16 @@ cudaError_t launch_permute(const int32_t* topk_idx, const int32_t* k_per_token, 
                                k_max, E_r, W, bitmap, status);
     if (e != cudaSuccess) return e;
   }
-  cudaError_t e = launch_pdl(scan_kernel, dim3(1), dim3(1024), 0, s,
-                             static_cast<const uint32_t*>(bitmap), E_r, W, wprefix, counts,
-                             offsets);
+  cudaError_t e = launch_pdl(unit_scan_kernel, dim3((E_r + 7) / 8), dim3(256), 0, s,
+                             static_cast<const uint32_t*>(bitmap), E_r, W, wprefix, counts);
   if (e != cudaSuccess) return e;
   const long long slots = static_cast<long long>(T) * k_max;
-  if (slots > 0) {
-    e = launch_pdl(scatter_kernel, dim3(static_cast<unsigned>((slots + 255) / 256)), dim3(256), 0,
-                   s, topk_idx, k_per_token, T, k_max, E_r, W,
-                   static_cast<const uint32_t*>(bitmap), static_cast<const int32_t*>(wprefix),
-                   static_cast<const int32_t*>(offsets), sorted_token, inv_row);
-    if (e != cudaSuccess) return e;
-  }
+  const unsigned blocks = static_cast<unsigned>(slots > 0 ? (slots + 255) / 256 : 1);
+  e = launch_pdl(scatter_kernel, dim3(blocks), dim3(256), 0, s, topk_idx, k_per_token, T, k_max,
+                 E_r, W, static_cast<const uint32_t*>(bitmap),
+                 static_cast<const int32_t*>(wprefix), static_cast<const int32_t*>(counts),
+                 offsets, sorted_token, inv_row);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

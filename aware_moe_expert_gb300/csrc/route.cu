@@ -83,29 +83,24 @@ __device__ __forceinline__ uint32_t order_key(float L) {
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-// One warp per token.  Lane l holds units l, l+32, ... (IPL per lane).
-// Round j picks the best remaining unit with a 64-bit warp max over
-// (key << 32 | ~u), so equal keys resolve to the lower unit index.
+// One warp selects the k_t best units of one token.  Lane l holds units l,
+// l+32, ... (IPL per lane).  Round j picks the best remaining unit with a
+// 64-bit warp max over (key << 32 | ~u), so equal keys resolve to the lower
+// unit index.  On return lane j < k holds the j-th unit (*out_u) and its gate
+// weight after renormalisation and route_scale (*out_w); returns k.
 template <int IPL>
-__global__ void __launch_bounds__(256) topk_gate_kernel(
-    const float* __restrict__ logits, const int32_t* __restrict__ kpt, int T, int E_r,
-    int k_max, int score, int renorm, float route_scale, int32_t* __restrict__ topk_idx,
-    float* __restrict__ topk_w, int32_t* status) {
-  pdl_wait_and_trigger();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + warp;
-  if (t >= T) return;
-  int k = kpt[t];
+__device__ __forceinline__ int warp_topk(const float* __restrict__ row, int kt, int E_r, int k_max,
+                                         int score, int renorm, float route_scale,
+                                         int32_t* status, int lane, int* out_u, float* out_w) {
+  int k = kt;
   if (k < 1 || k > k_max) {
     if (lane == 0) report(status, MOE_ERR_K_RANGE);
     k = min(max(k, 0), k_max);
   }
   k = min(k, E_r);
-
   float v[IPL];
   uint32_t key[IPL];
   bool bad = false;
-  const float* row = logits + static_cast<size_t>(t) * E_r;
 #pragma unroll
   for (int i = 0; i < IPL; ++i) {
     const int u = lane + 32 * i;
@@ -174,16 +169,29 @@ __global__ void __launch_bounds__(256) topk_gate_kernel(
   float selsum = lane < k ? my_s : 0.f;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) selsum += __shfl_xor_sync(0xffffffffu, selsum, off);
+  *out_u = lane < k ? my_u : -1;
+  *out_w = lane < k ? (renorm ? my_s / selsum : my_s) * route_scale : 0.f;
+  return k;
+}
+
+// One warp per token, eight tokens per CTA.
+template <int IPL>
+__global__ void __launch_bounds__(256) topk_gate_kernel(
+    const float* __restrict__ logits, const int32_t* __restrict__ kpt, int T, int E_r,
+    int k_max, int score, int renorm, float route_scale, int32_t* __restrict__ topk_idx,
+    float* __restrict__ topk_w, int32_t* status) {
+  pdl_wait_and_trigger();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  int u;
+  float w;
+  warp_topk<IPL>(logits + static_cast<size_t>(t) * E_r, kpt[t], E_r, k_max, score, renorm,
+                 route_scale, status, lane, &u, &w);
   if (lane < k_max) {
     const size_t o = static_cast<size_t>(t) * k_max + lane;
-    if (lane < k) {
-      const float w = renorm ? my_s / selsum : my_s;
-      topk_idx[o] = my_u;
-      topk_w[o] = w * route_scale;
-    } else {
-      topk_idx[o] = -1;
-      topk_w[o] = 0.f;
-    }
+    topk_idx[o] = u;
+    topk_w[o] = w;
   }
 }
 

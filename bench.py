@@ -204,9 +204,18 @@ def run_ours(args, wl, rank, world, local):
         for _, f in calls:
             f(sp)
 
+    out_fused = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    ws_fused = torch.empty(B.moe_workspace_size(desc), dtype=torch.uint8, device=dev)
+
+    def layer_step(sp):
+        B.check(B.moe_layer_forward(desc, d["x"], d["router_w"], d["w_gate_up"], d["w_down"],
+                                    d["k_per_token"], out_fused, st, ws_fused, sp),
+                "moe_layer_forward")
+
     # one eager pass: realised routing statistics, per-device set-up
     with torch.cuda.stream(stream):
         step(sp)
+        layer_step(sp)
     torch.cuda.synchronize(dev)
     code = B.moe_get_device_status(st, sp)
     if code != 0:
@@ -216,14 +225,15 @@ def run_ours(args, wl, rank, world, local):
     D = int(np.count_nonzero(cnt))
 
     # The step is replayed from CUDA graphs so that the device timeline is
-    # not stretched by host enqueue time: one graph of the whole step (the
-    # timed value) and one graph per call (the per-call breakdown).
+    # not stretched by host enqueue time: one graph of moe_layer_forward (the
+    # whole step, the timed value) and one graph per component call (the
+    # per-call breakdown and the dominant call's roofline).
     def capture(fn):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
             fn(torch.cuda.current_stream().cuda_stream)
         return g
-    g_full = capture(step)
+    g_full = capture(layer_step)
     g_parts = [(n, capture(f)) for n, f in calls]
 
     # L2 handling: flush with a 2x-L2 write between steps unless the step
@@ -371,7 +381,7 @@ def run_ours(args, wl, rank, world, local):
                 "kernel": "moe_gate_up (row gather + grouped gate|up GEMM, SwiGLU epilogue)",
                 "algorithmic_flops": alg, "peak_source": peaks["source"] + " bf16_tflops (burst)"}
 
-    n_launch = launches_per_step(wl, T)
+    n_launch = launches_per_step(wl, T, args.path)
     us = ms * 1000.0
     res = {
         "metric": METRIC,
@@ -410,17 +420,24 @@ def run_ours(args, wl, rank, world, local):
     return res, d
 
 
-def launches_per_step(wl, T):
-    """Kernels libmoe enqueues per step (mirrors the host sequencing)."""
-    n = 0
-    tensor_router = T >= 128 and wl.E_r in (64, 128, 256)
-    n += 1 + 1                 # logits (GEMM or CUDA-core) + top-k
-    n += (1 if T > 0 else 0) + 1 + (1 if T > 0 else 0)   # bitmap, scan, scatter
-    n += 2 if wl.I_shared else 0
-    n += 2                     # gather + gate|up GEMM
-    n += 1                     # down GEMM
-    n += 1                     # combine
-    del tensor_router
+def launches_per_step(wl, T, path=0):
+    """Kernels libmoe enqueues per step (mirrors the host sequencing in
+    csrc/api.cu: router + top-k, permutation, [shared expert], gate|up (+ the
+    split-K reduction of the weight-stationary family), down (+ its split
+    reduction), combine)."""
+    n_cap = T * wl.k_max
+    decode = path == 2 or (path == 0 and n_cap <= 64 * wl.E_r)
+    budget = 256 << 20
+    n = 2                                            # logits, top-k
+    n += 1 if (T + 31) // 32 <= 8 else 3            # permutation (one CTA, or bitmap/scan/scatter)
+    n += 2 if wl.I_shared else 0                     # shared expert gate|up, down
+    n += 2                                           # row gather + gate|up GEMM
+    if decode and wl.I_sub % 128 == 0:
+        n += 1 if budget // max(n_cap * 2 * wl.I_sub * 4, 1) >= 2 else 0
+    n += 1                                           # down GEMM
+    if decode and wl.H % 128 == 0:
+        n += 1 if budget // max(n_cap * wl.H * 4, 1) >= 2 else 0
+    n += 1                                           # combine
     return n
 
 

@@ -123,3 +123,34 @@ def test_full_size_routing_and_permutation_bit_exact(name):
     np.testing.assert_array_equal(st_tok.cpu().numpy()[: int(wo[-1])], wst)
     np.testing.assert_array_equal(inv.cpu().numpy().reshape(wl.T, wl.k_max), winv)
     assert int(wo[-1]) == int(kn.sum())
+
+
+@pytest.mark.parametrize("name,T", [("tiny", None), ("qwen_decode", 64), ("qwen_decode", 256),
+                                    ("qwen_decode", 300), ("mixtral_decode", None)])
+def test_layer_forward_equals_component_calls(name, T):
+    """moe_layer_forward gives bit-identical results to moe_route ->
+    moe_permute -> moe_grouped_ffn -> moe_combine on the same inputs."""
+    wl = WL.ALL[name] if T is None else WL.ALL[name].with_T(T)
+    d = make_layer_inputs(wl, DEV)
+    desc = B.desc_for(wl, expert_bias=d["expert_bias"])
+    layer = B.MoeLayer(desc, DEV)
+    out = layer.forward(d["x"], d["router_w"], d["w_gate_up"], d["w_down"], d["k_per_token"])
+    assert layer.device_status() == 0
+    Tt, k_max, E_r = wl.T, wl.k_max, wl.E_r
+    ws = torch.empty(B.moe_workspace_size(desc), dtype=torch.uint8, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    idx = torch.empty(Tt, k_max, dtype=torch.int32, device=DEV)
+    w = torch.empty(Tt, k_max, dtype=torch.float32, device=DEV)
+    counts = torch.empty(E_r, dtype=torch.int32, device=DEV)
+    offsets = torch.empty(E_r + 1, dtype=torch.int32, device=DEV)
+    st_tok = torch.empty(Tt * k_max, dtype=torch.int32, device=DEV)
+    inv = torch.empty(Tt * k_max, dtype=torch.int32, device=DEV)
+    y = torch.empty(Tt * k_max, wl.H, dtype=torch.bfloat16, device=DEV)
+    out2 = torch.empty(Tt, wl.H, dtype=torch.bfloat16, device=DEV)
+    B.check(B.moe_route(desc, d["x"], d["router_w"], None, d["k_per_token"], None, idx, w, st, ws))
+    B.check(B.moe_permute(desc, idx, d["k_per_token"], counts, offsets, st_tok, inv, st, ws))
+    B.check(B.moe_grouped_ffn(desc, d["x"], st_tok, offsets, d["w_gate_up"], d["w_down"], y, st,
+                              ws))
+    B.check(B.moe_combine(desc, y, None, inv, w, d["k_per_token"], out2, st))
+    assert B.moe_get_device_status(st) == 0
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))

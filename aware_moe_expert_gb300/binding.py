@@ -28,7 +28,7 @@ DEBUG_SKIP_FIRST_LOAD = 1
 
 EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_gate_up", "moe_down",
            "moe_grouped_ffn", "moe_shared_ffn", "moe_combine", "moe_layer_forward",
-           "moe_get_device_status", "moe_status_string")
+           "moe_get_device_status", "moe_status_string", "moe_permute_static")
 
 
 class MoeLayerDesc(ctypes.Structure):
@@ -64,6 +64,8 @@ def lib() -> ctypes.CDLL:
             "moe_workspace_size": (ctypes.c_size_t, [D]),
             "moe_route": (ctypes.c_int, [D, vp, vp, vp, i32p, vp, i32p, vp, i32p, vp, vp]),
             "moe_permute": (ctypes.c_int, [D, i32p, i32p, i32p, i32p, i32p, i32p, i32p, vp, vp]),
+            "moe_permute_static": (ctypes.c_int, [D, i32p, i32p, i32p, i32p, i32p, i32p, i32p,
+                                                  vp]),
             "moe_gate_up": (ctypes.c_int, [D, vp, i32p, i32p, vp, vp, i32p, vp, vp]),
             "moe_down": (ctypes.c_int, [D, vp, i32p, vp, vp, i32p, vp, vp]),
             "moe_grouped_ffn": (ctypes.c_int, [D, vp, i32p, i32p, vp, vp, vp, i32p, vp, vp]),
@@ -165,6 +167,16 @@ def moe_permute(desc, topk_idx, k_per_token, counts, offsets, sorted_token, inv_
     return lib().moe_permute(ctypes.byref(d), _ptr(topk_idx), _ptr(k_per_token), _ptr(counts),
                              _ptr(offsets), _ptr(sorted_token), _ptr(inv_row), _ptr(dev_status),
                              _ptr(workspace), _stream(stream))
+
+
+def moe_permute_static(desc, topk_idx, k_per_token, counts, offsets, sorted_token, inv_row,
+                       dev_status, stream=None) -> int:
+    """moe_permute with its scratch in the library's own device array (no
+    workspace argument, nothing allocated)."""
+    d = desc.c()
+    return lib().moe_permute_static(ctypes.byref(d), _ptr(topk_idx), _ptr(k_per_token),
+                                    _ptr(counts), _ptr(offsets), _ptr(sorted_token),
+                                    _ptr(inv_row), _ptr(dev_status), _stream(stream))
 
 
 def moe_gate_up(desc, x, sorted_token, offsets, w_gate_up, act, dev_status, workspace,

@@ -161,6 +161,25 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, const vo
                              const int32_t* k_per_token, void* out, int32_t* dev_status,
                              void* workspace, void* stream);
 
+/* moe_permute without a workspace, for callers that cannot allocate device
+ * memory where they route (while a stream is being captured into a CUDA
+ * graph, inside a serving loop that must stay out of the allocator, or in a
+ * plug-in that owns no buffers of its own).  The published method has no
+ * counterpart to this call: it only changes where the scratch lives.
+ *   Arguments and results are those of moe_permute, minus `workspace`.
+ *   Scratch: a 1 MiB array in device memory that every GPU loading this
+ *   library keeps until exit; 2 * E_r * ceil(T/32) * 4 bytes must fit, else
+ *   MOE_ERR_UNSUPPORTED_SHAPE (e.g. E_r = 256 allows T <= 16384).
+ *   The first call on a device looks up the array's device address (a
+ *   runtime call); make that first call before any stream capture.
+ *   All calls share the array: calls whose kernels may overlap on the GPU
+ *   race and must not be issued.  Nothing in it needs clearing between calls.
+ *   Allocates nothing (no cudaMalloc, cudaFree or allocating library call). */
+moe_status moe_permute_static(const moe_layer_desc* desc, const int32_t* topk_idx,
+                              const int32_t* k_per_token, int32_t* counts, int32_t* offsets,
+                              int32_t* sorted_token, int32_t* inv_row, int32_t* dev_status,
+                              void* stream);
+
 /* Synchronises `stream`, then returns the code stored in *dev_status
  * (MOE_OK if zero), or MOE_ERR_CUDA if the synchronisation itself failed. */
 moe_status moe_get_device_status(const int32_t* dev_status, void* stream);

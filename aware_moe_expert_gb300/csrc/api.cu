@@ -139,8 +139,8 @@ inline int E_r_of(const moe_layer_desc* d) { return d->n_experts * d->n_sub; }
 
 // Decode-shaped batches (at most 64 rows per routing unit on average, from
 // the T * k_max bound) run the swap-AB kernels; desc->path forces either.
-bool use_decode_path(const moe_layer_desc* d, int n_out) {
-  if (!moe::decode_gemm_supports(n_out)) return false;
+bool use_decode_path(const moe_layer_desc* d, int n_out, bool gate_up) {
+  if (!moe::decode_gemm_supports(n_out, gate_up)) return false;
   if (d->path == MOE_PATH_DECODE) return true;
   if (d->path == MOE_PATH_PREFILL) return false;
   return static_cast<long long>(d->T) * d->k_max <= 64ll * E_r_of(d);
@@ -225,7 +225,7 @@ moe_status do_gate_up(const moe_layer_desc* d, const void* x, const int32_t* sor
   MOE_TRY(cuda_status(moe::launch_gather_rows(x, sorted_token, offsets, E_r, d->T, d->H,
                                               static_cast<int>(n_cap), xperm, status,
                                               sm_count(), s)));
-  if (use_decode_path(d, d->I_sub)) {
+  if (use_decode_path(d, d->I_sub, true)) {
     moe::DecodeGemmArgs a{};
     a.gate_up = true;
     a.w = w_gate_up;
@@ -274,7 +274,7 @@ moe_status do_down(const moe_layer_desc* d, const void* act, const int32_t* offs
   const int E_r = E_r_of(d);
   const long long n_cap = static_cast<long long>(d->T) * d->k_max;
   if (n_cap == 0) return MOE_OK;
-  if (use_decode_path(d, d->H)) {
+  if (use_decode_path(d, d->H, false)) {
     moe::DecodeGemmArgs a{};
     a.gate_up = false;
     a.w = w_down;

@@ -28,6 +28,7 @@ namespace {
 
 constexpr int kBK = 64;           // columns of one 128-byte swizzled sub-block
 constexpr int kM = 128;           // weight rows per item (MMA M)
+constexpr int kGU = 64;           // gate|up: neurons per item (64 gate rows over 64 up rows)
 constexpr int kTokBox = 16;       // token rows per TMA box
 constexpr int kThreads = 192;
 constexpr uint32_t kWBytes = kM * kBK * 2;  // one weight sub-block: 16 KB
@@ -57,10 +58,10 @@ struct DParams {
 template <bool GATE_UP, int STAGES, int CHUNK, int KSUB>
 struct DCfg {
   static constexpr uint32_t kW = kWBytes * KSUB;                        // one weight tile
-  static constexpr uint32_t kA = GATE_UP ? 2 * kW : kW;
+  static constexpr uint32_t kA = kW;  // gate|up: 64 gate rows stacked over 64 up rows
   static constexpr uint32_t kTokSub = CHUNK * kBK * 2;                  // tokens, one sub-block
   static constexpr uint32_t kTokBytes = kTokSub * KSUB;
-  static constexpr uint32_t kSlot = GATE_UP ? 2 * CHUNK : CHUNK;        // TMEM columns per slot
+  static constexpr uint32_t kSlot = CHUNK;                              // TMEM columns per slot
   static constexpr uint32_t kStage = kA + kTokBytes;
   static constexpr uint32_t kOffB = STAGES * kA;
   static constexpr uint32_t kOffBar = STAGES * kStage;
@@ -68,7 +69,9 @@ struct DCfg {
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
   static constexpr uint32_t kOffPrefix = kOffMisc + 16;
   static constexpr uint32_t kOffOffs = kOffPrefix + (kMaxGroups + 1) * 4;
-  static constexpr uint32_t kSmemBytes = kOffOffs + (kMaxGroups + 1) * 4 + 1024;
+  static constexpr uint32_t kOffX = (kOffOffs + (kMaxGroups + 1) * 4 + 15) / 16 * 16;
+  static constexpr uint32_t kXBytes = GATE_UP ? kGU * 17 * 4 : 0;  // up values for gate warps
+  static constexpr uint32_t kSmemBytes = kOffX + kXBytes + 1024;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
   static_assert(2 * kSlot <= kTmemCols, "two accumulator slots in TMEM");
   static_assert(CHUNK % 16 == 0 && CHUNK <= 256 && CHUNK >= 64, "tcgen05 N for M = 128");
@@ -129,6 +132,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* s_total = reinterpret_cast<int*>(smem + C::kOffMisc + 8);
   int* s_prefix = reinterpret_cast<int*>(smem + C::kOffPrefix);
   int* s_offs = reinterpret_cast<int*>(smem + C::kOffOffs);
+  float* s_xchg = reinterpret_cast<float*>(smem + C::kOffX);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_wait_and_trigger();
 
@@ -185,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nb64 = (t.rows + 63) / 64;
         const uint32_t tok_rows = wide ? 64u * nb64 : static_cast<uint32_t>(nb * kTokBox);
         const uint32_t bytes = C::kA + KSUB * tok_rows * kBK * 2;
-        const int wrow = t.g * p.w_group_rows + m * kM;
+        const int wrow = t.g * p.w_group_rows + m * (GATE_UP ? kGU : kM);
         const int kb0 = s * KB / S, kb1 = (s + 1) * KB / S;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, s_abort)) {
@@ -202,8 +206,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < KSUB; ++j) {
               const int kc = (kb * KSUB + j) * kBK;
               tma_load_2d(sa + j * kWBytes, &tmW, &full[stage], kc, wrow);
-              if (GATE_UP)
-                tma_load_2d(sa + C::kW + j * kWBytes, &tmW, &full[stage], kc, wrow + p.w_up_offset);
+              if (GATE_UP)  // up rows of the same 64 neurons fill the lower half of the tile
+                tma_load_2d(sa + j * kWBytes + kGU * kBK * 2, &tmW, &full[stage], kc,
+                            wrow + p.w_up_offset);
               if (wide) {
                 for (int b = 0; b < nb64; ++b)
                   tma_load_2d(sb + j * C::kTokSub + b * 64 * kBK * 2, &tmX64, &full[stage], kc,
@@ -247,7 +252,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t dg = tmem_base + static_cast<uint32_t>(acc) * C::kSlot;
-        const uint32_t du = dg + static_cast<uint32_t>(CHUNK);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full[stage], phase, s_abort)) {
             ok = false;
@@ -257,14 +261,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < KSUB; ++j) {
             const uint64_t ag = sdesc_sw128(smem_u32(smem + stage * C::kA + j * kWBytes));
-            const uint64_t au = sdesc_sw128(smem_u32(smem + stage * C::kA + C::kW + j * kWBytes));
             const uint64_t bx =
                 sdesc_sw128(smem_u32(smem + C::kOffB + stage * C::kTokBytes + j * C::kTokSub));
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k) {
               const uint32_t accum = (kb != kb0 || j != 0 || k != 0) ? 1u : 0u;
               umma_bf16(dg, ag + 2u * k, bx + 2u * k, idesc, accum);
-              if (GATE_UP) umma_bf16(du, au + 2u * k, bx + 2u * k, idesc, accum);
             }
           }
           umma_commit(&empty[stage]);
@@ -305,33 +307,58 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t tg = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                           static_cast<uint32_t>(acc) * C::kSlot;
-      const int col = m * kM + r_in;  // output column of this thread
-      for (int c0 = 0; c0 < t.rows; c0 += 16) {
-        uint32_t gv[16], uv[16];
-        tmem_ld16(tg + c0, gv);
-        if (GATE_UP) tmem_ld16(tg + static_cast<uint32_t>(CHUNK) + c0, uv);
-        tmem_ld_wait();
+      if (GATE_UP) {
+        // TMEM lanes 0-63 hold the gate rows, 64-127 the up rows of the same
+        // 64 neurons: warps of quadrants 2-3 hand their up values to the
+        // gate warps (quadrants 0-1) through shared memory.
+        const bool is_gate = q < 2;
+        const int nl = (q & 1) * 32 + lane;
+        const int col = m * kGU + nl;
+        for (int c0 = 0; c0 < t.rows; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(tg + c0, v);
+          tmem_ld_wait();
+          if (S > 1) {
 #pragma unroll
-        for (int cc = 0; cc < 16; ++cc) {
-          const int c = c0 + cc;
-          if (c < t.rows) {
-            const long long r = static_cast<long long>(t.row0) + c;
-            if (r >= p.out_rows) continue;
-            const float g = __uint_as_float(gv[cc]);
-            if (GATE_UP) {
-              const float u = __uint_as_float(uv[cc]);
-              if (S == 1) {
-                static_cast<__nv_bfloat16*>(p.out)[r * p.n_out + col] =
-                    __float2bfloat16_rn(silu_f(g) * u);
-              } else {
-                float* prow = p.partial + (static_cast<long long>(s) * p.out_rows + r) * 2 * p.n_out;
-                prow[col] = g;
-                prow[p.n_out + col] = u;
+            for (int cc = 0; cc < 16; ++cc) {
+              const long long r = static_cast<long long>(t.row0) + c0 + cc;
+              if (c0 + cc < t.rows && r < p.out_rows)
+                p.partial[(static_cast<long long>(s) * p.out_rows + r) * 2 * p.n_out +
+                          (is_gate ? 0 : p.n_out) + col] = __uint_as_float(v[cc]);
+            }
+          } else {
+            if (!is_gate) {
+#pragma unroll
+              for (int cc = 0; cc < 16; ++cc) s_xchg[nl * 17 + cc] = __uint_as_float(v[cc]);
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (is_gate) {
+#pragma unroll
+              for (int cc = 0; cc < 16; ++cc) {
+                const long long r = static_cast<long long>(t.row0) + c0 + cc;
+                if (c0 + cc < t.rows && r < p.out_rows)
+                  static_cast<__nv_bfloat16*>(p.out)[r * p.n_out + col] = __float2bfloat16_rn(
+                      silu_f(__uint_as_float(v[cc])) * s_xchg[nl * 17 + cc]);
               }
-            } else if (S == 1) {
-              static_cast<__nv_bfloat16*>(p.out)[r * p.n_out + col] = __float2bfloat16_rn(g);
-            } else {
-              p.partial[(static_cast<long long>(s) * p.out_rows + r) * p.n_out + col] = g;
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+          }
+        }
+      } else {
+        const int col = m * kM + r_in;  // output column of this thread
+        for (int c0 = 0; c0 < t.rows; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(tg + c0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int cc = 0; cc < 16; ++cc) {
+            const long long r = static_cast<long long>(t.row0) + c0 + cc;
+            if (c0 + cc < t.rows && r < p.out_rows) {
+              const float g = __uint_as_float(v[cc]);
+              if (S == 1)
+                static_cast<__nv_bfloat16*>(p.out)[r * p.n_out + col] = __float2bfloat16_rn(g);
+              else
+                p.partial[(static_cast<long long>(s) * p.out_rows + r) * p.n_out + col] = g;
             }
           }
         }
@@ -419,7 +446,7 @@ template <bool GATE_UP, int STAGES, int CHUNK, int KSUB>
 cudaError_t run_decode(const DecodeGemmArgs& a, cudaStream_t s) {
   using C = DCfg<GATE_UP, STAGES, CHUNK, KSUB>;
   CUtensorMap tw, tx, tx64;
-  if (!make_tmap_bf16(&tw, a.w, a.w_rows, a.K, kM)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&tw, a.w, a.w_rows, a.K, GATE_UP ? kGU : kM)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tx, a.x, a.x_rows, a.K, kTokBox)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tx64, a.x, a.x_rows, a.K, 64))
     return cudaErrorInvalidValue;
@@ -427,7 +454,7 @@ cudaError_t run_decode(const DecodeGemmArgs& a, cudaStream_t s) {
   p.offsets = a.offsets;
   p.n_groups = a.n_groups;
   p.K = a.K;
-  p.m_tiles = a.n_out / kM;
+  p.m_tiles = a.n_out / (GATE_UP ? kGU : kM);
   p.w_group_rows = a.w_group_rows;
   p.w_up_offset = GATE_UP ? a.n_out : 0;
   p.n_out = a.n_out;
@@ -438,7 +465,7 @@ cudaError_t run_decode(const DecodeGemmArgs& a, cudaStream_t s) {
   p.max_split = a.max_split;
   p.status = a.status;
   p.debug_flags = a.debug_flags;
-  p.item_bytes = static_cast<float>(GATE_UP ? 2 * kM : kM) * a.K * 2.f;
+  p.item_bytes = static_cast<float>(kM) * a.K * 2.f;
   p.total_scale = 1.f / 6200.f;  // ~6.2 TB/s sustained weight streaming
   auto kern = decode_gemm_kernel<GATE_UP, STAGES, CHUNK, KSUB>;
   static bool attr_done[64] = {false};
@@ -449,13 +476,20 @@ cudaError_t run_decode(const DecodeGemmArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-bool decode_gemm_supports(int n_out) { return n_out % kM == 0; }
+bool decode_gemm_supports(int n_out, bool gate_up) {
+  return n_out % (gate_up ? kGU : kM) == 0;
+}
 
 cudaError_t launch_decode_gemm(const DecodeGemmArgs& a, cudaStream_t s) {
   if (a.x_rows <= 0) return cudaSuccess;
   if (a.gate_up) {
-    cudaError_t e = a.chunk <= 64 ? run_decode<true, 5, 64, 1>(a, s)
-                                  : run_decode<true, 4, 128, 1>(a, s);
+    cudaError_t e;
+    if (a.chunk > 64)
+      e = run_decode<true, 6, 128, 1>(a, s);
+    else if (a.K % 128 == 0)
+      e = run_decode<true, 4, 64, 2>(a, s);
+    else
+      e = run_decode<true, 8, 64, 1>(a, s);
     if (e != cudaSuccess || a.max_split <= 1) return e;
     return launch_pdl(split_swiglu_kernel, dim3(a.sm_count * 4), dim3(256), 0, s,
                       static_cast<const float*>(a.partial),

@@ -85,7 +85,7 @@ struct DecodeGemmArgs {
 };
 
 cudaError_t launch_decode_gemm(const DecodeGemmArgs& a, cudaStream_t s);
-bool decode_gemm_supports(int n_out);
+bool decode_gemm_supports(int n_out, bool gate_up);
 
 // bf16 [rows, cols] row-major tensor map: box of 64 columns x box_rows rows,
 // 128-byte swizzle, zero fill out of bounds.

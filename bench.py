@@ -432,7 +432,7 @@ def launches_per_step(wl, T, path=0):
     n += 1 if (T + 31) // 32 <= 8 else 3            # permutation (one CTA, or bitmap/scan/scatter)
     n += 2 if wl.I_shared else 0                     # shared expert gate|up, down
     n += 2                                           # row gather + gate|up GEMM
-    if decode and wl.I_sub % 128 == 0:
+    if decode and wl.I_sub % 64 == 0:
         n += 1 if budget // max(n_cap * 2 * wl.I_sub * 4, 1) >= 2 else 0
     n += 1                                           # down GEMM
     if decode and wl.H % 128 == 0:

@@ -17,8 +17,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "libmoe.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
-SOURCES = ["api.cu", "route.cu", "permute.cu", "gemm.cu", "gemm_decode.cu", "combine.cu",
-           "noalloc.cu"]
+SOURCES = ["api.cu", "route.cu", "permute.cu", "gemm.cu", "gemm_decode.cu", "ffn_decode.cu",
+           "combine.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include")]

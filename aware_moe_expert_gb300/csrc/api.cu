@@ -23,7 +23,7 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 // Byte offsets of every workspace region for one desc.
 struct Layout {
   size_t logits, topk_idx, topk_w, counts, offsets, sorted_token, inv_row, bitmap, wprefix, xperm,
-      act, yperm, act_sh, ysh, split_word, partial, total;
+      act, yperm, act_sh, ysh, split_word, partial, chunk_done, total;
   int max_split;       // K splits the decode gate|up kernel may use (1: none)
   int max_split_down;  // K splits the decode down kernel may use
 };
@@ -57,6 +57,7 @@ Layout layout_of(const moe_layer_desc& d) {
   l.act_sh = take(T * static_cast<size_t>(d.I_shared) * 2);
   l.ysh = take(T * static_cast<size_t>(d.H) * 2);
   l.split_word = take(16);
+  l.chunk_done = take((n_cap / 64 + E_r + 1) * 4);
   auto splits = [](size_t per_split) {
     size_t ms = per_split > 0 ? kPartialBudget / per_split : 1;
     return static_cast<int>(ms < 1 ? 1 : (ms > kMaxSplit ? kMaxSplit : ms));
@@ -319,6 +320,47 @@ moe_status do_down(const moe_layer_desc* d, const void* act, const int32_t* offs
   return cuda_status(moe::launch_gemm(g, s));
 }
 
+// Both FFN projections.  Decode-shaped batches with H and I_sub multiples of
+// 128 run the fused kernel (gate|up and down overlapped in one launch);
+// otherwise gate|up then down.
+moe_status do_grouped_ffn(const moe_layer_desc* d, const void* x, const int32_t* sorted_token,
+                          const int32_t* offsets, const void* w_gate_up, const void* w_down,
+                          void* y_perm, int32_t* status, void* ws, cudaStream_t s) {
+  const Layout l = layout_of(*d);
+  void* act = at<void>(ws, l.act);
+  const long long n_cap = static_cast<long long>(d->T) * d->k_max;
+  if (n_cap == 0) return MOE_OK;
+  if (use_decode_path(d, d->I_sub, true) && use_decode_path(d, d->H, false) &&
+      moe::decode_ffn_supports(d->H, d->I_sub)) {
+    const int E_r = E_r_of(d);
+    void* xperm = at<void>(ws, l.xperm);
+    int32_t* done = at<int32_t>(ws, l.chunk_done);
+    const int n_done = static_cast<int>(n_cap / 64 + E_r + 1);
+    MOE_TRY(cuda_status(moe::launch_gather_rows(x, sorted_token, offsets, E_r, d->T, d->H,
+                                                static_cast<int>(n_cap), xperm, status,
+                                                sm_count(), s, done, n_done)));
+    moe::DecodeFfnArgs a{};
+    a.x_perm = xperm;
+    a.x_rows = n_cap;
+    a.w_gate_up = w_gate_up;
+    a.w_down = w_down;
+    a.offsets = offsets;
+    a.n_groups = E_r;
+    a.H = d->H;
+    a.I = d->I_sub;
+    a.act = act;
+    a.y = y_perm;
+    a.done = done;
+    a.rows = n_cap;
+    a.status = status;
+    a.debug_flags = d->debug_flags;
+    a.sm_count = sm_count();
+    return cuda_status(moe::launch_decode_ffn(a, s));
+  }
+  MOE_TRY(do_gate_up(d, x, sorted_token, offsets, w_gate_up, act, status, ws, s));
+  return do_down(d, act, offsets, w_down, y_perm, status, ws, s);
+}
+
 moe_status do_shared(const moe_layer_desc* d, const void* x, void* y_shared, int32_t* status,
                      void* ws, cudaStream_t s) {
   if (d->T == 0) return MOE_OK;
@@ -447,10 +489,8 @@ moe_status moe_grouped_ffn(const moe_layer_desc* desc, const void* x,
   MOE_TRY(check_ptrs({x, w_gate_up, w_down, y_perm}));
   MOE_TRY(check_ptrs4({sorted_token, offsets, dev_status}));
   MOE_TRY(check_ws(workspace));
-  const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  void* act = at<void>(workspace, layout_of(*desc).act);
-  MOE_TRY(do_gate_up(desc, x, sorted_token, offsets, w_gate_up, act, dev_status, workspace, s));
-  return do_down(desc, act, offsets, w_down, y_perm, dev_status, workspace, s);
+  return do_grouped_ffn(desc, x, sorted_token, offsets, w_gate_up, w_down, y_perm, dev_status,
+                        workspace, static_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_shared_ffn(const moe_layer_desc* desc, const void* x, void* y_shared,
@@ -501,8 +541,8 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, const vo
   MOE_TRY(do_permute(desc, topk_idx, k_per_token, counts, offsets, sorted_token, inv_row,
                      dev_status, workspace, s));
   if (ysh != nullptr) MOE_TRY(do_shared(desc, x, ysh, dev_status, workspace, s));
-  MOE_TRY(do_gate_up(desc, x, sorted_token, offsets, w_gate_up, act, dev_status, workspace, s));
-  MOE_TRY(do_down(desc, act, offsets, w_down, yperm, dev_status, workspace, s));
+  MOE_TRY(do_grouped_ffn(desc, x, sorted_token, offsets, w_gate_up, w_down, yperm, dev_status,
+                         workspace, s));
   return do_combine(desc, yperm, ysh, inv_row, topk_w, k_per_token, out, dev_status, s);
 }
 

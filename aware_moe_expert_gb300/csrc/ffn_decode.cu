@@ -1,0 +1,431 @@
+// Fused decode FFN: the grouped gate|up (with SwiGLU) and the grouped down
+// projection of decode-sized batches in ONE persistent tcgen05 kernel.
+//
+// Decode is bound by the bytes of the activated sub-experts' weights
+// (METRO, "Balancing Activated Experts (not Tokens) for Memory-Bound MoE
+// Serving", §1-2); each weight byte is read once per step.  Running the two
+// projections as separate launches leaves a launch gap and an idle tail
+// between them.  Here every CTA walks one list: all gate|up items first,
+// then all down items.  A down item streams its first weight stages at once
+// and only its activation loads wait for the gate|up items of its token chunk
+// (a per-chunk completion counter, bounded wait), so the down weight stream
+// overlaps the end of the gate|up phase (MoE-Prism, arXiv 2510.19366, §III-B1
+// Eq. (1): A = SiLU(X Wg) * (X Wu), X' = A Wdown).
+//
+// Item shapes (weight-stationary, "swap AB"): 128 weight rows are the MMA M
+// side and a unit's token chunk (<= 64 rows) the N side.
+//   gate|up item: 64 gate rows over the matching 64 up rows, K = H;
+//                 TMEM lanes 0-63 gate, 64-127 up; up warps hand their values
+//                 to the gate warps through shared memory; act is bf16.
+//   down item:    128 rows of Wdown, K = I_sub; y_perm is bf16.
+// Each pipeline stage carries two 64-column sub-blocks (H and I_sub are
+// multiples of 128).  Roles: warp 0 TMA producer, warp 1 TMEM owner and MMA
+// issuer, warps 2-5 epilogue.  Every wait is bounded.
+#include "gemm_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kBK = 64;
+constexpr int kKsub = 2;                       // 64-column sub-blocks per stage
+constexpr int kM = 128;
+constexpr int kGU = 64;                        // neurons per gate|up item
+constexpr int kChunk = 64;                     // tokens per item
+constexpr int kTokBox = 16;
+constexpr int kThreads = 192;
+constexpr int kStages = 4;
+constexpr uint32_t kWSub = kM * kBK * 2;        // 16 KB per weight sub-block
+constexpr uint32_t kW = kWSub * kKsub;          // 32 KB
+constexpr uint32_t kTokSub = kChunk * kBK * 2;  // 8 KB per token sub-block
+constexpr uint32_t kTok = kTokSub * kKsub;      // 16 KB
+constexpr uint32_t kStage = kW + kTok;
+constexpr uint32_t kOffB = kStages * kW;
+constexpr uint32_t kOffBar = kStages * kStage;
+constexpr uint32_t kNumBars = 2 * kStages + 5;
+constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
+constexpr uint32_t kOffPrefix = kOffMisc + 16;
+constexpr uint32_t kOffOffs = kOffPrefix + (kMaxGroups + 1) * 4;
+constexpr uint32_t kOffX = (kOffOffs + (kMaxGroups + 1) * 4 + 15) / 16 * 16;
+constexpr uint32_t kSmemBytes = kOffX + kGU * 17 * 4 + 1024;
+constexpr uint32_t kTmemCols = 128;             // 2 slots x 64 columns
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+
+struct FParams {
+  const int32_t* offsets;
+  int n_groups;
+  int H;
+  int I;
+  int gu_tiles;          // I / 64 gate|up items per token chunk
+  int dn_tiles;          // H / 128 down items per token chunk
+  __nv_bfloat16* act;    // [out_rows, I]
+  __nv_bfloat16* y;      // [out_rows, H]
+  int32_t* done;         // [m-tiles] gate|up items finished per chunk; zero at launch
+  long long out_rows;
+  int32_t* status;
+  uint32_t debug_flags;
+};
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ int ld_acquire(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+struct Item {
+  bool gu;
+  int mt, m;
+};
+
+__device__ __forceinline__ Item item_of(int w, int n_gu, int gu_tiles, int dn_tiles) {
+  Item it;
+  it.gu = w < n_gu;
+  const int v = it.gu ? w : w - n_gu;
+  const int per = it.gu ? gu_tiles : dn_tiles;
+  it.mt = v / per;
+  it.m = v - it.mt * per;
+  return it;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_ffn_kernel(const __grid_constant__ CUtensorMap tmWgu,
+                      const __grid_constant__ CUtensorMap tmX16,
+                      const __grid_constant__ CUtensorMap tmX64,
+                      const __grid_constant__ CUtensorMap tmWdn,
+                      const __grid_constant__ CUtensorMap tmA16,
+                      const __grid_constant__ CUtensorMap tmA64, const FParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* tfull = bars + 2 * kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* mma_done = tempty + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  int* s_total = reinterpret_cast<int*>(smem + kOffMisc + 8);
+  int* s_prefix = reinterpret_cast<int*>(smem + kOffPrefix);
+  int* s_offs = reinterpret_cast<int*>(smem + kOffOffs);
+  float* s_xchg = reinterpret_cast<float*>(smem + kOffX);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_wait_and_trigger();
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&tfull[0], 1);
+    mbar_init(&tfull[1], 1);
+    mbar_init(&tempty[0], 4);
+    mbar_init(&tempty[1], 4);
+    mbar_init(mma_done, 1);
+    *s_abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmWgu);
+    tma_prefetch_desc(&tmX16);
+    tma_prefetch_desc(&tmX64);
+    tma_prefetch_desc(&tmWdn);
+    tma_prefetch_desc(&tmA16);
+    tma_prefetch_desc(&tmA64);
+  }
+  if (warp == 2)
+    build_tile_table<kChunk>(p.offsets, p.n_groups, 0, p.out_rows, s_prefix, s_offs, s_total,
+                             p.status, lane);
+  if (warp == 1) {
+    tmem_alloc(s_tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+  const int n_mt = *s_total;
+  const int n_gu = n_mt * p.gu_tiles;
+  const int total_work = n_gu + n_mt * p.dn_tiles;
+  const int KB_gu = p.H / (kBK * kKsub);
+  const int KB_dn = p.I / (kBK * kKsub);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, issued_par = 0;
+      bool skip = (p.debug_flags & MOE_DEBUG_SKIP_FIRST_LOAD) != 0u;
+      bool ok = true;
+      for (int w = blockIdx.x; ok && w < total_work; w += gridDim.x) {
+        const Item it = item_of(w, n_gu, p.gu_tiles, p.dn_tiles);
+        const Tile t = decode_tile<kChunk>(it.mt, 1, p.n_groups, s_prefix, s_offs);
+        const int nb = (t.rows + kTokBox - 1) / kTokBox;
+        const bool wide = nb > 2;
+        const uint32_t tok_rows = wide ? 64u : static_cast<uint32_t>(nb * kTokBox);
+        const uint32_t bytes = kW + kKsub * tok_rows * kBK * 2;
+        const int KB = it.gu ? KB_gu : KB_dn;
+        const CUtensorMap* mW = it.gu ? &tmWgu : &tmWdn;
+        const CUtensorMap* mT = it.gu ? (wide ? &tmX64 : &tmX16) : (wide ? &tmA64 : &tmA16);
+        const int wrow = it.gu ? t.g * 2 * p.I + it.m * kGU : t.g * p.H + it.m * kM;
+        auto weights = [&](uint8_t* sa, int kb) {
+#pragma unroll
+          for (int j = 0; j < kKsub; ++j) {
+            const int kc = (kb * kKsub + j) * kBK;
+            tma_load_2d(sa + j * kWSub, mW, &full[stage], kc, wrow);
+            if (it.gu)  // the same 64 neurons' up rows fill the lower half
+              tma_load_2d(sa + j * kWSub + kGU * kBK * 2, mW, &full[stage], kc, wrow + p.I);
+          }
+        };
+        auto tokens = [&](uint8_t* sb, uint64_t* bar, int kb) {
+#pragma unroll
+          for (int j = 0; j < kKsub; ++j) {
+            const int kc = (kb * kKsub + j) * kBK;
+            if (wide) {
+              tma_load_2d(sb + j * kTokSub, mT, bar, kc, t.row0);
+            } else {
+              for (int b = 0; b < nb; ++b)
+                tma_load_2d(sb + j * kTokSub + b * kTokBox * kBK * 2, mT, bar, kc,
+                            t.row0 + b * kTokBox);
+            }
+          }
+        };
+        int kb = 0;
+        if (!it.gu) {
+          // Down item: put the first weight stages in flight, then wait until
+          // every gate|up item of this token chunk has stored its act rows.
+          const int pre = KB < kStages ? KB : kStages;
+          int st0 = stage;
+          for (; kb < pre; ++kb) {
+            if (!mbar_wait(&empty[stage], phase ^ 1u, s_abort)) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(&full[stage], bytes);
+            weights(smem + stage * kW, kb);
+            issued |= 1u << stage;
+            issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          const uint64_t t0 = globaltimer();
+          while (ld_acquire(p.done + it.mt) < p.gu_tiles) {
+            if (*s_abort || globaltimer() - t0 > kWaitLimitNs) {
+              ok = false;
+              break;
+            }
+          }
+          fence_proxy_async_global();
+          // the token loads of the pre-issued stages (their full barriers
+          // already expect these bytes)
+          for (int i = 0; i < pre; ++i) {
+            const int s = (st0 + i) % kStages;
+            tokens(smem + kOffB + s * kTok, &full[s], i);
+          }
+          if (!ok) break;
+        }
+        for (; kb < KB; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, s_abort)) {
+            ok = false;
+            break;
+          }
+          if (skip) {
+            skip = false;  // test hook: the consumer of this slot must time out
+          } else {
+            mbar_expect_tx(&full[stage], bytes);
+            weights(smem + stage * kW, kb);
+            tokens(smem + kOffB + stage * kTok, &full[stage], kb);
+            issued |= 1u << stage;
+            issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+          }
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) fail(s_abort, p.status);
+      for (int s = 0; s < kStages; ++s)
+        if ((issued >> s) & 1u) mbar_wait(&full[s], (issued_par >> s) & 1u, nullptr);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, aphase = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; ok && w < total_work; w += gridDim.x) {
+        const Item it = item_of(w, n_gu, p.gu_tiles, p.dn_tiles);
+        const Tile t = decode_tile<kChunk>(it.mt, 1, p.n_groups, s_prefix, s_offs);
+        const int n = ((t.rows + 15) / 16) * 16;
+        const uint32_t idesc = idesc_bf16_f32(kM, n);
+        const int KB = it.gu ? KB_gu : KB_dn;
+        if (!mbar_wait(&tempty[acc], aphase ^ 1u, s_abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kChunk);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&full[stage], phase, s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int j = 0; j < kKsub; ++j) {
+            const uint64_t a = sdesc_sw128(smem_u32(smem + stage * kW + j * kWSub));
+            const uint64_t b = sdesc_sw128(smem_u32(smem + kOffB + stage * kTok + j * kTokSub));
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k)
+              umma_bf16(d, a + 2u * k, b + 2u * k, idesc, (kb | j | k) != 0 ? 1u : 0u);
+          }
+          umma_commit(&empty[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          aphase ^= 1u;
+        }
+      }
+      if (!ok) fail(s_abort, p.status);
+      umma_commit(mma_done);
+      mbar_wait(mma_done, 0u, nullptr);
+    }
+    __syncwarp();
+  } else {
+    const int q = warp & 3;
+    const int r_in = q * 32 + lane;
+    int acc = 0;
+    uint32_t aphase = 0;
+    for (int w = blockIdx.x; w < total_work; w += gridDim.x) {
+      const Item it = item_of(w, n_gu, p.gu_tiles, p.dn_tiles);
+      const Tile t = decode_tile<kChunk>(it.mt, 1, p.n_groups, s_prefix, s_offs);
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&tfull[acc], aphase, s_abort) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) fail(s_abort, p.status);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                          static_cast<uint32_t>(acc * kChunk);
+      if (it.gu) {
+        const bool is_gate = q < 2;
+        const int nl = (q & 1) * 32 + lane;
+        const int col = it.m * kGU + nl;
+        for (int c0 = 0; c0 < t.rows; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(tb + c0, v);
+          tmem_ld_wait();
+          if (!is_gate) {
+#pragma unroll
+            for (int cc = 0; cc < 16; ++cc) s_xchg[nl * 17 + cc] = __uint_as_float(v[cc]);
+          }
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+          if (is_gate) {
+#pragma unroll
+            for (int cc = 0; cc < 16; ++cc) {
+              const long long r = static_cast<long long>(t.row0) + c0 + cc;
+              if (c0 + cc < t.rows && r < p.out_rows)
+                p.act[r * p.I + col] = __float2bfloat16_rn(silu_f(__uint_as_float(v[cc])) *
+                                                           s_xchg[nl * 17 + cc]);
+            }
+          }
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+        }
+        // publish: this chunk's act columns [m*64, m*64+64) are stored
+        fence_proxy_async_global();
+        __threadfence();
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (warp == 2 && lane == 0) atomicAdd(p.done + it.mt, 1);
+      } else {
+        const int col = it.m * kM + r_in;
+        for (int c0 = 0; c0 < t.rows; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(tb + c0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int cc = 0; cc < 16; ++cc) {
+            const long long r = static_cast<long long>(t.row0) + c0 + cc;
+            if (c0 + cc < t.rows && r < p.out_rows)
+              p.y[r * p.H + col] = __float2bfloat16_rn(__uint_as_float(v[cc]));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        aphase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace
+
+bool decode_ffn_supports(int H, int I_sub) { return H % 128 == 0 && I_sub % 128 == 0; }
+
+cudaError_t launch_decode_ffn(const DecodeFfnArgs& a, cudaStream_t s) {
+  if (a.x_rows <= 0 || a.rows <= 0) return cudaSuccess;
+  CUtensorMap wgu, x16, x64, wdn, a16, a64;
+  const int E_r = a.n_groups;
+  if (!make_tmap_bf16(&wgu, a.w_gate_up, static_cast<long long>(E_r) * 2 * a.I, a.H, kGU) ||
+      !make_tmap_bf16(&x16, a.x_perm, a.x_rows, a.H, kTokBox) ||
+      !make_tmap_bf16(&x64, a.x_perm, a.x_rows, a.H, 64) ||
+      !make_tmap_bf16(&wdn, a.w_down, static_cast<long long>(E_r) * a.H, a.I, kM) ||
+      !make_tmap_bf16(&a16, a.act, a.rows, a.I, kTokBox) ||
+      !make_tmap_bf16(&a64, a.act, a.rows, a.I, 64))
+    return cudaErrorInvalidValue;
+  FParams p;
+  p.offsets = a.offsets;
+  p.n_groups = E_r;
+  p.H = a.H;
+  p.I = a.I;
+  p.gu_tiles = a.I / kGU;
+  p.dn_tiles = a.H / kM;
+  p.act = static_cast<__nv_bfloat16*>(a.act);
+  p.y = static_cast<__nv_bfloat16*>(a.y);
+  p.done = a.done;
+  p.out_rows = a.rows;
+  p.status = a.status;
+  p.debug_flags = a.debug_flags;
+  static bool attr_done[64] = {false};
+  cudaError_t e = set_smem_once(decode_ffn_kernel, static_cast<int>(kSmemBytes), attr_done);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(decode_ffn_kernel, dim3(a.sm_count), dim3(kThreads), kSmemBytes, s, wgu, x16,
+                    x64, wdn, a16, a64, p);
+}
+
+}  // namespace moe

@@ -23,9 +23,11 @@ cudaError_t launch_permute(const int32_t* topk_idx, const int32_t* k_per_token, 
                            int k_max, int E_r, uint32_t* bitmap, int32_t* wprefix,
                            int32_t* counts, int32_t* offsets, int32_t* sorted_token,
                            int32_t* inv_row, int32_t* status, cudaStream_t s);
+// also zeroes zero_ptr[0, zero_n) (counters for the kernel that follows)
 cudaError_t launch_gather_rows(const void* x, const int32_t* sorted_token,
                                const int32_t* offsets, int E_r, int T, int H, int n_cap,
-                               void* x_perm, int32_t* status, int sm_count, cudaStream_t s);
+                               void* x_perm, int32_t* status, int sm_count, cudaStream_t s,
+                               int32_t* zero_ptr = nullptr, int zero_n = 0);
 
 // ---- combine.cu
 cudaError_t launch_combine(const void* y_perm, const void* y_shared, const int32_t* inv_row,
@@ -86,6 +88,28 @@ struct DecodeGemmArgs {
 
 cudaError_t launch_decode_gemm(const DecodeGemmArgs& a, cudaStream_t s);
 bool decode_gemm_supports(int n_out, bool gate_up);
+
+// ---- ffn_decode.cu: gate|up + SwiGLU + down of a decode-sized batch in one kernel
+struct DecodeFfnArgs {
+  const void* x_perm;        // bf16 [x_rows, H], permuted token rows
+  long long x_rows;
+  const void* w_gate_up;     // bf16 [E_r, 2 I, H]
+  const void* w_down;        // bf16 [E_r, H, I]
+  const int32_t* offsets;    // [n_groups + 1]
+  int n_groups;
+  int H;
+  int I;
+  void* act;                 // bf16 [rows, I] (scratch)
+  void* y;                   // bf16 [rows, H]
+  int32_t* done;             // per 64-row chunk counters, zero before the launch
+  long long rows;
+  int32_t* status;
+  uint32_t debug_flags;
+  int sm_count;
+};
+
+cudaError_t launch_decode_ffn(const DecodeFfnArgs& a, cudaStream_t s);
+bool decode_ffn_supports(int H, int I_sub);
 
 // bf16 [rows, cols] row-major tensor map: box of 64 columns x box_rows rows,
 // 128-byte swizzle, zero fill out of bounds.

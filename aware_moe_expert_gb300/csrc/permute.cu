@@ -144,8 +144,12 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
                                                            const int32_t* __restrict__ offsets,
                                                            int E_r, int T, int nv, int n_cap,
                                                            uint4* __restrict__ x_perm,
-                                                           int32_t* status) {
+                                                           int32_t* status,
+                                                           int32_t* __restrict__ zero_ptr,
+                                                           int zero_n) {
   pdl_wait_and_trigger();
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < zero_n; i += gridDim.x * blockDim.x)
+    zero_ptr[i] = 0;
   const int n = min(offsets[E_r], n_cap);
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -285,14 +289,15 @@ cudaError_t launch_permute(const int32_t* topk_idx, const int32_t* k_per_token, 
 
 cudaError_t launch_gather_rows(const void* x, const int32_t* sorted_token,
                                const int32_t* offsets, int E_r, int T, int H, int n_cap,
-                               void* x_perm, int32_t* status, int sm_count, cudaStream_t s) {
+                               void* x_perm, int32_t* status, int sm_count, cudaStream_t s,
+                               int32_t* zero_ptr, int zero_n) {
   if (n_cap <= 0) return cudaSuccess;
   const int warps_needed = n_cap;
   int blocks = (warps_needed + 7) / 8;
   blocks = blocks < sm_count * 8 ? blocks : sm_count * 8;
   return launch_pdl(gather_rows_kernel, dim3(blocks), dim3(256), 0, s,
                     static_cast<const uint4*>(x), sorted_token, offsets, E_r, T, H / 8, n_cap,
-                    static_cast<uint4*>(x_perm), status);
+                    static_cast<uint4*>(x_perm), status, zero_ptr, zero_n);
 }
 
 }  // namespace moe

@@ -192,13 +192,18 @@ def run_ours(args, wl, rank, world, local):
     def call_down(sp):
         B.check(B.moe_down(desc, act, offsets, d["w_down"], y, st, ws, sp), "moe_down")
 
+    def call_grouped_ffn(sp):
+        B.check(B.moe_grouped_ffn(desc, d["x"], st_tok, offsets, d["w_gate_up"], d["w_down"], y,
+                                  st, ws, sp), "moe_grouped_ffn")
+
     def call_combine(sp):
         B.check(B.moe_combine(desc, y, ysh, inv, w, d["k_per_token"], out, st, sp), "moe_combine")
 
     calls = [("route", call_route), ("permute", call_permute)]
     if ysh is not None:
         calls.append(("shared_ffn", call_shared))
-    calls += [("gate_up", call_gate_up), ("down", call_down), ("combine", call_combine)]
+    calls += [("gate_up", call_gate_up), ("down", call_down), ("grouped_ffn", call_grouped_ffn),
+              ("combine", call_combine)]
 
     def step(sp):
         for _, f in calls:
@@ -362,15 +367,19 @@ def run_ours(args, wl, rank, world, local):
     t_roof_us = max(F / (peaks["bf16_tflops"] * 1e12), Bytes / (peaks["hbm_gbs"] * 1e9)) * 1e6
     bound = "tensor" if F / (peaks["bf16_tflops"] * 1e12) > Bytes / (peaks["hbm_gbs"] * 1e9) else "hbm"
 
-    # dominant kernel: the grouped gate|up call (2/3 of the routed work)
+    # dominant kernel.  Decode: moe_grouped_ffn, whose work is one fused
+    # kernel (gate|up + SwiGLU + down) after the row gather; prefill: the
+    # grouped gate|up GEMM (2/3 of the routed FLOPs).
     gu_us = parts["gate_up"]
     if wl.phase == "decode":
-        alg = 2.0 * (D * 2 * I_sub * H + n_assign * H + n_assign * I_sub)  # weights + x rows + act
-        achieved = alg / (gu_us * 1e-6) / 1e9
+        ffn_us = parts["grouped_ffn"]
+        alg = 2.0 * (3 * D * H * I_sub + 2 * n_assign * H)   # unit weights + x rows + y rows
+        achieved = alg / (ffn_us * 1e-6) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "traffic": traffic_for(wl.name, "gate_up", 1.0),
-                "kernel": "moe_gate_up (row gather + grouped gate|up GEMM, SwiGLU epilogue)",
+                "traffic": traffic_for(wl.name, "grouped_ffn", 1.0),
+                "kernel": "moe_grouped_ffn (row gather + fused decode FFN kernel: "
+                          "gate|up + SwiGLU + down)",
                 "algorithmic_bytes": alg, "peak_source": peaks["source"] + " hbm_gbs"}
     else:
         alg = 4.0 * H * I_sub * n_assign
@@ -431,12 +440,15 @@ def launches_per_step(wl, T, path=0):
     n = 2                                            # logits, top-k
     n += 1 if (T + 31) // 32 <= 8 else 3            # permutation (one CTA, or bitmap/scan/scatter)
     n += 2 if wl.I_shared else 0                     # shared expert gate|up, down
-    n += 2                                           # row gather + gate|up GEMM
-    if decode and wl.I_sub % 64 == 0:
-        n += 1 if budget // max(n_cap * 2 * wl.I_sub * 4, 1) >= 2 else 0
-    n += 1                                           # down GEMM
-    if decode and wl.H % 128 == 0:
-        n += 1 if budget // max(n_cap * wl.H * 4, 1) >= 2 else 0
+    if decode and wl.H % 128 == 0 and wl.I_sub % 128 == 0:
+        n += 2                                       # row gather + fused decode FFN kernel
+    else:
+        n += 2                                       # row gather + gate|up GEMM
+        if decode and wl.I_sub % 64 == 0:
+            n += 1 if budget // max(n_cap * 2 * wl.I_sub * 4, 1) >= 2 else 0
+        n += 1                                       # down GEMM
+        if decode and wl.H % 128 == 0:
+            n += 1 if budget // max(n_cap * wl.H * 4, 1) >= 2 else 0
     n += 1                                           # combine
     return n
 

@@ -39,7 +39,21 @@ __global__ void __launch_bounds__(256) router_logits_small_kernel(
   const int nt = min(tok_per_cta, T - t0);
   const int nv = H / 8;
   const uint4* xg = reinterpret_cast<const uint4*>(x) + static_cast<size_t>(t0) * nv;
-  for (int i = threadIdx.x; i < nt * nv; i += blockDim.x) xs[i] = __ldg(xg + i);
+  // eight 16-byte loads per thread in flight before they are stored
+  const int total = nt * nv;
+  for (int i0 = threadIdx.x; i0 < total; i0 += 8 * blockDim.x) {
+    uint4 tmp[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int i = i0 + q * blockDim.x;
+      tmp[q] = i < total ? __ldg(xg + i) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int i = i0 + q * blockDim.x;
+      if (i < total) xs[i] = tmp[q];
+    }
+  }
   __syncthreads();
   if (u >= E_r) return;
   float acc[kTokPerCta];

@@ -25,6 +25,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARGUMENT", 2: "MOE_ERR_UNSUPPOR
 SCORE = {"softmax": 0, "sigmoid": 1}
 PATH_AUTO, PATH_PREFILL, PATH_DECODE = 0, 1, 2
 DEBUG_SKIP_FIRST_LOAD = 1
+DEBUG_FORCE_PAIR = 2
 
 EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_gate_up", "moe_down",
            "moe_grouped_ffn", "moe_shared_ffn", "moe_combine", "moe_layer_forward",

@@ -265,6 +265,7 @@ moe_status do_gate_up(const moe_layer_desc* d, const void* x, const int32_t* sor
   g.out_rows = n_cap;
   g.status = status;
   g.debug_flags = d->debug_flags;
+  g.force_pair = (d->debug_flags & MOE_DEBUG_FORCE_PAIR) != 0u;
   g.sm_count = sm_count();
   g.max_rows_hint = static_cast<int>(n_cap);
   return cuda_status(moe::launch_gemm(g, s));
@@ -315,6 +316,7 @@ moe_status do_down(const moe_layer_desc* d, const void* act, const int32_t* offs
   g.out_rows = n_cap;
   g.status = status;
   g.debug_flags = 0;
+  g.force_pair = (d->debug_flags & MOE_DEBUG_FORCE_PAIR) != 0u;
   g.sm_count = sm_count();
   g.max_rows_hint = static_cast<int>(n_cap);
   return cuda_status(moe::launch_gemm(g, s));

@@ -20,8 +20,10 @@
 //               accumulators, and commits to `empty` (ring slot free) and
 //               `tfull` (accumulator ready) mbarriers
 //   warps 2..5  epilogue: tcgen05.ld of their 32-lane TMEM quadrant (one
-//               output row per thread), math, 16-byte global stores; then
-//               release the accumulator on `tempty`
+//               output row per thread), math; a warp whose 32 rows all belong
+//               to the tile's unit stages each 32 x 64 bf16 block in shared
+//               memory and writes it with one TMA store, a partial slab uses
+//               masked 16-byte stores; then release the accumulator on `tempty`
 // Work items are (m-tile, n-tile) pairs, m-tile major, handed out
 // round-robin; the m-tile -> (unit, first row) map is rebuilt in shared
 // memory from `offsets` at kernel start, so no host sync is needed.
@@ -75,7 +77,8 @@ struct Cfg {
                                                               : 512;
   static constexpr uint32_t kOffA = 0;
   static constexpr uint32_t kOffB = STAGES * kABytes;
-  static constexpr uint32_t kOffBar = STAGES * kStageBytes;
+  static constexpr uint32_t kOffStage = STAGES * kStageBytes;  // 4 epilogue buffers
+  static constexpr uint32_t kOffBar = kOffStage + 4 * kStageRowsBytes;
   static constexpr uint32_t kNumBars = 2 * STAGES + 5;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
   static constexpr uint32_t kOffPrefix = kOffMisc + 16;
@@ -89,7 +92,8 @@ struct Cfg {
 template <int BN_MMA, int EPI, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB, const KParams p) {
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmOut, const KParams p) {
   using C = Cfg<BN_MMA, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -125,6 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (EPI != EPI_F32) tma_prefetch_desc(&tmOut);
   }
   if (warp == 2) build_tile_table(p.offsets, p.n_groups, p.dense_rows, p.out_rows, s_prefix, s_offs,
                                   s_total, p.status, lane);
@@ -230,6 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     const int r_in = q * 32 + lane;
+    uint8_t* sbuf = smem + C::kOffStage + q * kStageRowsBytes;
     int acc = 0;
     uint32_t aphase = 0;
     for (int w = blockIdx.x; w < total_work; w += gridDim.x) {
@@ -246,44 +252,51 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN_MMA);
       const long long grow = static_cast<long long>(t.row0) + r_in;
       const bool valid = r_in < t.rows && grow < p.out_rows;
-      if (EPI == EPI_SWIGLU) {
-        constexpr int BNH = BN_MMA / 2;
-        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + grow * p.ld_out +
-                              static_cast<long long>(t.nt) * p.bn_out;
+      if (EPI != EPI_F32) {
+        // every row of this warp's slab belongs to the tile's unit
+        const bool full_slab = q * 32 + 32 <= t.rows &&
+                               static_cast<long long>(t.row0) + q * 32 + 32 <= p.out_rows;
+        const int col0 = t.nt * p.bn_out;
+        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + grow * p.ld_out + col0;
+        constexpr int kCols = EPI == EPI_SWIGLU ? BN_MMA / 2 : BN_MMA;  // outputs per row
 #pragma unroll 1
-        for (int c = 0; c < BNH; c += 32) {
-          uint32_t gv[32], uv[32];
-          tmem_ld32(tbase + c, gv);
-          tmem_ld32(tbase + BNH + c, uv);
-          tmem_ld_wait();
+        for (int c = 0; c < kCols; c += 32) {
           uint32_t pk[16];
+          if (EPI == EPI_SWIGLU) {
+            uint32_t gv[32], uv[32];
+            tmem_ld32(tbase + c, gv);
+            tmem_ld32(tbase + BN_MMA / 2 + c, uv);
+            tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float a0 = silu_f(__uint_as_float(gv[2 * i])) * __uint_as_float(uv[2 * i]);
-            const float a1 =
-                silu_f(__uint_as_float(gv[2 * i + 1])) * __uint_as_float(uv[2 * i + 1]);
-            pk[i] = pack_bf16x2(a0, a1);
+            for (int i = 0; i < 16; ++i) {
+              const float a0 = silu_f(__uint_as_float(gv[2 * i])) * __uint_as_float(uv[2 * i]);
+              const float a1 =
+                  silu_f(__uint_as_float(gv[2 * i + 1])) * __uint_as_float(uv[2 * i + 1]);
+              pk[i] = pack_bf16x2(a0, a1);
+            }
+          } else {
+            uint32_t v[32];
+            tmem_ld32(tbase + c, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
           }
-          if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-          }
-        }
-      } else if (EPI == EPI_BF16) {
-        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + grow * p.ld_out +
-                              static_cast<long long>(t.nt) * p.bn_out;
-#pragma unroll 1
-        for (int c = 0; c < BN_MMA; c += 32) {
-          uint32_t v[32];
-          tmem_ld32(tbase + c, v);
-          tmem_ld_wait();
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-          if (valid) {
+          if (full_slab) {
+            if ((c & 32) == 0) {  // first half of a 64-column block: buffer free?
+              if (lane == 0) bulk_wait_read_all();
+              __syncwarp();
+            }
+            stage_row_32(sbuf, lane, (c & 32) >> 3, pk);
+            if ((c & 32) != 0) {
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&tmOut, sbuf, col0 + c - 32, t.row0 + q * 32);
+                bulk_commit();
+              }
+            }
+          } else if (valid) {
             uint4* dst = reinterpret_cast<uint4*>(orow + c);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -328,6 +341,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         aphase ^= 1u;
       }
     }
+    if (EPI != EPI_F32) {
+      if (lane == 0) bulk_wait_all();  // stores done before the CTA (and its smem) goes
+      __syncwarp();
+    }
   }
 
   tc_fence_before();
@@ -344,9 +361,13 @@ template <int BN_MMA, int EPI, int STAGES>
 cudaError_t run_gemm(const GemmArgs& g, cudaStream_t s) {
   using C = Cfg<BN_MMA, STAGES>;
   const int box_b = EPI == EPI_SWIGLU ? BN_MMA / 2 : BN_MMA;  // output columns per n-tile
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, to;
   if (!make_tmap_bf16(&ta, g.a, g.a_rows, g.K, BM)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tb, g.b, g.b_rows, g.K, box_b)) return cudaErrorInvalidValue;
+  if (EPI == EPI_F32)
+    to = tb;  // unused
+  else if (!make_tmap_bf16(&to, g.out, g.out_rows, static_cast<int>(g.ld_out), 32))
+    return cudaErrorInvalidValue;
   KParams kp;
   kp.offsets = g.offsets;
   kp.n_groups = g.offsets == nullptr ? 1 : g.n_groups;
@@ -378,7 +399,7 @@ cudaError_t run_gemm(const GemmArgs& g, cudaStream_t s) {
   static bool attr_done[64] = {false};
   cudaError_t e = set_smem_once(kern, static_cast<int>(C::kSmemBytes), attr_done);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(grid), dim3(kThreads), C::kSmemBytes, s, ta, tb, kp);
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), C::kSmemBytes, s, ta, tb, to, kp);
 }
 
 }  // namespace
@@ -415,6 +436,19 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, long long rows, int cols, 
 bool gemm_supports_f32_router(int E_r) { return E_r == 64 || E_r == 128 || E_r == 256; }
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s) {
+  // CTA pairs stage a third fewer bytes per SM and k-block (12-17% less time
+  // per executed row on GB300) but tile 256 rows of one unit at a time; a
+  // routed batch leaves many units with a partial tile, which costs twice as
+  // much padding as with 128-row tiles, and the host cannot see the row
+  // counts.  Dense GEMMs use pairs when the padding allows it.
+  if (gemm_pair_supports(g.epi, g.n_out)) {
+    bool pair = g.force_pair && g.offsets != nullptr;
+    if (g.offsets == nullptr) {
+      const long long p = (g.dense_rows + 255) / 256, t = (g.dense_rows + 127) / 128;
+      pair = 86 * p <= 50 * t;  // 256 p rows at ~0.86 the cost of 128 t rows
+    }
+    if (pair) return launch_gemm_pair(g, s);
+  }
   switch (g.epi) {
     case EPI_SWIGLU:
       if (g.n_out % 128 == 0) return run_gemm<256, EPI_SWIGLU, 4>(g, s);

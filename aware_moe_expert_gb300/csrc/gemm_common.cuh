@@ -37,6 +37,22 @@ __device__ __forceinline__ Tile decode_tile(int w, int n_tiles, int n_groups, co
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
+// Epilogue staging of one warp's 32 output rows x 64 bf16 columns (4 KB,
+// 1024-byte aligned) in the layout a TMA store with the 128-byte swizzle
+// reads: 16-byte chunk c of row r sits at chunk c ^ (r % 8) of the row, so
+// the eight lanes writing one chunk index hit eight different bank groups.
+constexpr uint32_t kStageRowsBytes = 32 * 128;
+
+// Lane `lane` writes chunks c0 .. c0 + 3 (32 columns) of its row.
+__device__ __forceinline__ void stage_row_32(uint8_t* buf, int lane, int c0,
+                                             const uint32_t (&pk)[16]) {
+  uint8_t* row = buf + lane * 128;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    *reinterpret_cast<uint4*>(row + (((c0 + i) ^ (lane & 7)) << 4)) =
+        make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+}
+
 __device__ __forceinline__ void fail(volatile int* abort, int32_t* status) {
   *abort = 1;
   report(status, MOE_ERR_DEVICE_TIMEOUT);

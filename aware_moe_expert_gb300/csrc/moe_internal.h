@@ -59,9 +59,14 @@ struct GemmArgs {
   int sm_count;
   int max_rows_hint;         // upper bound of total rows (grid sizing)
   int bn_hint;               // EPI_F32: output columns per tile (64/128/256), 0 = all
+  bool force_pair;           // grouped SWIGLU/BF16: use the CTA-pair kernel
 };
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s);
+
+// ---- gemm_pair.cu: the same grouped GEMM on CTA pairs (tcgen05 cta_group::2)
+bool gemm_pair_supports(int epi, int n_out);
+cudaError_t launch_gemm_pair(const GemmArgs& g, cudaStream_t s);
 
 // ---- gemm_decode.cu
 struct DecodeGemmArgs {

@@ -62,6 +62,9 @@ typedef enum { MOE_PATH_AUTO = 0, MOE_PATH_PREFILL = 1, MOE_PATH_DECODE = 2 } mo
 #define MOE_DEBUG_SKIP_FIRST_LOAD 1u /* the FFN producer skips its first load, so the
                                         consumer's bounded wait must give up and report
                                         MOE_ERR_DEVICE_TIMEOUT (about 2 s)            */
+#define MOE_DEBUG_FORCE_PAIR 2u      /* grouped prefill-path GEMMs run on the CTA-pair
+                                        kernel (tcgen05 cta_group::2), which the library
+                                        otherwise keeps for dense GEMMs; same results */
 
 typedef struct {
   int32_t T;          /* tokens                                                  */

@@ -30,7 +30,7 @@ def _weights(E_r, H, I_sub, n_sub, seed):
     return x, wgu, wd
 
 
-@pytest.mark.parametrize("path", [B.PATH_PREFILL, B.PATH_DECODE])
+@pytest.mark.parametrize("path", [B.PATH_PREFILL, B.PATH_DECODE, "pair"])
 @pytest.mark.parametrize("T,H,n_experts,n_sub,I_sub,k_max,skew", [
     (64, 256, 16, 4, 128, 8, 0.0),      # tiny layer shape
     (300, 512, 8, 1, 192, 4, 3.0),      # 3 m-tiles on hot units, I_sub % 128 != 0
@@ -41,8 +41,12 @@ def _weights(E_r, H, I_sub, n_sub, seed):
     (400, 512, 4, 2, 256, 4, 4.0),      # > 128 rows on a unit: decode chunks of 128 tokens
 ])
 def test_grouped_ffn_rows_match_oracle(T, H, n_experts, n_sub, I_sub, k_max, skew, path):
-    """Both kernel families (prefill tiles, decode swap-AB) on the same inputs;
-    shapes a family does not support fall back to the other one."""
+    """Every kernel family (prefill tiles on one CTA or on CTA pairs, decode
+    swap-AB) on the same inputs; shapes a family does not support fall back
+    to another one."""
+    debug = 0
+    if path == "pair":
+        path, debug = B.PATH_PREFILL, B.DEBUG_FORCE_PAIR
     E_r = n_experts * n_sub
     x, wgu, wd = _weights(E_r, H, I_sub, n_sub, seed=T * 31 + H)
     x = x[:T].contiguous()
@@ -52,7 +56,7 @@ def test_grouped_ffn_rows_match_oracle(T, H, n_experts, n_sub, I_sub, k_max, ske
     g = torch.Generator().manual_seed(T)
     k = torch.randint(1, k_max + 1, (T,), generator=g, dtype=torch.int32).to(DEV)
     desc = B.LayerDesc(T=T, H=H, n_experts=n_experts, n_sub=n_sub, I_sub=I_sub, k_max=k_max,
-                       path=path)
+                       path=path, debug_flags=debug)
     ws = torch.empty(B.moe_workspace_size(desc), dtype=torch.uint8, device=DEV)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
     idx = torch.empty(T, k_max, dtype=torch.int32, device=DEV)
@@ -74,7 +78,10 @@ def test_grouped_ffn_rows_match_oracle(T, H, n_experts, n_sub, I_sub, k_max, ske
     assert_close_layer(got, ref["y_perm"], "y_perm")
 
 
-@pytest.mark.parametrize("T,H,I_sh", [(100, 256, 128), (300, 512, 192)])
+@pytest.mark.parametrize("T,H,I_sh", [
+    (100, 256, 128), (300, 512, 192),   # one-CTA tiles
+    (700, 512, 256), (1024, 256, 128),  # CTA pairs (ragged last pair tile; exact)
+])
 def test_shared_expert_matches_oracle(T, H, I_sh):
     g = torch.Generator(device=DEV).manual_seed(T)
     x = torch.randn(T, H, generator=g, device=DEV).to(torch.bfloat16)

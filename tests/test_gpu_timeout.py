@@ -50,13 +50,16 @@ def _ffn(desc, x, wgu, wd, L, k):
     return B.moe_get_device_status(st), y
 
 
-@pytest.mark.parametrize("path", [B.PATH_PREFILL, B.PATH_DECODE])
+@pytest.mark.parametrize("path", [B.PATH_PREFILL, B.PATH_DECODE, "pair"])
 def test_skipped_load_times_out_and_context_survives(path):
-    desc, x, wgu, wd, L, k = _setup(path, B.DEBUG_SKIP_FIRST_LOAD)
+    extra = 0
+    if path == "pair":                     # the CTA-pair GEMM's leader skips the load
+        path, extra = B.PATH_PREFILL, B.DEBUG_FORCE_PAIR
+    desc, x, wgu, wd, L, k = _setup(path, B.DEBUG_SKIP_FIRST_LOAD | extra)
     code, _ = _ffn(desc, x, wgu, wd, L, k)
     assert code == 5, B.STATUS_NAMES.get(code, code)     # MOE_ERR_DEVICE_TIMEOUT
-    # the same context keeps working
-    desc.debug_flags = 0
+    # the same context keeps working (same kernel family)
+    desc.debug_flags = extra
     code, y = _ffn(desc, x, wgu, wd, L, k)
     assert code == 0
     ref = O.layer_forward(spec_of(desc), bf16_bits(x), None, unit_fetch(wgu), unit_fetch(wd),

@@ -51,6 +51,8 @@ def parse():
     p.add_argument("--cpu-budget-s", type=float, default=30.0)
     p.add_argument("--path", type=int, default=0,
                    help="GEMM family: 0 auto, 1 token tiles, 2 weight-stationary (swap-AB)")
+    p.add_argument("--force-pair", action="store_true",
+                   help="run grouped prefill GEMMs on the CTA-pair kernel (debug flag)")
     return p.parse_args()
 
 
@@ -158,6 +160,8 @@ def run_ours(args, wl, rank, world, local):
     desc = B.desc_for(wl, expert_bias=d["expert_bias"], w_shared_gate_up=d.get("w_shared_gate_up"),
                       w_shared_down=d.get("w_shared_down"))
     desc.path = args.path
+    if args.force_pair:
+        desc.debug_flags |= B.DEBUG_FORCE_PAIR
     T, H, E_r, k_max, I_sub = wl.T, wl.H, wl.E_r, wl.k_max, wl.I_sub
     ws = torch.empty(B.moe_workspace_size(desc), dtype=torch.uint8, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)

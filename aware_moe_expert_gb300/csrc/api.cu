@@ -22,8 +22,9 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 // Byte offsets of every workspace region for one desc.
 struct Layout {
-  size_t logits, topk_idx, topk_w, counts, offsets, sorted_token, inv_row, bitmap, wprefix, xperm,
-      act, yperm, act_sh, ysh, split_word, partial, chunk_done, total;
+  size_t logits, router_partial, topk_idx, topk_w, counts, offsets, sorted_token, inv_row, bitmap,
+      wprefix, xperm, act, yperm, act_sh, ysh, split_word, partial, chunk_done, total;
+  int router_slices;   // slices of the CUDA-core router (0: the tensor-core router runs)
   int max_split;       // K splits the decode gate|up kernel may use (1: none)
   int max_split_down;  // K splits the decode down kernel may use
 };
@@ -31,6 +32,12 @@ struct Layout {
 // Budget of the decode kernel's fp32 split-K partial buffer.
 constexpr size_t kPartialBudget = size_t(256) << 20;
 constexpr int kMaxSplit = 8;
+
+// The tensor-core GEMM computes the router logits for T >= 128 tokens when
+// E_r is one of its tile widths; otherwise CUDA cores do, in slices of H.
+bool router_on_tensor_cores(const moe_layer_desc& d) {
+  return d.T >= 128 && moe::gemm_supports_f32_router(d.n_experts * d.n_sub);
+}
 
 Layout layout_of(const moe_layer_desc& d) {
   const size_t T = static_cast<size_t>(d.T), E_r = static_cast<size_t>(d.n_experts) * d.n_sub;
@@ -43,6 +50,12 @@ Layout layout_of(const moe_layer_desc& d) {
     return at;
   };
   l.logits = take(T * E_r * 4);
+  l.router_slices = 0;
+  if (!router_on_tensor_cores(d)) {
+    int vs = 0;
+    l.router_slices = moe::router_slices(d.T, d.H, static_cast<int>(E_r), &vs);
+  }
+  l.router_partial = take(static_cast<size_t>(l.router_slices) * T * E_r * 4);
   l.topk_idx = take(n_cap * 4);
   l.topk_w = take(n_cap * 4);
   l.counts = take(E_r * 4);
@@ -157,38 +170,35 @@ int decode_chunk(const moe_layer_desc* d) {
 
 // Router logits into dst: tcgen05 GEMM for T >= 128 with E_r in {64,128,256},
 // else the CUDA-core kernel.
-moe_status do_logits(const moe_layer_desc* d, const void* x, const void* router_w, float* dst,
-                     int32_t* status, cudaStream_t s) {
+// Finished logits (with bias) into dst on the tensor cores.
+moe_status do_logits_gemm(const moe_layer_desc* d, const void* x, const void* router_w,
+                          float* dst, int32_t* status, cudaStream_t s) {
   const int E_r = E_r_of(d);
-  if (d->T >= 128 && moe::gemm_supports_f32_router(E_r)) {
-    GemmArgs g{};
-    g.epi = moe::EPI_F32;
-    g.a = x;
-    g.a_rows = d->T;
-    g.b = router_w;
-    g.b_rows = E_r;
-    g.K = d->H;
-    g.offsets = nullptr;
-    g.n_groups = 1;
-    g.dense_rows = d->T;
-    g.n_out = E_r;
-    g.b_group_rows = 0;
-    g.out = dst;
-    g.ld_out = E_r;
-    g.out_rows = d->T;
-    g.bias = d->expert_bias;
-    g.bias_div = d->n_sub;
-    g.status = status;
-    g.debug_flags = 0;
-    g.sm_count = sm_count();
-    g.max_rows_hint = d->T;
-    // small batches: 64-column tiles for more CTAs; large ones: one n-tile,
-    // so x is read once
-    g.bn_hint = d->T < 4096 ? 64 : 0;
-    return cuda_status(moe::launch_gemm(g, s));
-  }
-  return cuda_status(moe::launch_router_logits_small(x, router_w, d->expert_bias, d->T, d->H,
-                                                     E_r, d->n_sub, dst, s));
+  GemmArgs g{};
+  g.epi = moe::EPI_F32;
+  g.a = x;
+  g.a_rows = d->T;
+  g.b = router_w;
+  g.b_rows = E_r;
+  g.K = d->H;
+  g.offsets = nullptr;
+  g.n_groups = 1;
+  g.dense_rows = d->T;
+  g.n_out = E_r;
+  g.b_group_rows = 0;
+  g.out = dst;
+  g.ld_out = E_r;
+  g.out_rows = d->T;
+  g.bias = d->expert_bias;
+  g.bias_div = d->n_sub;
+  g.status = status;
+  g.debug_flags = 0;
+  g.sm_count = sm_count();
+  g.max_rows_hint = d->T;
+  // small batches: 64-column tiles for more CTAs; large ones: one n-tile,
+  // so x is read once
+  g.bn_hint = d->T < 4096 ? 64 : 0;
+  return cuda_status(moe::launch_gemm(g, s));
 }
 
 moe_status do_route(const moe_layer_desc* d, const void* x, const void* router_w,
@@ -196,14 +206,29 @@ moe_status do_route(const moe_layer_desc* d, const void* x, const void* router_w
                     int32_t* topk_idx, float* topk_w, int32_t* status, void* ws,
                     cudaStream_t s) {
   const int E_r = E_r_of(d);
-  const float* L = logits_in;
-  if (L == nullptr) {
-    float* dst = logits_out != nullptr ? logits_out : at<float>(ws, layout_of(*d).logits);
-    MOE_TRY(do_logits(d, x, router_w, dst, status, s));
-    L = dst;
+  const Layout l = layout_of(*d);
+  const float* P = logits_in;   // what the top-k kernel sums
+  int S = 1;
+  const float* bias = nullptr;
+  float* lout = nullptr;
+  if (P == nullptr) {
+    if (router_on_tensor_cores(*d)) {
+      float* dst = logits_out != nullptr ? logits_out : at<float>(ws, l.logits);
+      MOE_TRY(do_logits_gemm(d, x, router_w, dst, status, s));
+      P = dst;
+    } else {
+      float* part = at<float>(ws, l.router_partial);
+      MOE_TRY(cuda_status(
+          moe::launch_router_logits_small(x, router_w, d->T, d->H, E_r, part, s)));
+      P = part;
+      S = l.router_slices;
+      bias = d->expert_bias;
+      lout = logits_out;
+    }
   }
-  return cuda_status(moe::launch_topk_gate(L, kpt, d->T, E_r, d->k_max, d->score, d->renorm,
-                                           d->route_scale, topk_idx, topk_w, status, s));
+  return cuda_status(moe::launch_topk_gate(P, S, bias, d->n_sub, lout, kpt, d->T, E_r, d->k_max,
+                                           d->score, d->renorm, d->route_scale, topk_idx, topk_w,
+                                           status, s));
 }
 
 moe_status do_permute(const moe_layer_desc* d, const int32_t* topk_idx, const int32_t* kpt,

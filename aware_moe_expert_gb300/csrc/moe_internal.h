@@ -10,10 +10,17 @@
 namespace moe {
 
 // ---- route.cu
-cudaError_t launch_router_logits_small(const void* x, const void* router_w,
-                                       const float* expert_bias, int T, int H, int E_r,
-                                       int n_sub, float* logits, cudaStream_t s);
-cudaError_t launch_topk_gate(const float* logits, const int32_t* k_per_token, int T, int E_r,
+// Partial logits P[s, t, u] over router_slices(T, H, E_r) slices of the
+// hidden dimension (no bias); P: fp32 [S, T, E_r], S <= router_slices_max(H).
+int router_slices(int T, int H, int E_r, int* vec_per_slice);
+int router_slices_max(int H);
+cudaError_t launch_router_logits_small(const void* x, const void* router_w, int T, int H,
+                                       int E_r, float* partial, cudaStream_t s);
+// Top-k_t and gates from the sum of S partial logit arrays [S, T, E_r] (S = 1:
+// finished logits) plus bias[u / n_sub] (nullable); logits_out (nullable)
+// receives the summed logits.
+cudaError_t launch_topk_gate(const float* partial, int S, const float* bias, int n_sub,
+                             float* logits_out, const int32_t* k_per_token, int T, int E_r,
                              int k_max, int score, int renorm, float route_scale,
                              int32_t* topk_idx, float* topk_w, int32_t* status,
                              cudaStream_t s);

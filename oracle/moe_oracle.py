@@ -276,20 +276,26 @@ def route(spec: LayerSpec, x=None, router_w=None, expert_bias=None,
 
 def layer_forward(spec: LayerSpec, x, router_w, w_gate_up, w_down, k_per_token,
                   expert_bias=None, logits=None, w_shared_gate_up=None,
-                  w_shared_down=None) -> dict:
+                  w_shared_down=None, routed=None) -> dict:
     """The whole layer forward, in the order of the method's steps.
 
     Output of token t ([Prism] §III-B2, the routed output sum_j w_j FFN_j(x)):
         out_t = sum_{j < k_t} w_{t,j} * FFN_{u_{t,j}}(x_t)  +  FFN_shared(x_t)
     Weights may be arrays indexed by unit or callables u -> array (bf16 bit
     patterns as uint16, or floats).  ``logits`` (float32 [T, E_r]) replaces
-    step 1 when given.
+    step 1 when given; ``routed`` = (topk_idx, topk_w) replaces steps 1-3 (a
+    routing made by another router, e.g. the proxy router).
     """
     flops = FlopCounter()
     X = bf16_to_f64(x)
     T, H = X.shape
     assert T == spec.T and H == spec.H
-    L, idx, w, flags = route(spec, X, router_w, expert_bias, k_per_token, logits, flops)
+    if routed is None:
+        L, idx, w, flags = route(spec, X, router_w, expert_bias, k_per_token, logits, flops)
+    else:
+        L, flags = None, 0
+        idx = np.asarray(routed[0], dtype=np.int32)
+        w = np.asarray(routed[1], dtype=np.float64)
     counts, offsets, sorted_token, inv_row = permute(idx, k_per_token, spec.E_r)
     n_assign = int(offsets[-1])
     y_perm = np.zeros((n_assign, H), dtype=np.float64)

@@ -29,7 +29,9 @@ DEBUG_FORCE_PAIR = 2
 
 EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_gate_up", "moe_down",
            "moe_grouped_ffn", "moe_shared_ffn", "moe_combine", "moe_layer_forward",
-           "moe_get_device_status", "moe_status_string", "moe_permute_static")
+           "moe_get_device_status", "moe_status_string", "moe_permute_static",
+           "moe_cg_workspace_size", "moe_pack_proxy_rows", "moe_route_cg",
+           "moe_layer_forward_cg")
 
 
 class MoeLayerDesc(ctypes.Structure):
@@ -40,6 +42,12 @@ class MoeLayerDesc(ctypes.Structure):
                 ("I_shared", ctypes.c_int32), ("w_shared_gate_up", ctypes.c_void_p),
                 ("w_shared_down", ctypes.c_void_p), ("path", ctypes.c_int),
                 ("debug_flags", ctypes.c_uint32)]
+
+
+class MoeCgRouter(ctypes.Structure):
+    _fields_ = [("m", ctypes.c_int32), ("r", ctypes.c_int32),
+                ("router_w_expert", ctypes.c_void_p), ("proxy_w", ctypes.c_void_p),
+                ("kappa", ctypes.c_void_p)]
 
 
 class MoeError(RuntimeError):
@@ -74,6 +82,12 @@ def lib() -> ctypes.CDLL:
             "moe_combine": (ctypes.c_int, [D, vp, vp, i32p, vp, i32p, vp, i32p, vp]),
             "moe_layer_forward": (ctypes.c_int, [D, vp, vp, vp, vp, i32p, vp, i32p, vp, vp]),
             "moe_get_device_status": (ctypes.c_int, [i32p, vp]),
+            "moe_cg_workspace_size": (ctypes.c_size_t, [D, ctypes.POINTER(MoeCgRouter)]),
+            "moe_pack_proxy_rows": (ctypes.c_int, [D, ctypes.c_int32, vp, i32p, vp, i32p, vp]),
+            "moe_route_cg": (ctypes.c_int, [D, ctypes.POINTER(MoeCgRouter), vp, i32p, vp, vp,
+                                            i32p, vp, i32p, vp, vp]),
+            "moe_layer_forward_cg": (ctypes.c_int, [D, ctypes.POINTER(MoeCgRouter), vp, vp, vp,
+                                                    i32p, vp, i32p, vp, vp]),
             "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         }
         for name, (res, args) in sig.items():
@@ -222,6 +236,54 @@ def moe_layer_forward(desc, x, router_w, w_gate_up, w_down, k_per_token, out, de
     return lib().moe_layer_forward(ctypes.byref(d), _ptr(x), _ptr(router_w), _ptr(w_gate_up),
                                    _ptr(w_down), _ptr(k_per_token), _ptr(out), _ptr(dev_status),
                                    _ptr(workspace), _stream(stream))
+
+
+@dataclass
+class CgRouter:
+    """Python mirror of moe_cg_router (the training-free proxy router)."""
+    m: int
+    r: int
+    router_w_expert: torch.Tensor      # bf16 [n_experts, H]
+    proxy_w: torch.Tensor              # bf16 [E_r * 2 * r, H] (moe_pack_proxy_rows)
+    kappa: torch.Tensor                # int32 [k_max + 1, m] on the device
+
+    def c(self) -> MoeCgRouter:
+        g = MoeCgRouter()
+        g.m, g.r = int(self.m), int(self.r)
+        g.router_w_expert = _ptr(self.router_w_expert)
+        g.proxy_w = _ptr(self.proxy_w)
+        g.kappa = _ptr(self.kappa)
+        return g
+
+
+def moe_cg_workspace_size(desc: LayerDesc, cg: CgRouter) -> int:
+    d, g = desc.c(), cg.c()
+    return int(lib().moe_cg_workspace_size(ctypes.byref(d), ctypes.byref(g)))
+
+
+def moe_pack_proxy_rows(desc, r, w_gate_up, gate_neurons, proxy_w, dev_status,
+                        stream=None) -> int:
+    d = desc.c()
+    return lib().moe_pack_proxy_rows(ctypes.byref(d), int(r), _ptr(w_gate_up),
+                                     _ptr(gate_neurons), _ptr(proxy_w), _ptr(dev_status),
+                                     _stream(stream))
+
+
+def moe_route_cg(desc, cg, x, k_per_token, expert_logits_out, proxy_out, topk_idx, topk_w,
+                 dev_status, workspace, stream=None) -> int:
+    d, g = desc.c(), cg.c()
+    return lib().moe_route_cg(ctypes.byref(d), ctypes.byref(g), _ptr(x), _ptr(k_per_token),
+                              _ptr(expert_logits_out), _ptr(proxy_out), _ptr(topk_idx),
+                              _ptr(topk_w), _ptr(dev_status), _ptr(workspace), _stream(stream))
+
+
+def moe_layer_forward_cg(desc, cg, x, w_gate_up, w_down, k_per_token, out, dev_status,
+                         workspace, stream=None) -> int:
+    d, g = desc.c(), cg.c()
+    return lib().moe_layer_forward_cg(ctypes.byref(d), ctypes.byref(g), _ptr(x),
+                                      _ptr(w_gate_up), _ptr(w_down), _ptr(k_per_token),
+                                      _ptr(out), _ptr(dev_status), _ptr(workspace),
+                                      _stream(stream))
 
 
 def moe_get_device_status(dev_status, stream=None) -> int:

@@ -441,6 +441,127 @@ moe_status do_combine(const moe_layer_desc* d, const void* y_perm, const void* y
                                          d->k_max, static_cast<int>(n_cap), out, status, s));
 }
 
+// ---------------------------------------------------------------- proxy router
+
+moe_status validate_cg(const moe_layer_desc* d, const moe_cg_router* cg) {
+  MOE_TRY(validate(d));
+  if (cg == nullptr) return MOE_ERR_INVALID_ARGUMENT;
+  if (cg->m < 1 || cg->m > d->n_experts || cg->m > 32 || cg->r < 1 || cg->r > d->I_sub)
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (d->n_sub > 32 || d->k_max > cg->m * d->n_sub) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (cg->m * d->n_sub * cg->r > moe::kMaxProxyPairs) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+// The expert-level router: the layer's desc with one unit per expert and the
+// native m as k.
+moe_layer_desc expert_desc(const moe_layer_desc& d, int m) {
+  moe_layer_desc e = d;
+  e.n_sub = 1;
+  e.k_max = m;
+  e.I_shared = 0;
+  return e;
+}
+
+struct CgLayout {
+  size_t e_logits, e_part, e_idx, e_w, p_buf, total;
+  int e_slices;   // 0: expert logits on the tensor cores
+  bool p_dense;   // proxy pre-activations of every unit on the tensor cores (else kept
+                  // experts only, on CUDA cores)
+  int R;          // packed proxy rows = E_r * 2r
+};
+
+bool proxy_on_tensor_cores(const moe_layer_desc& d, int R) { return d.T >= 128 && R % 64 == 0; }
+
+// Placed after the layer's own workspace layout.
+CgLayout cg_layout_of(const moe_layer_desc& d, const moe_cg_router& cg) {
+  const size_t T = static_cast<size_t>(d.T), E = static_cast<size_t>(d.n_experts);
+  const moe_layer_desc ed = expert_desc(d, cg.m);
+  CgLayout c;
+  size_t o = layout_of(d).total;
+  auto take = [&o](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes);
+    return at;
+  };
+  int vs = 0;
+  c.R = E_r_of(&d) * 2 * cg.r;
+  c.e_slices = router_on_tensor_cores(ed) ? 0 : moe::router_slices(d.T, d.H, d.n_experts, &vs);
+  c.p_dense = proxy_on_tensor_cores(d, c.R);
+  c.e_logits = take(T * E * 4);
+  c.e_part = take(static_cast<size_t>(c.e_slices) * T * E * 4);
+  c.e_idx = take(T * cg.m * 4);
+  c.e_w = take(T * cg.m * 4);
+  const size_t rows_e = static_cast<size_t>(d.n_sub) * 2 * cg.r;   // per kept expert
+  c.p_buf = take(c.p_dense ? T * c.R * 4 : T * cg.m * rows_e * 4);
+  c.total = o;
+  return c;
+}
+
+moe_status do_route_cg(const moe_layer_desc* d, const moe_cg_router* cg, const void* x,
+                       const int32_t* kpt, float* expert_logits_out, float* proxy_out,
+                       int32_t* topk_idx, float* topk_w, int32_t* status, void* ws,
+                       cudaStream_t s) {
+  const CgLayout c = cg_layout_of(*d, *cg);
+  const moe_layer_desc ed = expert_desc(*d, cg->m);
+  int32_t* eidx = at<int32_t>(ws, c.e_idx);
+  float* ew = at<float>(ws, c.e_w);
+  // 1. the original router keeps m experts per token
+  if (c.e_slices == 0) {
+    float* dst = expert_logits_out != nullptr ? expert_logits_out : at<float>(ws, c.e_logits);
+    MOE_TRY(do_logits_gemm(&ed, x, cg->router_w_expert, dst, status, s));
+    MOE_TRY(cuda_status(moe::launch_topk_gate(dst, 1, nullptr, 1, nullptr, nullptr, d->T,
+                                              d->n_experts, cg->m, d->score, d->renorm,
+                                              d->route_scale, eidx, ew, status, s)));
+  } else {
+    float* part = at<float>(ws, c.e_part);
+    MOE_TRY(cuda_status(moe::launch_router_logits_small(x, cg->router_w_expert, d->T, d->H,
+                                                        d->n_experts, part, s)));
+    MOE_TRY(cuda_status(moe::launch_topk_gate(part, c.e_slices, d->expert_bias, 1,
+                                              expert_logits_out, nullptr, d->T, d->n_experts,
+                                              cg->m, d->score, d->renorm, d->route_scale, eidx,
+                                              ew, status, s)));
+  }
+  // 2. gate-neuron pre-activations of every unit (not needed when every
+  // expert has a single sub-expert and nobody asks for the scores)
+  float* pre = at<float>(ws, c.p_buf);
+  int S = 1;
+  if (d->n_sub == 1 && proxy_out == nullptr) {
+    pre = nullptr;
+  } else if (c.p_dense) {
+    GemmArgs g{};
+    g.epi = moe::EPI_F32;
+    g.a = x;
+    g.a_rows = d->T;
+    g.b = cg->proxy_w;
+    g.b_rows = c.R;
+    g.K = d->H;
+    g.offsets = nullptr;
+    g.n_groups = 1;
+    g.dense_rows = d->T;
+    g.n_out = c.R;
+    g.b_group_rows = 0;
+    g.out = pre;
+    g.ld_out = c.R;
+    g.out_rows = d->T;
+    g.bias = nullptr;
+    g.bias_div = 1;
+    g.status = status;
+    g.sm_count = sm_count();
+    g.max_rows_hint = d->T;
+    g.bn_hint = c.R % 256 == 0 ? 256 : (c.R % 128 == 0 ? 128 : 64);
+    MOE_TRY(cuda_status(moe::launch_gemm(g, s)));
+  } else {
+    MOE_TRY(cuda_status(moe::launch_proxy_gemv(x, cg->proxy_w, eidx, d->T, d->H, d->n_experts,
+                                               cg->m, d->n_sub * 2 * cg->r, pre, s)));
+  }
+  // 3. proxy scores and the per-expert top-kappa_j
+  return cuda_status(moe::launch_cg_select(pre, S, c.R, !c.p_dense, eidx, ew, cg->kappa, kpt,
+                                           d->T, cg->m,
+                                           d->n_sub, cg->r, d->k_max, d->n_experts, proxy_out,
+                                           topk_idx, topk_w, status, s));
+}
+
 }  // namespace
 
 extern "C" {
@@ -565,6 +686,67 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, const vo
   void* ysh = desc->I_shared > 0 ? at<void>(workspace, l.ysh) : nullptr;
   MOE_TRY(do_route(desc, x, router_w, nullptr, k_per_token, nullptr, topk_idx, topk_w,
                    dev_status, workspace, s));
+  MOE_TRY(do_permute(desc, topk_idx, k_per_token, counts, offsets, sorted_token, inv_row,
+                     dev_status, workspace, s));
+  if (ysh != nullptr) MOE_TRY(do_shared(desc, x, ysh, dev_status, workspace, s));
+  MOE_TRY(do_grouped_ffn(desc, x, sorted_token, offsets, w_gate_up, w_down, yperm, dev_status,
+                         workspace, s));
+  return do_combine(desc, yperm, ysh, inv_row, topk_w, k_per_token, out, dev_status, s);
+}
+
+size_t moe_cg_workspace_size(const moe_layer_desc* desc, const moe_cg_router* cg) {
+  if (validate_cg(desc, cg) != MOE_OK) return 0;
+  return cg_layout_of(*desc, *cg).total;
+}
+
+moe_status moe_pack_proxy_rows(const moe_layer_desc* desc, int32_t r, const void* w_gate_up,
+                               const int32_t* gate_neurons, void* proxy_w, int32_t* dev_status,
+                               void* stream) {
+  MOE_TRY(validate(desc));
+  if (r < 1 || r > desc->I_sub) return MOE_ERR_UNSUPPORTED_SHAPE;
+  MOE_TRY(check_ptrs({w_gate_up, proxy_w}));
+  MOE_TRY(check_ptrs4({gate_neurons, dev_status}));
+  return cuda_status(moe::launch_pack_proxy(w_gate_up, gate_neurons, E_r_of(desc), r,
+                                            desc->I_sub, desc->H, proxy_w, dev_status,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_route_cg(const moe_layer_desc* desc, const moe_cg_router* cg, const void* x,
+                        const int32_t* k_per_token, float* expert_logits_out, float* proxy_out,
+                        int32_t* topk_idx, float* topk_w, int32_t* dev_status, void* workspace,
+                        void* stream) {
+  MOE_TRY(validate_cg(desc, cg));
+  if (desc->T == 0) return MOE_OK;
+  MOE_TRY(check_ptrs({x, cg->router_w_expert, cg->proxy_w}));
+  MOE_TRY(check_ptrs4({cg->kappa, k_per_token, topk_idx, topk_w, dev_status}));
+  if (expert_logits_out != nullptr) MOE_TRY(check_ptrs4({expert_logits_out}));
+  if (proxy_out != nullptr) MOE_TRY(check_ptrs4({proxy_out}));
+  MOE_TRY(check_ws(workspace));
+  return do_route_cg(desc, cg, x, k_per_token, expert_logits_out, proxy_out, topk_idx, topk_w,
+                     dev_status, workspace, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_layer_forward_cg(const moe_layer_desc* desc, const moe_cg_router* cg,
+                                const void* x, const void* w_gate_up, const void* w_down,
+                                const int32_t* k_per_token, void* out, int32_t* dev_status,
+                                void* workspace, void* stream) {
+  MOE_TRY(validate_cg(desc, cg));
+  if (desc->T == 0) return MOE_OK;
+  MOE_TRY(check_ptrs({x, cg->router_w_expert, cg->proxy_w, w_gate_up, w_down, out}));
+  MOE_TRY(check_ptrs4({cg->kappa, k_per_token, dev_status}));
+  MOE_TRY(check_ws(workspace));
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Layout l = layout_of(*desc);
+  int32_t* topk_idx = at<int32_t>(workspace, l.topk_idx);
+  float* topk_w = at<float>(workspace, l.topk_w);
+  int32_t* counts = at<int32_t>(workspace, l.counts);
+  int32_t* offsets = at<int32_t>(workspace, l.offsets);
+  int32_t* sorted_token = at<int32_t>(workspace, l.sorted_token);
+  int32_t* inv_row = at<int32_t>(workspace, l.inv_row);
+  void* yperm = at<void>(workspace, l.yperm);
+  void* ysh = desc->I_shared > 0 ? at<void>(workspace, l.ysh) : nullptr;
+  MOE_TRY(do_route_cg(desc, cg, x, k_per_token, nullptr, nullptr, topk_idx, topk_w, dev_status,
+                      workspace, s));
   MOE_TRY(do_permute(desc, topk_idx, k_per_token, counts, offsets, sorted_token, inv_row,
                      dev_status, workspace, s));
   if (ysh != nullptr) MOE_TRY(do_shared(desc, x, ysh, dev_status, workspace, s));

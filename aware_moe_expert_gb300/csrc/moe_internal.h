@@ -18,12 +18,28 @@ cudaError_t launch_router_logits_small(const void* x, const void* router_w, int 
                                        int E_r, float* partial, cudaStream_t s);
 // Top-k_t and gates from the sum of S partial logit arrays [S, T, E_r] (S = 1:
 // finished logits) plus bias[u / n_sub] (nullable); logits_out (nullable)
-// receives the summed logits.
+// receives the summed logits; k_per_token == nullptr keeps k_max per token.
 cudaError_t launch_topk_gate(const float* partial, int S, const float* bias, int n_sub,
                              float* logits_out, const int32_t* k_per_token, int T, int E_r,
                              int k_max, int score, int renorm, float route_scale,
                              int32_t* topk_idx, float* topk_w, int32_t* status,
                              cudaStream_t s);
+
+// ---- cg_router.cu: training-free proxy router
+constexpr int kMaxProxyPairs = 2048;   // m * n_sub * r per token (8 KB of scores per warp)
+cudaError_t launch_pack_proxy(const void* w_gate_up, const int32_t* gate_neurons, int E_r, int r,
+                              int I_sub, int H, void* proxy_w, int32_t* status, cudaStream_t s);
+// Pre-activations of the kept experts' gate-neuron rows only: out fp32
+// [T, m, rows_e] (rows_e = n_sub * 2r); H <= 49152.
+cudaError_t launch_proxy_gemv(const void* x, const void* proxy_w, const int32_t* expert_idx,
+                              int T, int H, int n_experts, int m, int rows_e, float* out,
+                              cudaStream_t s);
+// partial: S arrays [T, R] (R = E_r * 2r), or with compact one [T, m, n_sub * 2r]
+cudaError_t launch_cg_select(const float* partial, int S, int R, bool compact,
+                             const int32_t* expert_idx, const float* expert_w,
+                             const int32_t* kappa, const int32_t* kpt, int T, int m, int N,
+                             int r, int k_max, int n_experts, float* proxy_out, int32_t* topk_idx,
+                             float* topk_w, int32_t* status, cudaStream_t s);
 
 // ---- permute.cu
 cudaError_t launch_permute(const int32_t* topk_idx, const int32_t* k_per_token, int T,

@@ -251,7 +251,8 @@ __device__ __forceinline__ int warp_topk(const float* __restrict__ P, int S, siz
 }
 
 // One warp per token, eight tokens per CTA.  P holds S partial logit arrays
-// [T, E_r] one after another (S = 1: finished logits).
+// [T, E_r] one after another (S = 1: finished logits).  kpt == nullptr: every
+// token keeps k_max units.
 template <int IPL>
 __global__ void __launch_bounds__(256) topk_gate_kernel(
     const float* __restrict__ P, int S, const float* __restrict__ bias, int n_sub,
@@ -266,7 +267,8 @@ __global__ void __launch_bounds__(256) topk_gate_kernel(
   float w;
   const size_t row = static_cast<size_t>(t) * E_r;
   warp_topk<IPL>(P + row, S, static_cast<size_t>(T) * E_r, bias, n_sub,
-                 logits_out != nullptr ? logits_out + row : nullptr, kpt[t], E_r, k_max, score,
+                 logits_out != nullptr ? logits_out + row : nullptr,
+                 kpt != nullptr ? kpt[t] : k_max, E_r, k_max, score,
                  renorm, route_scale, status, lane, &u, &w);
   if (lane < k_max) {
     const size_t o = static_cast<size_t>(t) * k_max + lane;

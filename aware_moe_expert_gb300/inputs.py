@@ -18,6 +18,12 @@ Distributions:
                     rank permutation (Zipf(s) popularity in logit space)
   k_per_token       uniform over the workload's choices, drawn per token or per
                     request (then shared by the request's tokens)
+  proxy router      expert-level router_w_expert ~ N(0, 1/H) (or router_std);
+                    gate neurons: r distinct local indices per unit, uniformly
+                    at random (a stand-in for the co-activation calibration,
+                    which needs real activations); allocation table: k split as
+                    evenly as possible over the m kept experts, the
+                    higher-ranked ones taking the remainder
 """
 from __future__ import annotations
 
@@ -29,7 +35,8 @@ import torch
 from .workloads import Workload
 
 _IDS = {"x": 1, "router_w": 2, "w_gate_up": 3, "w_down": 4, "bias": 5, "k": 6,
-        "w_shared_gate_up": 7, "w_shared_down": 8, "logits": 9}
+        "w_shared_gate_up": 7, "w_shared_down": 8, "logits": 9, "router_w_expert": 10,
+        "gate_neurons": 11}
 
 
 def _gen(seed: int, name: str, device) -> torch.Generator:
@@ -109,6 +116,38 @@ def make_layer_inputs(wl: Workload, device="cpu", seed: Optional[int] = None,
             d["w_shared_down"] = _normal_bf16((H, wl.I_shared), 1.0 / math.sqrt(wl.I_shared),
                                               _gen(seed, "w_shared_down", dev), dev)
     return d
+
+
+def draw_gate_neurons(wl: Workload, r: int, seed: Optional[int] = None) -> torch.Tensor:
+    """int32 [E_r, r]: r distinct local neuron indices per unit (random)."""
+    seed = wl.seed if seed is None else seed
+    g = _gen(seed, "gate_neurons", "cpu")
+    rows = [torch.randperm(wl.I_sub, generator=g)[:r] for _ in range(wl.E_r)]
+    return torch.stack(rows).to(torch.int32)
+
+
+def allocation_table(k_max: int, m: int, n_sub: int) -> torch.Tensor:
+    """int32 [k_max + 1, m]: row k gives each of the m kept experts
+    floor(k / m) sub-experts, plus one for the first k mod m of them."""
+    rows = []
+    for k in range(k_max + 1):
+        rows.append([k // m + (1 if j < k % m else 0) for j in range(m)])
+    t = torch.tensor(rows, dtype=torch.int32)
+    if int(t.max()) > n_sub:
+        raise ValueError("k_max exceeds m * n_sub")
+    return t
+
+
+def make_cg_inputs(wl: Workload, device="cpu", seed: Optional[int] = None, r: int = 8):
+    """Inputs of the proxy router: router_w_expert bf16 [n_experts, H], gate
+    neurons int32 [E_r, r], allocation table int32 [k_max + 1, native_m]."""
+    seed = wl.seed if seed is None else seed
+    dev = torch.device(device)
+    rstd = wl.router_std if wl.router_std is not None else 1.0 / math.sqrt(wl.H)
+    return {"router_w_expert": _normal_bf16((wl.n_experts, wl.H), rstd,
+                                            _gen(seed, "router_w_expert", dev), dev),
+            "gate_neurons": draw_gate_neurons(wl, r, seed).to(dev),
+            "kappa": allocation_table(wl.k_max, wl.native_m, wl.n_sub).to(dev)}
 
 
 def make_logits(T: int, E_r: int, device="cpu", seed: int = 7, kind: str = "normal"):

@@ -31,6 +31,7 @@ class Workload:
     I_shared: int = 0
     phase: str = "prefill"              # "prefill" or "decode" (what the bench reports)
     seed: int = 20261202
+    native_m: int = 2                   # the original model's experts per token (proxy router)
 
     @property
     def E_r(self) -> int:
@@ -61,14 +62,14 @@ MIXTRAL_DECODE = Workload("mixtral8x7b-decode-h4096-e8x4-t64", T=64, H=4096, n_e
 QWEN_PREFILL = Workload("qwen3-30b-a3b-prefill-h2048-e128-t8192", T=8192, H=2048,
                         n_experts=128, n_sub=1, I_sub=768, k_max=8, k_choices=(2, 4, 6, 8),
                         k_per="request", tokens_per_request=512, router_std=0.02,
-                        bias="zipf", seed=20261202 + 2)
+                        bias="zipf", seed=20261202 + 2, native_m=8)
 
 # Qwen3-30B-A3B-shaped decode sweep: 128 experts x 2 sub-experts of 384,
 # T in {1, 8, 64, 256, 1024} one-token requests, k ~ U{4..16}.
 QWEN_DECODE = Workload("qwen3-30b-a3b-decode-h2048-e128x2-t64", T=64, H=2048,
                        n_experts=128, n_sub=2, I_sub=384, k_max=16,
                        k_choices=tuple(range(4, 17)), k_per="token", phase="decode",
-                       seed=20261202 + 3)
+                       seed=20261202 + 3, native_m=8)
 QWEN_DECODE_T = (1, 8, 64, 256, 1024)
 
 # DeepSeek-V3-shaped prefill: 256 experts of 2048 plus one shared expert of 2048,
@@ -76,7 +77,7 @@ QWEN_DECODE_T = (1, 8, 64, 256, 1024)
 DEEPSEEK_PREFILL = Workload("deepseek-v3-prefill-h7168-e256-shared-t16384", T=16384, H=7168,
                             n_experts=256, n_sub=1, I_sub=2048, k_max=8, k_choices=(4, 6, 8),
                             k_per="request", tokens_per_request=512, score="sigmoid",
-                            renorm=True, I_shared=2048, seed=20261202 + 4)
+                            renorm=True, I_shared=2048, seed=20261202 + 4, native_m=8)
 
 ALL = {
     "tiny": TINY,

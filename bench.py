@@ -51,6 +51,10 @@ def parse():
     p.add_argument("--cpu-budget-s", type=float, default=30.0)
     p.add_argument("--path", type=int, default=0,
                    help="GEMM family: 0 auto, 1 token tiles, 2 weight-stationary (swap-AB)")
+    p.add_argument("--router", default="linear", choices=["linear", "cg"],
+                   help="linear: the expanded linear gate over all units (the default); "
+                        "cg: the training-free proxy router (original router + gate neurons)")
+    p.add_argument("--cg-r", type=int, default=8, help="gate neurons per sub-expert (--router cg)")
     p.add_argument("--force-pair", action="store_true",
                    help="run grouped prefill GEMMs on the CTA-pair kernel (debug flag)")
     return p.parse_args()
@@ -163,7 +167,18 @@ def run_ours(args, wl, rank, world, local):
     if args.force_pair:
         desc.debug_flags |= B.DEBUG_FORCE_PAIR
     T, H, E_r, k_max, I_sub = wl.T, wl.H, wl.E_r, wl.k_max, wl.I_sub
-    ws = torch.empty(B.moe_workspace_size(desc), dtype=torch.uint8, device=dev)
+    cg = None
+    if args.router == "cg":
+        from aware_moe_expert_gb300.inputs import make_cg_inputs
+        ci = make_cg_inputs(wl, dev, seed=wl.seed + 1000 * rank, r=args.cg_r)
+        proxy_w = torch.empty(E_r * 2 * args.cg_r, H, dtype=torch.bfloat16, device=dev)
+        st0 = torch.zeros(1, dtype=torch.int32, device=dev)
+        B.check(B.moe_pack_proxy_rows(desc, args.cg_r, d["w_gate_up"], ci["gate_neurons"],
+                                      proxy_w, st0), "moe_pack_proxy_rows")
+        cg = B.CgRouter(m=wl.native_m, r=args.cg_r, router_w_expert=ci["router_w_expert"],
+                        proxy_w=proxy_w, kappa=ci["kappa"])
+    ws_bytes = B.moe_workspace_size(desc) if cg is None else B.moe_cg_workspace_size(desc, cg)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     idx = torch.empty(T, k_max, dtype=torch.int32, device=dev)
     w = torch.empty(T, k_max, dtype=torch.float32, device=dev)
@@ -179,6 +194,10 @@ def run_ours(args, wl, rank, world, local):
     sp = stream.cuda_stream
 
     def call_route(sp):
+        if cg is not None:
+            B.check(B.moe_route_cg(desc, cg, d["x"], d["k_per_token"], None, None, idx, w, st, ws,
+                                   sp), "moe_route_cg")
+            return
         B.check(B.moe_route(desc, d["x"], d["router_w"], None, d["k_per_token"], None, idx, w,
                             st, ws, sp), "moe_route")
 
@@ -214,9 +233,14 @@ def run_ours(args, wl, rank, world, local):
             f(sp)
 
     out_fused = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
-    ws_fused = torch.empty(B.moe_workspace_size(desc), dtype=torch.uint8, device=dev)
+    ws_fused = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
 
     def layer_step(sp):
+        if cg is not None:
+            B.check(B.moe_layer_forward_cg(desc, cg, d["x"], d["w_gate_up"], d["w_down"],
+                                           d["k_per_token"], out_fused, st, ws_fused, sp),
+                    "moe_layer_forward_cg")
+            return
         B.check(B.moe_layer_forward(desc, d["x"], d["router_w"], d["w_gate_up"], d["w_down"],
                                     d["k_per_token"], out_fused, st, ws_fused, sp),
                 "moe_layer_forward")
@@ -322,6 +346,8 @@ def run_ours(args, wl, rank, world, local):
     e2e = None
     if not args.no_e2e:
         layer = B.MoeLayer(desc, dev)
+        if cg is not None:
+            layer.workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
         hx = d["x"].cpu().pin_memory()
         hk = d["k_per_token"].cpu().pin_memory()
         hout = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
@@ -337,8 +363,13 @@ def run_ours(args, wl, rank, world, local):
                     e0[i].record(stream)
                 dx.copy_(hx, non_blocking=True)
                 dk.copy_(hk, non_blocking=True)
-                B.check(B.moe_layer_forward(desc, dx, d["router_w"], d["w_gate_up"], d["w_down"],
-                                            dk, dout, layer.status, layer.workspace, sp))
+                if cg is not None:
+                    B.check(B.moe_layer_forward_cg(desc, cg, dx, d["w_gate_up"], d["w_down"], dk,
+                                                   dout, layer.status, layer.workspace, sp))
+                else:
+                    B.check(B.moe_layer_forward(desc, dx, d["router_w"], d["w_gate_up"],
+                                                d["w_down"], dk, dout, layer.status,
+                                                layer.workspace, sp))
                 hout.copy_(dout, non_blocking=True)
                 if i is not None:
                     e1[i].record(stream)
@@ -365,9 +396,12 @@ def run_ours(args, wl, rank, world, local):
     # algorithmic work (spec formulas)
     F_routed = 6.0 * H * I_sub * n_assign
     F_shared = 6.0 * H * wl.I_shared * T
-    F_router = 2.0 * T * H * E_r
+    # router rows: one per unit (linear gate), or the original router's rows
+    # plus the packed gate-neuron rows (proxy router)
+    router_rows = E_r if cg is None else wl.n_experts + E_r * 2 * args.cg_r
+    F_router = 2.0 * T * H * router_rows
     F = F_routed + F_shared + F_router
-    Bytes = 2.0 * (D * 3 * H * I_sub + 3 * H * wl.I_shared + E_r * H + 2 * T * H)
+    Bytes = 2.0 * (D * 3 * H * I_sub + 3 * H * wl.I_shared + router_rows * H + 2 * T * H)
     t_roof_us = max(F / (peaks["bf16_tflops"] * 1e12), Bytes / (peaks["hbm_gbs"] * 1e9)) * 1e6
     bound = "tensor" if F / (peaks["bf16_tflops"] * 1e12) > Bytes / (peaks["hbm_gbs"] * 1e9) else "hbm"
 
@@ -394,7 +428,7 @@ def run_ours(args, wl, rank, world, local):
                 "kernel": "moe_gate_up (row gather + grouped gate|up GEMM, SwiGLU epilogue)",
                 "algorithmic_flops": alg, "peak_source": peaks["source"] + " bf16_tflops (burst)"}
 
-    n_launch = launches_per_step(wl, T, args.path)
+    n_launch = launches_per_step(wl, T, args.path) + (2 if cg is not None else 0)
     us = ms * 1000.0
     res = {
         "metric": METRIC,
@@ -410,6 +444,9 @@ def run_ours(args, wl, rank, world, local):
                      "n_sub": wl.n_sub, "E_r": E_r, "I_sub": I_sub, "I_shared": wl.I_shared,
                      "k_choices": list(wl.k_choices), "k_per": wl.k_per, "score": wl.score,
                      "parallelism": f"replicas{world}",
+                     "router": ("linear gate over all units" if cg is None else
+                                f"proxy router: top-{wl.native_m} experts, {args.cg_r} gate "
+                                f"neurons per sub-expert, even allocation table"),
                      "l2": (f"flushed between steps ({2 * l2 >> 20} MiB write)" if flush else
                             f"inputs larger than L2 ({w_active / 2**20:.0f} MiB of active weights "
                             f"per step vs {l2 >> 20} MiB L2)")}

@@ -183,6 +183,60 @@ moe_status moe_permute_static(const moe_layer_desc* desc, const int32_t* topk_id
                               int32_t* sorted_token, int32_t* inv_row, int32_t* dev_status,
                               void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Training-free proxy router (MoE-Prism §III-B2, "Training-Free Proxy Gating",
+ * Fig. 7 left).  The original router scores the n_experts original experts and
+ * keeps its native m of them per token (selection, normalisation and scaling
+ * as moe_route, with one unit per expert); for each kept expert j and each of
+ * its n_sub sub-experts, the proxy score is
+ *     s_n = (1/r) sum_{c in G_n} |SiLU(x . Wg[c]) * (x . Wu[c])|
+ * over the sub-expert's r gate neurons G_n; the kappa_j best sub-experts of
+ * expert j (kappa = row k_t of the allocation table) are routed, each with the
+ * expert's weight w_j (no second softmax).  Ties: lower index first.
+ */
+typedef struct {
+  int32_t m;                   /* original experts kept per token, 1..min(n_experts, 32) */
+  int32_t r;                   /* gate neurons per sub-expert, 1..I_sub                   */
+  const void* router_w_expert; /* bf16 [n_experts, H]: the original router                */
+  const void* proxy_w;         /* bf16 [E_r * 2 * r, H], from moe_pack_proxy_rows         */
+  const int32_t* kappa;        /* device int32 [k_max + 1, m]: row k allocates a budget k;
+                                  a row with entries outside [0, n_sub] or not summing to
+                                  k gives MOE_ERR_K_RANGE and no units for that token     */
+} moe_cg_router;
+/* Requirements beyond moe_layer_desc's: n_sub <= 32, k_max <= m * n_sub,
+ * m * n_sub * r <= 2048 (else MOE_ERR_UNSUPPORTED_SHAPE). */
+
+/* Workspace bytes for moe_route_cg and moe_layer_forward_cg (0 on a bad desc).
+ * It includes moe_workspace_size(desc) (at its start). */
+size_t moe_cg_workspace_size(const moe_layer_desc* desc, const moe_cg_router* cg);
+
+/* Model set-up: gather the gate-neuron rows of every unit into
+ *   proxy_w bf16 [E_r * 2 * r, H]: row (u * r + i) * 2 = w_gate_up[u] gate row
+ *   gate_neurons[u * r + i], the next row the matching up row.
+ *   gate_neurons  device int32 [E_r, r], indices local to the unit (0..I_sub-1);
+ *                 an index outside that range -> MOE_ERR_BAD_INDEX, zero rows. */
+moe_status moe_pack_proxy_rows(const moe_layer_desc* desc, int32_t r, const void* w_gate_up,
+                               const int32_t* gate_neurons, void* proxy_w, int32_t* dev_status,
+                               void* stream);
+
+/* Routing with the proxy router.  Outputs as moe_route (topk_idx [T, k_max],
+ * best-ranked expert first, inside an expert by proxy score; topk_w [T, k_max]),
+ * plus, when non-null,
+ *   expert_logits_out  fp32 [T, n_experts]: the original router's logits + bias
+ *   proxy_out          fp32 [T, m, n_sub]: the proxy scores the selection used.
+ * Workspace: moe_cg_workspace_size bytes. */
+moe_status moe_route_cg(const moe_layer_desc* desc, const moe_cg_router* cg, const void* x,
+                        const int32_t* k_per_token, float* expert_logits_out, float* proxy_out,
+                        int32_t* topk_idx, float* topk_w, int32_t* dev_status, void* workspace,
+                        void* stream);
+
+/* The whole layer with the proxy router: route_cg -> permute -> [shared FFN] ->
+ * grouped FFN -> combine.  out bf16 [T, H].  Workspace: moe_cg_workspace_size. */
+moe_status moe_layer_forward_cg(const moe_layer_desc* desc, const moe_cg_router* cg,
+                                const void* x, const void* w_gate_up, const void* w_down,
+                                const int32_t* k_per_token, void* out, int32_t* dev_status,
+                                void* workspace, void* stream);
+
 /* Synchronises `stream`, then returns the code stored in *dev_status
  * (MOE_OK if zero), or MOE_ERR_CUDA if the synchronisation itself failed. */
 moe_status moe_get_device_status(const int32_t* dev_status, void* stream);

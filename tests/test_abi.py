@@ -90,3 +90,40 @@ def test_host_rejects_bad_arguments_without_a_gpu(lib):
     assert B.moe_shared_ffn(_desc(), fake, fake, fake, ws, 0) == 1
     assert B.moe_workspace_size(_desc(I_shared=128)) == 0
     assert B.moe_get_device_status(None, 0) == 1
+
+
+def _cg(m=2, r=4):
+    fake = 1 << 20
+    return B.CgRouter(m=m, r=r, router_w_expert=fake, proxy_w=fake, kappa=fake)
+
+
+@pytest.mark.parametrize("kw,cg_kw,expect_zero", [
+    (dict(), dict(), False),
+    (dict(), dict(m=0), True),                       # m < 1
+    (dict(), dict(m=17), True),                      # m > n_experts
+    (dict(), dict(r=0), True),
+    (dict(), dict(r=129), True),                     # r > I_sub
+    (dict(n_experts=2, n_sub=33, k_max=8), dict(), True),   # n_sub > 32
+    (dict(k_max=9), dict(m=2), True),                # k_max > m * n_sub
+])
+def test_cg_workspace_size_validates(lib, kw, cg_kw, expect_zero):
+    n = B.moe_cg_workspace_size(_desc(**kw), _cg(**cg_kw))
+    assert (n == 0) == expect_zero
+    if not expect_zero:
+        assert n > B.moe_workspace_size(_desc(**kw)) and n % 256 == 0
+
+
+def test_cg_calls_reject_bad_arguments_without_a_gpu(lib):
+    d, fake, ws = _desc(), 1 << 20, 1 << 21
+    assert B.moe_route_cg(d, _cg(m=0), fake, fake, None, None, fake, fake, fake, ws, 0) == 2
+    assert B.moe_route_cg(d, _cg(), None, fake, None, None, fake, fake, fake, ws, 0) == 1
+    assert B.moe_route_cg(d, _cg(), fake, fake, None, None, fake, fake, fake, None, 0) == 3
+    assert B.moe_pack_proxy_rows(d, 0, fake, fake, fake, fake, 0) == 2
+    assert B.moe_pack_proxy_rows(d, 4, fake + 2, fake, fake, fake, 0) == 1
+    assert B.moe_layer_forward_cg(d, _cg(), fake, fake, fake, fake, fake, fake, ws + 16, 0) == 3
+
+
+def test_cg_rejects_too_many_proxy_pairs(lib):
+    # m * n_sub * r = 4 * 4 * 129 > 2048
+    assert B.moe_cg_workspace_size(_desc(I_sub=256), _cg(m=4, r=129)) == 0
+    assert B.moe_cg_workspace_size(_desc(I_sub=256), _cg(m=4, r=128)) > 0

@@ -177,3 +177,12 @@ def test_invalid_allocation_row_is_flagged_and_routes_nothing():
     assert res["flags"] & O.FLAG_K_RANGE
     assert (res["topk_idx"][0] == -1).all()
     assert (res["topk_idx"][1, :2] >= 0).all()
+
+
+def test_package_allocation_table_equals_the_oracle_default():
+    """The bench's input generator builds the allocation table on its own; it
+    must equal the oracle's default rule on every workload shape."""
+    from aware_moe_expert_gb300 import inputs as I, workloads as W
+    for wl in W.ALL.values():
+        got = I.allocation_table(wl.k_max, wl.native_m, wl.n_sub).numpy()
+        np.testing.assert_array_equal(got, CG.default_kappa(wl.k_max, wl.native_m, wl.n_sub))

@@ -216,6 +216,10 @@ moe_status do_route(const moe_layer_desc* d, const void* x, const void* router_w
       float* dst = logits_out != nullptr ? logits_out : at<float>(ws, l.logits);
       MOE_TRY(do_logits_gemm(d, x, router_w, dst, status, s));
       P = dst;
+    } else if (moe::route_cluster_supports(d->H, E_r)) {
+      return cuda_status(moe::launch_route_cluster(
+          x, router_w, d->expert_bias, d->n_sub, kpt, d->T, d->H, E_r, d->k_max, d->score,
+          d->renorm, d->route_scale, logits_out, topk_idx, topk_w, status, nullptr, s));
     } else {
       float* part = at<float>(ws, l.router_partial);
       MOE_TRY(cuda_status(
@@ -350,22 +354,35 @@ moe_status do_down(const moe_layer_desc* d, const void* act, const int32_t* offs
 // Both FFN projections.  Decode-shaped batches with H and I_sub multiples of
 // 128 run the fused kernel (gate|up and down overlapped in one launch);
 // otherwise gate|up then down.
+bool use_decode_ffn(const moe_layer_desc* d) {
+  return use_decode_path(d, d->I_sub, true) && use_decode_path(d, d->H, false) &&
+         moe::decode_ffn_supports(d->H, d->I_sub);
+}
+
+// Counters of the fused decode FFN kernel (one per 64-row chunk), zeroed by
+// the launch that writes x_perm.
+inline int decode_ffn_counters(const moe_layer_desc* d) {
+  return static_cast<int>(static_cast<long long>(d->T) * d->k_max / 64 + E_r_of(d) + 1);
+}
+
+// pre_gathered: x_perm already holds the permuted rows and the decode FFN's
+// counters are zero (the fused small-batch router wrote them).
 moe_status do_grouped_ffn(const moe_layer_desc* d, const void* x, const int32_t* sorted_token,
                           const int32_t* offsets, const void* w_gate_up, const void* w_down,
-                          void* y_perm, int32_t* status, void* ws, cudaStream_t s) {
+                          void* y_perm, int32_t* status, void* ws, cudaStream_t s,
+                          bool pre_gathered = false) {
   const Layout l = layout_of(*d);
   void* act = at<void>(ws, l.act);
   const long long n_cap = static_cast<long long>(d->T) * d->k_max;
   if (n_cap == 0) return MOE_OK;
-  if (use_decode_path(d, d->I_sub, true) && use_decode_path(d, d->H, false) &&
-      moe::decode_ffn_supports(d->H, d->I_sub)) {
+  if (use_decode_ffn(d)) {
     const int E_r = E_r_of(d);
     void* xperm = at<void>(ws, l.xperm);
     int32_t* done = at<int32_t>(ws, l.chunk_done);
-    const int n_done = static_cast<int>(n_cap / 64 + E_r + 1);
-    MOE_TRY(cuda_status(moe::launch_gather_rows(x, sorted_token, offsets, E_r, d->T, d->H,
-                                                static_cast<int>(n_cap), xperm, status,
-                                                sm_count(), s, done, n_done)));
+    if (!pre_gathered)
+      MOE_TRY(cuda_status(moe::launch_gather_rows(x, sorted_token, offsets, E_r, d->T, d->H,
+                                                  static_cast<int>(n_cap), xperm, status,
+                                                  sm_count(), s, done, decode_ffn_counters(d))));
     moe::DecodeFfnArgs a{};
     a.x_perm = xperm;
     a.x_rows = n_cap;
@@ -684,13 +701,30 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, const vo
   void* act = at<void>(workspace, l.act);
   void* yperm = at<void>(workspace, l.yperm);
   void* ysh = desc->I_shared > 0 ? at<void>(workspace, l.ysh) : nullptr;
-  MOE_TRY(do_route(desc, x, router_w, nullptr, k_per_token, nullptr, topk_idx, topk_w,
-                   dev_status, workspace, s));
-  MOE_TRY(do_permute(desc, topk_idx, k_per_token, counts, offsets, sorted_token, inv_row,
+  const int E_r = E_r_of(desc);
+  bool gathered = false;
+  if (desc->T <= moe::kRouteFuseMaxT && !router_on_tensor_cores(*desc) &&
+      moe::route_cluster_supports(desc->H, E_r)) {
+    // small batch: logits, top-k, permutation (and the row gather of the
+    // fused decode FFN) in one launch
+    gathered = use_decode_ffn(desc);
+    moe::RoutePermuteOut f{counts, offsets, sorted_token, inv_row,
+                           gathered ? at<void>(workspace, l.xperm) : nullptr,
+                           gathered ? at<int32_t>(workspace, l.chunk_done) : nullptr,
+                           gathered ? decode_ffn_counters(desc) : 0};
+    MOE_TRY(cuda_status(moe::launch_route_cluster(
+        x, router_w, desc->expert_bias, desc->n_sub, k_per_token, desc->T, desc->H, E_r,
+        desc->k_max, desc->score, desc->renorm, desc->route_scale, nullptr, topk_idx, topk_w,
+        dev_status, &f, s)));
+  } else {
+    MOE_TRY(do_route(desc, x, router_w, nullptr, k_per_token, nullptr, topk_idx, topk_w,
                      dev_status, workspace, s));
+    MOE_TRY(do_permute(desc, topk_idx, k_per_token, counts, offsets, sorted_token, inv_row,
+                       dev_status, workspace, s));
+  }
   if (ysh != nullptr) MOE_TRY(do_shared(desc, x, ysh, dev_status, workspace, s));
   MOE_TRY(do_grouped_ffn(desc, x, sorted_token, offsets, w_gate_up, w_down, yperm, dev_status,
-                         workspace, s));
+                         workspace, s, gathered));
   return do_combine(desc, yperm, ysh, inv_row, topk_w, k_per_token, out, dev_status, s);
 }
 

@@ -25,6 +25,27 @@ cudaError_t launch_topk_gate(const float* partial, int S, const float* bias, int
                              int32_t* topk_idx, float* topk_w, int32_t* status,
                              cudaStream_t s);
 
+// Logits and top-k_t of clusters of eight tokens in one launch (mma.sync
+// tiles, H % 16 == 0, E_r <= 256).  With `fuse` (T <= 8 only) the same launch also
+// writes the permutation (counts, offsets, sorted_token, inv_row), copies the
+// permuted x rows into x_perm (when non-null) and zeroes zero_ptr[0, zero_n).
+struct RoutePermuteOut {
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* sorted_token;
+  int32_t* inv_row;
+  void* x_perm;
+  int32_t* zero_ptr;
+  int zero_n;
+};
+bool route_cluster_supports(int H, int E_r);
+constexpr int kRouteFuseMaxT = 8;
+cudaError_t launch_route_cluster(const void* x, const void* router_w, const float* bias,
+                                 int n_sub, const int32_t* k_per_token, int T, int H, int E_r,
+                                 int k_max, int score, int renorm, float route_scale,
+                                 float* logits_out, int32_t* topk_idx, float* topk_w,
+                                 int32_t* status, const RoutePermuteOut* fuse, cudaStream_t s);
+
 // ---- cg_router.cu: training-free proxy router
 constexpr int kMaxProxyPairs = 2048;   // m * n_sub * r per token (8 KB of scores per warp)
 cudaError_t launch_pack_proxy(const void* w_gate_up, const int32_t* gate_neurons, int E_r, int r,

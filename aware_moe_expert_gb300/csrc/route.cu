@@ -110,22 +110,84 @@ __device__ __forceinline__ float key_to_logit(uint32_t key) {
   return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
 }
 
+// The k best of the 32 * IPL units a warp holds (lane l holds units l,
+// l + 32, ...; key[i] = order_key of unit lane + 32 i, units >= E_r absent),
+// best first, ties to the lower index.  Lane j < k returns
+// (key << 32) | ~u of the j-th unit; other lanes return 0.  buf: 32 words of
+// this warp's shared memory.
+//
+// 1. Radix select of the k-th largest key: bit by bit from the top, keep the
+//    candidate threshold if at least k keys reach it (ballot counts; stops
+//    early once exactly k do).
+// 2. Every unit above the threshold is selected, plus the lowest-index units
+//    equal to it until k are taken.
+// 3. The k selected units are packed into buf, each lane j < k counts the
+//    selected units that order before its own (its rank), and the units are
+//    stored back at their ranks.
+template <int IPL>
+__device__ __forceinline__ unsigned long long warp_select_topk(const uint32_t (&key)[IPL],
+                                                               int E_r, int k, int lane,
+                                                               unsigned long long* buf) {
+  if (k <= 0) return 0ull;
+  uint32_t thr = 0u;
+  int at_thr = E_r;   // units with key >= thr
+  for (int b = 31; b >= 0 && at_thr != k; --b) {
+    const uint32_t cand = thr | (1u << b);
+    int c = 0;
+#pragma unroll
+    for (int i = 0; i < IPL; ++i) c += __popc(__ballot_sync(0xffffffffu, key[i] >= cand));
+    if (c >= k) {
+      thr = cand;
+      at_thr = c;
+    }
+  }
+  int above = 0;
+#pragma unroll
+  for (int i = 0; i < IPL; ++i) above += __popc(__ballot_sync(0xffffffffu, key[i] > thr));
+  const int need = k - above;   // units taken from those equal to thr
+  const uint32_t lt = (1u << lane) - 1u;
+  int taken_eq = 0, packed = 0;
+#pragma unroll
+  for (int i = 0; i < IPL; ++i) {
+    const int u = lane + 32 * i;
+    const bool eq = u < E_r && key[i] == thr;
+    const uint32_t meq = __ballot_sync(0xffffffffu, eq);
+    const bool sel = key[i] > thr || (eq && taken_eq + __popc(meq & lt) < need);
+    taken_eq += __popc(meq);
+    const uint32_t msel = __ballot_sync(0xffffffffu, sel);
+    if (sel)
+      buf[packed + __popc(msel & lt)] =
+          (static_cast<unsigned long long>(key[i]) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(u));
+    packed += __popc(msel);
+  }
+  __syncwarp();
+  unsigned long long mine = 0ull;
+  int rank = 0;
+  if (lane < k) {
+    mine = buf[lane];
+    for (int m = 0; m < k; ++m) rank += buf[m] > mine ? 1 : 0;
+  }
+  __syncwarp();
+  if (lane < k) buf[rank] = mine;
+  __syncwarp();
+  const unsigned long long best = lane < k ? buf[lane] : 0ull;
+  __syncwarp();
+  return best;
+}
+
 // One warp selects the k_t best units of one token.  Lane l holds units l,
 // l+32, ... (IPL per lane); the token's logit of unit u is the sum of the S
 // partial rows P[s] (s in order; S = 1 for finished logits) plus
 // bias[u / n_sub] when bias is given, and is stored to lout[u] when lout is
-// given.  Selection: a bitonic sort of all units on (key << 32 | ~u) in the
-// warp's registers (key descending, lower index first on equal keys), so
-// lane j < k ends up holding the j-th unit (*out_u) and its gate weight after
-// renormalisation and route_scale (*out_w).
-// Returns k.
+// given.  Lane j < k ends up holding the j-th unit (*out_u) and its gate
+// weight after renormalisation and route_scale (*out_w).  Returns k.
 template <int IPL>
 __device__ __forceinline__ int warp_topk(const float* __restrict__ P, int S, size_t sstride,
                                          const float* __restrict__ bias, int n_sub,
                                          float* __restrict__ lout, int kt, int E_r, int k_max,
                                          int score, int renorm, float route_scale,
-                                         int32_t* status, int lane, int* out_u,
-                                         float* out_w) {
+                                         int32_t* status, int lane, unsigned long long* buf,
+                                         int* out_u, float* out_w) {
   int k = kt;
   if (k < 1 || k > k_max) {
     if (lane == 0) report(status, MOE_ERR_K_RANGE);
@@ -189,52 +251,7 @@ __device__ __forceinline__ int warp_topk(const float* __restrict__ P, int S, siz
     for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
   }
 
-  // Sort all 32 * IPL units best first: a bitonic network over positions
-  // p = lane * IPL + i (strides below IPL inside a lane, the rest across
-  // lanes) on (key << 32 | ~u), which orders equal keys by lower index.
-  unsigned long long c[IPL];
-#pragma unroll
-  for (int i = 0; i < IPL; ++i) {
-    const int u = lane + 32 * i;
-    c[i] = u < E_r ? (static_cast<unsigned long long>(key[i]) << 32) |
-                         static_cast<uint32_t>(~static_cast<uint32_t>(u))
-                   : 0ull;  // below every unit, NaN ones included
-  }
-  constexpr int N = 32 * IPL;
-#pragma unroll
-  for (int size = 2; size <= N; size <<= 1) {
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      if (stride >= IPL) {
-#pragma unroll
-        for (int i = 0; i < IPL; ++i) {
-          const unsigned long long o = __shfl_xor_sync(0xffffffffu, c[i], stride / IPL);
-          const int p = lane * IPL + i;
-          const bool take_max = ((p & stride) == 0) == ((p & size) == 0);
-          c[i] = take_max ? (o > c[i] ? o : c[i]) : (o < c[i] ? o : c[i]);
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < IPL; ++i) {
-          if ((i & stride) == 0) {
-            const int j = i | stride;
-            const bool desc = ((lane * IPL + i) & size) == 0;
-            const unsigned long long hi = c[i] > c[j] ? c[i] : c[j];
-            const unsigned long long lo = c[i] > c[j] ? c[j] : c[i];
-            c[i] = desc ? hi : lo;
-            c[j] = desc ? lo : hi;
-          }
-        }
-      }
-    }
-  }
-  // lane j takes position j (held by lane j / IPL, item j % IPL)
-  unsigned long long best = 0ull;
-#pragma unroll
-  for (int i = 0; i < IPL; ++i) {
-    const unsigned long long o = __shfl_sync(0xffffffffu, c[i], lane / IPL);
-    if (i == lane % IPL) best = o;
-  }
+  const unsigned long long best = warp_select_topk<IPL>(key, E_r, k, lane, buf);
   int my_u = -1;
   float my_s = 0.f;
   if (lane < k) {
@@ -259,6 +276,7 @@ __global__ void __launch_bounds__(256) topk_gate_kernel(
     float* __restrict__ logits_out, const int32_t* __restrict__ kpt, int T, int E_r,
     int k_max, int score, int renorm, float route_scale, int32_t* __restrict__ topk_idx,
     float* __restrict__ topk_w, int32_t* status) {
+  __shared__ unsigned long long sbuf[8][32];
   pdl_wait_and_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
@@ -269,11 +287,328 @@ __global__ void __launch_bounds__(256) topk_gate_kernel(
   warp_topk<IPL>(P + row, S, static_cast<size_t>(T) * E_r, bias, n_sub,
                  logits_out != nullptr ? logits_out + row : nullptr,
                  kpt != nullptr ? kpt[t] : k_max, E_r, k_max, score,
-                 renorm, route_scale, status, lane, &u, &w);
+                 renorm, route_scale, status, lane, sbuf[warp], &u, &w);
   if (lane < k_max) {
     const size_t o = static_cast<size_t>(t) * k_max + lane;
     topk_idx[o] = u;
     topk_w[o] = w;
+  }
+}
+
+// ---------------------------------------------------------------- cluster router
+// Logits and top-k_t of up to eight tokens in one launch.  A cluster of C
+// CTAs (16, else 8) splits the units; each CTA stages its units' router rows
+// and the eight tokens' x rows in shared memory, chunk by chunk of the hidden
+// dimension (cp.async, two chunks in flight), and its 16 warps split every
+// chunk's k-steps between them: per k-step one mma.sync m16n8k16 (16 units x
+// 8 tokens, bf16 in, fp32 out).  The warps' partial tiles are added in warp
+// order, and each CTA pushes its logits into CTA 0's shared memory.  After a
+// cluster barrier CTA 0 runs the warp top-k per token.  With a single cluster
+// holding every token (T <= 8) the same launch also builds the permutation in
+// shared memory and, after a second cluster barrier, every CTA copies its
+// share of the permuted x rows.
+constexpr int kClTok = 8;
+constexpr int kClThreads = 512;
+constexpr int kClWarps = kClThreads / 32;
+constexpr int kClMaxMt = 2;                      // 16-unit m-tiles per CTA (C >= 8, E_r <= 256)
+constexpr uint32_t kClStageBudget = 208 * 1024;  // staged rows, all chunks in flight
+
+struct ClusterRouteParams {
+  const uint4* x;
+  const uint4* rw;
+  const float* bias;
+  int n_sub;
+  const int32_t* kpt;
+  int T, nv, E_r, k_max, score, renorm;
+  float route_scale;
+  float* logits_out;
+  int32_t* topk_idx;
+  float* topk_w;
+  int32_t* status;
+  int C;                 // CTAs per cluster
+  int MT;                // 16-unit m-tiles per CTA: ceil(ceil(E_r / C) / 16)
+  int kc;                // hidden columns per staged chunk (multiple of 16)
+  int ns;                // chunk buffers (1: all of H at once, or 2)
+  // fused permutation (nullptr: route only) and row gather (x_perm nullptr: none)
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* sorted_token;
+  int32_t* inv_row;
+  uint4* x_perm;
+  int32_t* zero_ptr;
+  int zero_n;
+};
+
+struct ClusterSmem {
+  uint32_t pitch, rows, stage, red, all, buf, bits, off, sorted, wt, total;
+};
+
+// Staged rows per buffer: MT * 16 unit rows, then the eight token rows, each
+// kc columns plus 16 bytes of padding (conflict-free ldmatrix).  The warps'
+// partial tiles reuse the staging area once the last chunk is consumed.
+__host__ __device__ inline ClusterSmem cluster_smem(int E_r, int MT, int kc, int ns) {
+  ClusterSmem o;
+  o.pitch = static_cast<uint32_t>(kc) * 2 + 16;
+  o.rows = static_cast<uint32_t>(MT * 16 + kClTok);
+  uint32_t b = 0;
+  o.stage = b;
+  o.red = b;                                     // [warp][m-tile][16 x 8] fp32
+  const uint32_t st = static_cast<uint32_t>(ns) * o.rows * o.pitch;
+  const uint32_t red = static_cast<uint32_t>(kClWarps * MT * 128 * 4);
+  b += st > red ? st : red;
+  b = (b + 15) & ~15u;
+  o.all = b;
+  b += kClTok * E_r * 4;
+  b = (b + 7) & ~7u;
+  o.buf = b;
+  b += kClWarps * 32 * 8;
+  o.bits = b;
+  b += 256 * 4;
+  o.off = b;
+  b += 260 * 4;
+  o.sorted = b;
+  b += 256 * 4;
+  o.wt = b;
+  b += kClWarps * 4;
+  o.total = b;
+  return o;
+}
+
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_cluster_s32(uint32_t addr) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t (&r)[2]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
+               : "=r"(r[0]), "=r"(r[1])
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
+                                          const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+template <int IPL>
+__global__ void __launch_bounds__(kClThreads, 1) route_cluster_kernel(const ClusterRouteParams p) {
+  extern __shared__ __align__(16) uint8_t csm[];
+  const ClusterSmem L = cluster_smem(p.E_r, p.MT, p.kc, p.ns);
+  float* s_red = reinterpret_cast<float*>(csm + L.red);
+  float* s_all = reinterpret_cast<float*>(csm + L.all);
+  unsigned long long* sbuf = reinterpret_cast<unsigned long long*>(csm + L.buf);
+  uint32_t* s_bits = reinterpret_cast<uint32_t*>(csm + L.bits);
+  int32_t* s_off = reinterpret_cast<int32_t*>(csm + L.off);
+  int32_t* s_sorted = reinterpret_cast<int32_t*>(csm + L.sorted);
+  int32_t* s_wt = reinterpret_cast<int32_t*>(csm + L.wt);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool fused = p.counts != nullptr;
+  const int t0 = blockIdx.y * kClTok;
+  const int nt = min(kClTok, p.T - t0);
+  const int nv = p.nv, E_r = p.E_r, MT = p.MT;
+  const int U = (E_r + p.C - 1) / p.C;           // units per CTA (<= MT * 16)
+  const int u0 = static_cast<int>(rank) * U;
+  const int nu = max(0, min(U, E_r - u0));
+  const int n_mt = (nu + 15) / 16;
+  const uint32_t pitch = L.pitch;
+  const uint32_t stage_bytes = L.rows * pitch;
+  const uint32_t tok_row0 = static_cast<uint32_t>(MT * 16);
+  if (fused && rank == 0)
+    for (int u = tid; u < 256; u += kClThreads) s_bits[u] = 0u;
+  // rows no chunk writes (units past nu, tokens past nt) are zero in every buffer
+  {
+    const int zrows_u = MT * 16 - nu, zrows_t = kClTok - nt;
+    const int vpr = p.kc / 8;
+    const int total = p.ns * (zrows_u + zrows_t) * vpr;
+    for (int i = tid; i < total; i += kClThreads) {
+      const int per = (zrows_u + zrows_t) * vpr;
+      const int s = i / per, j = i - s * per;
+      const int zr = j / vpr, v = j - zr * vpr;
+      const int row = zr < zrows_u ? nu + zr : MT * 16 + nt + (zr - zrows_u);
+      *reinterpret_cast<uint4*>(csm + L.stage + s * stage_bytes + row * pitch + v * 16) =
+          make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  pdl_wait_and_trigger();
+
+  // chunk c -> buffer c % ns: unit rows [0, nu), token rows [MT * 16, + nt)
+  const int vc = p.kc / 8;                       // 16-byte vectors per chunk row
+  const int n_chunks = (nv + vc - 1) / vc;
+  const uint32_t stage0 = smem_u32(csm + L.stage);
+  auto issue = [&](int c) {
+    const uint32_t base = stage0 + static_cast<uint32_t>((c % p.ns) * stage_bytes);
+    const int v0 = c * vc, nvc = min(vc, nv - v0);
+    const int total = (nu + nt) * nvc;
+    for (int i = tid; i < total; i += kClThreads) {
+      const int r = i / nvc, v = i - r * nvc;
+      const uint4* src;
+      uint32_t srow;
+      if (r < nu) {
+        src = p.rw + static_cast<size_t>(u0 + r) * nv;
+        srow = static_cast<uint32_t>(r);
+      } else {
+        src = p.x + static_cast<size_t>(t0 + r - nu) * nv;
+        srow = tok_row0 + static_cast<uint32_t>(r - nu);
+      }
+      cp_async16(base + srow * pitch + static_cast<uint32_t>(v * 16), src + v0 + v);
+    }
+    cp_async_commit();
+  };
+  float acc[kClMaxMt][4];
+#pragma unroll
+  for (int m = 0; m < kClMaxMt; ++m)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[m][j] = 0.f;
+  if (nu > 0) {
+    issue(0);
+    if (n_chunks > 1 && p.ns > 1) issue(1);
+  }
+  for (int c = 0; c < n_chunks && nu > 0; ++c) {
+    if (c + 1 < n_chunks && p.ns > 1)
+      cp_async_wait<1>();
+    else
+      cp_async_wait<0>();
+    __syncthreads();
+    const uint32_t base = stage0 + static_cast<uint32_t>((c % p.ns) * stage_bytes);
+    const int ks = min(vc, nv - c * vc) / 2;     // 16-column k-steps in this chunk
+    // A (units, row-major): matrix i = lane / 8 -> rows (i & 1) * 8 + lane % 8, k + (i >> 1) * 8
+    const uint32_t a_off = ((lane & 7) + ((lane >> 3) & 1) * 8) * pitch + (lane >> 4) * 16;
+    // B (tokens, k contiguous): matrix i = (lane / 8) & 1 -> token lane % 8, k + i * 8
+    const uint32_t b_off = (tok_row0 + (lane & 7)) * pitch + ((lane >> 3) & 1) * 16;
+    for (int k = warp; k < ks; k += kClWarps) {
+      uint32_t b[2];
+      ldsm_x2(base + b_off + static_cast<uint32_t>(k * 32), b);
+#pragma unroll
+      for (int m = 0; m < kClMaxMt; ++m) {
+        if (m < n_mt) {
+          uint32_t a[4];
+          ldsm_x4(base + a_off + static_cast<uint32_t>(m * 16) * pitch + static_cast<uint32_t>(k * 32), a);
+          mma_16816(acc[m], a, b);
+        }
+      }
+    }
+    __syncthreads();
+    if (c + p.ns < n_chunks) issue(c + p.ns);
+  }
+  // partial tiles -> s_red[warp][m][row][col] (over the staging area); C
+  // fragment: c0,c1 at row lane/4, cols 2(lane%4)+{0,1}; c2,c3 at row lane/4 + 8
+#pragma unroll
+  for (int m = 0; m < kClMaxMt; ++m) {
+    if (m < MT) {
+      float* t = s_red + (warp * MT + m) * 128;
+      const int r = lane >> 2, cc = (lane & 3) * 2;
+      t[r * 8 + cc] = acc[m][0];
+      t[r * 8 + cc + 1] = acc[m][1];
+      t[(r + 8) * 8 + cc] = acc[m][2];
+      t[(r + 8) * 8 + cc + 1] = acc[m][3];
+    }
+  }
+  __syncthreads();
+  // warps in order -> CTA 0's s_all[token][unit]
+  const uint32_t all0 = mapa_shared(smem_u32(s_all), 0u);
+  for (int i = tid; i < nt * nu; i += kClThreads) {
+    const int tt = i / nu, ul = i - tt * nu;
+    const int m = ul >> 4, r = ul & 15;
+    float v = 0.f;
+    for (int w = 0; w < kClWarps; ++w) v += s_red[(w * MT + m) * 128 + r * 8 + tt];
+    st_cluster_f32(all0 + static_cast<uint32_t>((tt * E_r + u0 + ul) * 4), v);
+  }
+  cluster_sync_all();
+
+  if (rank == 0) {
+    int my_u = -1, k = 0;
+    if (warp < nt) {
+      const int t = t0 + warp;
+      const size_t row = static_cast<size_t>(t) * E_r;
+      float w;
+      k = warp_topk<IPL>(s_all + warp * E_r, 1, 0, p.bias, p.n_sub,
+                         p.logits_out != nullptr ? p.logits_out + row : nullptr,
+                         p.kpt != nullptr ? p.kpt[t] : p.k_max, E_r, p.k_max, p.score,
+                         p.renorm, p.route_scale, p.status, lane, sbuf + warp * 32, &my_u, &w);
+      if (lane < p.k_max) {
+        const size_t o = static_cast<size_t>(t) * p.k_max + lane;
+        p.topk_idx[o] = my_u;
+        p.topk_w[o] = w;
+      }
+      if (fused && lane < k) atomicOr(&s_bits[my_u], 1u << warp);
+    }
+    if (fused) {
+      __syncthreads();
+      // counts and exclusive offsets over the units (E_r <= 256 <= threads)
+      const int c = tid < E_r ? __popc(s_bits[tid]) : 0;
+      int incl = c;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      if (lane == 31) s_wt[warp] = incl;
+      __syncthreads();
+      int before = 0;
+      for (int w2 = 0; w2 < warp; ++w2) before += s_wt[w2];
+      if (tid < E_r) {
+        const int ex = before + incl - c;
+        s_off[tid] = ex;
+        p.offsets[tid] = ex;
+        p.counts[tid] = c;
+        if (tid == E_r - 1) {
+          s_off[E_r] = ex + c;
+          p.offsets[E_r] = ex + c;
+        }
+      }
+      __syncthreads();
+      if (warp < nt && lane < p.k_max) {
+        const int t = t0 + warp;
+        int pos = -1;
+        if (lane < k) {
+          pos = s_off[my_u] + __popc(s_bits[my_u] & ((1u << warp) - 1u));
+          p.sorted_token[pos] = t;
+          s_sorted[pos] = t;
+        }
+        p.inv_row[static_cast<size_t>(t) * p.k_max + lane] = pos;
+      }
+    }
+  }
+  if (fused) {
+    cluster_sync_all();
+    if (p.x_perm != nullptr) {
+      const int n = ld_cluster_s32(mapa_shared(smem_u32(s_off + E_r), 0u));
+      const uint32_t sorted0 = mapa_shared(smem_u32(s_sorted), 0u);
+      for (int r = static_cast<int>(rank) + p.C * warp; r < n; r += p.C * kClWarps) {
+        const int t = ld_cluster_s32(sorted0 + static_cast<uint32_t>(r * 4));
+        const uint4* src = p.x + static_cast<size_t>(t) * nv;
+        uint4* dst = p.x_perm + static_cast<size_t>(r) * nv;
+        for (int v = lane; v < nv; v += 32) dst[v] = __ldg(src + v);
+      }
+    }
+    if (rank == 0)
+      for (int i = tid; i < p.zero_n; i += kClThreads) p.zero_ptr[i] = 0;
+    cluster_sync_all();
   }
 }
 
@@ -319,6 +654,131 @@ cudaError_t launch_router_logits_small(const void* x, const void* router_w, int 
   return launch_pdl(router_logits_split_kernel, grid, dim3(256), smem, s,
                     static_cast<const uint4*>(x), static_cast<const uint4*>(router_w), T, H / 8,
                     E_r, vs, partial);
+}
+
+bool route_cluster_supports(int H, int E_r) { return H % 16 == 0 && E_r <= 256; }
+
+namespace {
+
+// Most 16-CTA clusters of the router that can be resident at once (0: the
+// device does not allow 16-CTA clusters; 8-CTA clusters are used instead).
+template <int IPL>
+cudaError_t route_clusters16(int* out) {
+  static int cached[64];
+  static bool known[64] = {false};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!known[dev]) {
+    auto kern = route_cluster_kernel<IPL>;
+    const int smem_max = static_cast<int>(kClStageBudget + 16 * 1024);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+        cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(16);
+      cfg.blockDim = dim3(kClThreads);
+      cfg.dynamicSmemBytes = smem_max;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 16;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+    }
+    (void)cudaGetLastError();
+    cached[dev] = n;
+    known[dev] = true;
+  }
+  *out = cached[dev];
+  return cudaSuccess;
+}
+
+template <int IPL>
+cudaError_t run_route_cluster(ClusterRouteParams p, cudaStream_t s) {
+  int n16 = 0;
+  cudaError_t e = route_clusters16<IPL>(&n16);
+  if (e != cudaSuccess) return e;
+  const int n_clusters = (p.T + kClTok - 1) / kClTok;
+  // 16-CTA clusters while they all fit at once, else 8-CTA clusters
+  const int C = (n16 > 0 && n_clusters <= n16) ? 16 : 8;
+  const int U = (p.E_r + C - 1) / C;
+  p.C = C;
+  p.MT = (U + 15) / 16;
+  const int rows = p.MT * 16 + kClTok;
+  const int H = p.nv * 8;
+  if (static_cast<uint32_t>(rows) * (2u * H + 16u) <= kClStageBudget) {
+    p.kc = H;
+    p.ns = 1;
+  } else {
+    int kc = 4096;
+    while (kc > 128 && 2u * rows * (2u * kc + 16u) > kClStageBudget) kc >>= 1;
+    p.kc = kc;
+    p.ns = 2;
+  }
+  const int smem = static_cast<int>(cluster_smem(p.E_r, p.MT, p.kc, p.ns).total);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C, n_clusters);
+  cfg.blockDim = dim3(kClThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, route_cluster_kernel<IPL>, p);
+}
+
+}  // namespace
+
+cudaError_t launch_route_cluster(const void* x, const void* router_w, const float* bias,
+                                 int n_sub, const int32_t* k_per_token, int T, int H, int E_r,
+                                 int k_max, int score, int renorm, float route_scale,
+                                 float* logits_out, int32_t* topk_idx, float* topk_w,
+                                 int32_t* status, const RoutePermuteOut* fuse, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  if (!route_cluster_supports(H, E_r)) return cudaErrorInvalidValue;
+  if (fuse != nullptr && T > kClTok) return cudaErrorInvalidValue;
+  ClusterRouteParams p{};
+  p.x = static_cast<const uint4*>(x);
+  p.rw = static_cast<const uint4*>(router_w);
+  p.bias = bias;
+  p.n_sub = n_sub;
+  p.kpt = k_per_token;
+  p.T = T;
+  p.nv = H / 8;
+  p.E_r = E_r;
+  p.k_max = k_max;
+  p.score = score;
+  p.renorm = renorm;
+  p.route_scale = route_scale;
+  p.logits_out = logits_out;
+  p.topk_idx = topk_idx;
+  p.topk_w = topk_w;
+  p.status = status;
+  if (fuse != nullptr) {
+    p.counts = fuse->counts;
+    p.offsets = fuse->offsets;
+    p.sorted_token = fuse->sorted_token;
+    p.inv_row = fuse->inv_row;
+    p.x_perm = static_cast<uint4*>(fuse->x_perm);
+    p.zero_ptr = fuse->zero_ptr;
+    p.zero_n = fuse->zero_ptr != nullptr ? fuse->zero_n : 0;
+  }
+  if (E_r <= 32) return run_route_cluster<1>(p, s);
+  if (E_r <= 64) return run_route_cluster<2>(p, s);
+  if (E_r <= 128) return run_route_cluster<4>(p, s);
+  return run_route_cluster<8>(p, s);
 }
 
 cudaError_t launch_topk_gate(const float* partial, int S, const float* bias, int n_sub,

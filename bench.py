@@ -471,18 +471,27 @@ def run_ours(args, wl, rank, world, local):
 
 
 def launches_per_step(wl, T, path=0):
-    """Kernels libmoe enqueues per step (mirrors the host sequencing in
-    csrc/api.cu: router + top-k, permutation, [shared expert], gate|up (+ the
+    """Kernels libmoe enqueues per moe_layer_forward (mirrors the host
+    sequencing in csrc/api.cu: router + top-k (one cluster launch on CUDA
+    cores, or the tensor-core GEMM and the top-k kernel), permutation (fused
+    into the router launch for <= 8 tokens), [shared expert], gate|up (+ the
     split-K reduction of the weight-stationary family), down (+ its split
     reduction), combine)."""
     n_cap = T * wl.k_max
     decode = path == 2 or (path == 0 and n_cap <= 64 * wl.E_r)
     budget = 256 << 20
-    n = 2                                            # logits, top-k
-    n += 1 if (T + 31) // 32 <= 8 else 3            # permutation (one CTA, or bitmap/scan/scatter)
+    tc_router = T >= 128 and wl.E_r in (64, 128, 256)
+    cluster_router = not tc_router and wl.H <= 12288
+    decode_ffn = decode and wl.H % 128 == 0 and wl.I_sub % 128 == 0
+    fused_front = cluster_router and T <= 8          # logits + top-k + permutation (+ gather)
+    if fused_front:
+        n = 1
+    else:
+        n = 1 if cluster_router else 2               # logits (+ top-k)
+        n += 1 if (T + 31) // 32 <= 8 else 3        # permutation (one CTA, or bitmap/scan/scatter)
     n += 2 if wl.I_shared else 0                     # shared expert gate|up, down
-    if decode and wl.H % 128 == 0 and wl.I_sub % 128 == 0:
-        n += 2                                       # row gather + fused decode FFN kernel
+    if decode_ffn:
+        n += 1 if fused_front else 2                 # (row gather +) fused decode FFN kernel
     else:
         n += 2                                       # row gather + gate|up GEMM
         if decode and wl.I_sub % 64 == 0:

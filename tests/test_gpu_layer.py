@@ -8,6 +8,8 @@ large prefill workloads compare a seeded sample of tokens (the oracle runs
 on that sample: tokens are independent) plus properties that hold at any
 size (routing and permutation bit-exact from generator-given logits).
 """
+from dataclasses import replace
+
 import numpy as np
 import pytest
 import torch
@@ -126,11 +128,18 @@ def test_full_size_routing_and_permutation_bit_exact(name):
 
 
 @pytest.mark.parametrize("name,T", [("tiny", None), ("qwen_decode", 64), ("qwen_decode", 256),
-                                    ("qwen_decode", 300), ("mixtral_decode", None)])
+                                    ("qwen_decode", 300), ("mixtral_decode", None),
+                                    ("qwen_decode", 1), ("qwen_decode", 8), ("mixtral_decode", 5),
+                                    ("tiny", 7), ("tiny_i192", 4)])
 def test_layer_forward_equals_component_calls(name, T):
     """moe_layer_forward gives bit-identical results to moe_route ->
-    moe_permute -> moe_grouped_ffn -> moe_combine on the same inputs."""
-    wl = WL.ALL[name] if T is None else WL.ALL[name].with_T(T)
+    moe_permute -> moe_grouped_ffn -> moe_combine on the same inputs (for
+    T <= 8 the layer runs router, permutation and row gather as one launch)."""
+    if name == "tiny_i192":   # no fused decode FFN (I_sub % 128 != 0): gate|up, down
+        wl = replace(WL.TINY, I_sub=192, name="tiny-i192")
+    else:
+        wl = WL.ALL[name]
+    wl = wl if T is None else wl.with_T(T)
     d = make_layer_inputs(wl, DEV)
     desc = B.desc_for(wl, expert_bias=d["expert_bias"])
     layer = B.MoeLayer(desc, DEV)

@@ -80,9 +80,14 @@ def test_topk_signed_zero_nan_and_k_range_flags():
 
 @pytest.mark.parametrize("T,H,n_experts,n_sub", [(64, 256, 16, 4), (64, 4096, 8, 4),
                                                  (200, 2048, 128, 1), (1024, 2048, 128, 2),
-                                                 (300, 7168, 256, 1), (5, 512, 3, 3)])
+                                                 (300, 7168, 256, 1), (5, 512, 3, 3),
+                                                 (1, 2048, 128, 2), (8, 7168, 256, 1),
+                                                 (9, 2048, 128, 2), (127, 2048, 64, 2),
+                                                 (130, 4096, 8, 4), (3, 12288, 16, 2),
+                                                 (4, 16384, 4, 2), (17, 64, 1, 1)])
 def test_router_logits_match_fp64(T, H, n_experts, n_sub):
-    """Logits from the CUDA-core path (small T) or the tensor-core GEMM."""
+    """Logits from the cluster router (CUDA cores, small T or other E_r), the
+    sliced CUDA-core kernel (H > 12288) or the tensor-core GEMM."""
     g = torch.Generator(device=DEV).manual_seed(T + H)
     E_r = n_experts * n_sub
     x = torch.randn(T, H, generator=g, device=DEV).to(torch.bfloat16)

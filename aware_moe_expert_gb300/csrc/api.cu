@@ -23,7 +23,7 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 // Byte offsets of every workspace region for one desc.
 struct Layout {
   size_t logits, router_partial, topk_idx, topk_w, counts, offsets, sorted_token, inv_row, bitmap,
-      wprefix, xperm, act, yperm, act_sh, ysh, split_word, partial, chunk_done, total;
+      wprefix, xperm, act, yperm, act_sh, ysh, split_word, partial, chunk_done, ffn_part, total;
   int router_slices;   // slices of the CUDA-core router (0: the tensor-core router runs)
   int max_split;       // K splits the decode gate|up kernel may use (1: none)
   int max_split_down;  // K splits the decode down kernel may use
@@ -38,6 +38,23 @@ constexpr int kMaxSplit = 8;
 bool router_on_tensor_cores(const moe_layer_desc& d) {
   return d.T >= 128 && moe::gemm_supports_f32_router(d.n_experts * d.n_sub);
 }
+
+inline int E_r_of(const moe_layer_desc* d) { return d->n_experts * d->n_sub; }
+
+// Decode-shaped batches (at most 64 rows per routing unit on average, from
+// the T * k_max bound) run the swap-AB kernels; desc->path forces either.
+bool use_decode_path(const moe_layer_desc* d, int n_out, bool gate_up) {
+  if (!moe::decode_gemm_supports(n_out, gate_up)) return false;
+  if (d->path == MOE_PATH_DECODE) return true;
+  if (d->path == MOE_PATH_PREFILL) return false;
+  return static_cast<long long>(d->T) * d->k_max <= 64ll * E_r_of(d);
+}
+
+bool use_decode_ffn(const moe_layer_desc* d) {
+  return use_decode_path(d, d->I_sub, true) && use_decode_path(d, d->H, false) &&
+         moe::decode_ffn_supports(d->H, d->I_sub);
+}
+inline bool decode_ffn_path(const moe_layer_desc& d) { return use_decode_ffn(&d); }
 
 Layout layout_of(const moe_layer_desc& d) {
   const size_t T = static_cast<size_t>(d.T), E_r = static_cast<size_t>(d.n_experts) * d.n_sub;
@@ -70,7 +87,10 @@ Layout layout_of(const moe_layer_desc& d) {
   l.act_sh = take(T * static_cast<size_t>(d.I_shared) * 2);
   l.ysh = take(T * static_cast<size_t>(d.H) * 2);
   l.split_word = take(16);
-  l.chunk_done = take((n_cap / 64 + E_r + 1) * 4);
+  // fused decode FFN: chunk counters, the work counter and the split
+  // counters (zeroed together), and the split partial sums
+  l.chunk_done = take((n_cap / 16 + E_r + 1 + 1 + moe::kFfnPartSlots / 2) * 4);
+  l.ffn_part = take(decode_ffn_path(d) ? static_cast<size_t>(moe::kFfnPartSlots) * 64 * 128 * 4 : 0);
   auto splits = [](size_t per_split) {
     size_t ms = per_split > 0 ? kPartialBudget / per_split : 1;
     return static_cast<int>(ms < 1 ? 1 : (ms > kMaxSplit ? kMaxSplit : ms));
@@ -149,16 +169,6 @@ inline moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK 
     if (_st != MOE_OK) return _st;         \
   } while (0)
 
-inline int E_r_of(const moe_layer_desc* d) { return d->n_experts * d->n_sub; }
-
-// Decode-shaped batches (at most 64 rows per routing unit on average, from
-// the T * k_max bound) run the swap-AB kernels; desc->path forces either.
-bool use_decode_path(const moe_layer_desc* d, int n_out, bool gate_up) {
-  if (!moe::decode_gemm_supports(n_out, gate_up)) return false;
-  if (d->path == MOE_PATH_DECODE) return true;
-  if (d->path == MOE_PATH_PREFILL) return false;
-  return static_cast<long long>(d->T) * d->k_max <= 64ll * E_r_of(d);
-}
 
 // Tokens per weight-stationary item: 64 when units hold few rows (decode),
 // else larger chunks so each weight tile is reused across more tokens.
@@ -354,15 +364,17 @@ moe_status do_down(const moe_layer_desc* d, const void* act, const int32_t* offs
 // Both FFN projections.  Decode-shaped batches with H and I_sub multiples of
 // 128 run the fused kernel (gate|up and down overlapped in one launch);
 // otherwise gate|up then down.
-bool use_decode_ffn(const moe_layer_desc* d) {
-  return use_decode_path(d, d->I_sub, true) && use_decode_path(d, d->H, false) &&
-         moe::decode_ffn_supports(d->H, d->I_sub);
+// Counters of the fused decode FFN kernel (one per 64-row chunk, the work
+// counter, the split counters), zeroed by the launch that writes x_perm.
+// Tokens per fused-decode-FFN item: 16 when no unit can hold more than 16
+// rows (T <= 16), else 64.
+inline int decode_ffn_chunk(const moe_layer_desc* d) { return d->T <= 16 ? 16 : 64; }
+inline int decode_ffn_chunks(const moe_layer_desc* d) {
+  return static_cast<int>(static_cast<long long>(d->T) * d->k_max / decode_ffn_chunk(d) +
+                          E_r_of(d) + 1);
 }
-
-// Counters of the fused decode FFN kernel (one per 64-row chunk), zeroed by
-// the launch that writes x_perm.
 inline int decode_ffn_counters(const moe_layer_desc* d) {
-  return static_cast<int>(static_cast<long long>(d->T) * d->k_max / 64 + E_r_of(d) + 1);
+  return decode_ffn_chunks(d) + 1 + moe::kFfnPartSlots / 2;
 }
 
 // pre_gathered: x_perm already holds the permuted rows and the decode FFN's
@@ -394,7 +406,11 @@ moe_status do_grouped_ffn(const moe_layer_desc* d, const void* x, const int32_t*
     a.I = d->I_sub;
     a.act = act;
     a.y = y_perm;
+    a.chunk = decode_ffn_chunk(d);
     a.done = done;
+    a.work = done + decode_ffn_chunks(d);
+    a.split_cnt = a.work + 1;
+    a.part = at<float>(ws, l.ffn_part);
     a.rows = n_cap;
     a.status = status;
     a.debug_flags = d->debug_flags;

@@ -31,25 +31,33 @@ constexpr int kBK = 64;
 constexpr int kKsub = 2;                       // 64-column sub-blocks per stage
 constexpr int kM = 128;
 constexpr int kGU = 64;                        // neurons per gate|up item
-constexpr int kChunk = 64;                     // tokens per item
 constexpr int kTokBox = 16;
 constexpr int kThreads = 192;
-constexpr int kStages = 4;
+constexpr int kQ = 4;                          // item queue depth
 constexpr uint32_t kWSub = kM * kBK * 2;        // 16 KB per weight sub-block
 constexpr uint32_t kW = kWSub * kKsub;          // 32 KB
-constexpr uint32_t kTokSub = kChunk * kBK * 2;  // 8 KB per token sub-block
-constexpr uint32_t kTok = kTokSub * kKsub;      // 16 KB
-constexpr uint32_t kStage = kW + kTok;
-constexpr uint32_t kOffB = kStages * kW;
-constexpr uint32_t kOffBar = kStages * kStage;
-constexpr uint32_t kNumBars = 2 * kStages + 5;
-constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
-constexpr uint32_t kOffPrefix = kOffMisc + 16;
-constexpr uint32_t kOffOffs = kOffPrefix + (kMaxGroups + 1) * 4;
-constexpr uint32_t kOffX = (kOffOffs + (kMaxGroups + 1) * 4 + 15) / 16 * 16;
-constexpr uint32_t kSmemBytes = kOffX + kGU * 17 * 4 + 1024;
-constexpr uint32_t kTmemCols = 128;             // 2 slots x 64 columns
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+
+// Token chunk (tokens per item: 64, or 16 for batches of at most 16 tokens,
+// whose smaller token buffers leave room for more weight stages in flight)
+// and ring depth.
+template <int CHUNK, int STAGES>
+struct FfnCfg {
+  static constexpr int kChunk = CHUNK;
+  static constexpr int kStages = STAGES;
+  static constexpr uint32_t kTokSub = CHUNK * kBK * 2;  // per token sub-block
+  static constexpr uint32_t kTok = kTokSub * kKsub;
+  static constexpr uint32_t kStage = kW + kTok;
+  static constexpr uint32_t kOffB = STAGES * kW;
+  static constexpr uint32_t kOffBar = STAGES * kStage;
+  static constexpr uint32_t kNumBars = 2 * STAGES + 5 + 2 * kQ;
+  static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr uint32_t kOffPrefix = kOffMisc + 16 + kQ * 4;
+  static constexpr uint32_t kOffOffs = kOffPrefix + (kMaxGroups + 1) * 4;
+  static constexpr uint32_t kOffX = (kOffOffs + (kMaxGroups + 1) * 4 + 15) / 16 * 16;
+  static constexpr uint32_t kSmemBytes = kOffX + kGU * 17 * 4 + 1024;
+  static constexpr uint32_t kTmemCols = 2 * CHUNK < 32 ? 32 : 2 * CHUNK;  // 2 accumulators
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
 
 struct FParams {
   const int32_t* offsets;
@@ -61,6 +69,9 @@ struct FParams {
   __nv_bfloat16* act;    // [out_rows, I]
   __nv_bfloat16* y;      // [out_rows, H]
   int32_t* done;         // [m-tiles] gate|up items finished per chunk; zero at launch
+  int32_t* work;         // next item number (dynamic schedule); zero at launch
+  int32_t* split_cnt;    // [kFfnPartSlots / 2] arrivals of split gate|up items; zero at launch
+  float* part;           // [kFfnPartSlots][kChunk][128] fp32 partial sums of split items
   long long out_rows;
   int32_t* status;
   uint32_t debug_flags;
@@ -86,21 +97,31 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// Item w of the launch: w < n_gu is a gate|up item (chunk mt, neuron block
+// m, hidden-dimension split s of S), else a down item (chunk mt, row block m).
 struct Item {
   bool gu;
-  int mt, m;
+  int mt, m, s;
 };
 
-__device__ __forceinline__ Item item_of(int w, int n_gu, int gu_tiles, int dn_tiles) {
+__device__ __forceinline__ Item item_of(int w, int n_gu, int S, int gu_tiles, int dn_tiles) {
   Item it;
   it.gu = w < n_gu;
-  const int v = it.gu ? w : w - n_gu;
-  const int per = it.gu ? gu_tiles : dn_tiles;
-  it.mt = v / per;
-  it.m = v - it.mt * per;
+  if (it.gu) {
+    const int r = w / S;
+    it.s = w - r * S;
+    it.mt = r / gu_tiles;
+    it.m = r - it.mt * gu_tiles;
+  } else {
+    const int v = w - n_gu;
+    it.s = 0;
+    it.mt = v / dn_tiles;
+    it.m = v - it.mt * dn_tiles;
+  }
   return it;
 }
 
+template <int CHUNK, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_ffn_kernel(const __grid_constant__ CUtensorMap tmWgu,
                       const __grid_constant__ CUtensorMap tmX16,
@@ -108,6 +129,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tmWdn,
                       const __grid_constant__ CUtensorMap tmA16,
                       const __grid_constant__ CUtensorMap tmA64, const FParams p) {
+  using Cfg = FfnCfg<CHUNK, STAGES>;
+  constexpr int kChunk = Cfg::kChunk;
+  constexpr int kStages = Cfg::kStages;
+  constexpr uint32_t kTokSub = Cfg::kTokSub, kTok = Cfg::kTok, kOffB = Cfg::kOffB;
+  constexpr uint32_t kOffBar = Cfg::kOffBar, kOffMisc = Cfg::kOffMisc;
+  constexpr uint32_t kOffPrefix = Cfg::kOffPrefix, kOffOffs = Cfg::kOffOffs, kOffX = Cfg::kOffX;
+  constexpr uint32_t kTmemCols = Cfg::kTmemCols;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -117,15 +145,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tfull = bars + 2 * kStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* mma_done = tempty + 2;
+  uint64_t* q_full = mma_done + 1;
+  uint64_t* q_empty = q_full + kQ;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   int* s_total = reinterpret_cast<int*>(smem + kOffMisc + 8);
+  volatile int* s_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 12);
+  volatile int* s_item = reinterpret_cast<volatile int*>(smem + kOffMisc + 16);
   int* s_prefix = reinterpret_cast<int*>(smem + kOffPrefix);
   int* s_offs = reinterpret_cast<int*>(smem + kOffOffs);
   float* s_xchg = reinterpret_cast<float*>(smem + kOffX);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  pdl_wait_and_trigger();
 
+  // set-up that reads nothing upstream overlaps the previous launch's tail
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -136,6 +168,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&tempty[0], 4);
     mbar_init(&tempty[1], 4);
     mbar_init(mma_done, 1);
+    for (int q = 0; q < kQ; ++q) {
+      mbar_init(&q_full[q], 1);
+      mbar_init(&q_empty[q], 5);   // the MMA thread and the four epilogue warps
+    }
     *s_abort = 0;
     fence_barrier_init();
   }
@@ -147,22 +183,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmA16);
     tma_prefetch_desc(&tmA64);
   }
-  if (warp == 2)
-    build_tile_table<kChunk>(p.offsets, p.n_groups, 0, p.out_rows, s_prefix, s_offs, s_total,
-                             p.status, lane);
   if (warp == 1) {
     tmem_alloc(s_tmem, kTmemCols);
     tmem_relinquish();
   }
+  pdl_wait_and_trigger();
+  if (warp == 2)
+    build_tile_table<kChunk>(p.offsets, p.n_groups, 0, p.out_rows, s_prefix, s_offs, s_total,
+                             p.status, lane);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
   const int n_mt = *s_total;
-  const int n_gu = n_mt * p.gu_tiles;
-  const int total_work = n_gu + n_mt * p.dn_tiles;
   const int KB_gu = p.H / (kBK * kKsub);
   const int KB_dn = p.I / (kBK * kKsub);
+  // Few gate|up items (small batches): split each over the hidden dimension
+  // so that more SMs stream the weights; the last split to finish adds the
+  // partial sums in split order and applies SwiGLU.
+  const int n_gu1 = n_mt * p.gu_tiles;
+  int S = 1;
+  if (KB_gu % 2 == 0 && 2 * n_gu1 <= static_cast<int>(gridDim.x) && 2 * n_gu1 <= kFfnPartSlots)
+    S = 2;
+  if (KB_gu % 4 == 0 && 4 * n_gu1 <= static_cast<int>(gridDim.x) && 4 * n_gu1 <= kFfnPartSlots)
+    S = 4;
+  const int n_gu = n_gu1 * S;
+  const int total_work = n_gu + n_mt * p.dn_tiles;
+  const int KB_split = KB_gu / S;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -170,14 +217,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0, issued = 0, issued_par = 0;
       bool skip = (p.debug_flags & MOE_DEBUG_SKIP_FIRST_LOAD) != 0u;
       bool ok = true;
-      for (int w = blockIdx.x; ok && w < total_work; w += gridDim.x) {
-        const Item it = item_of(w, n_gu, p.gu_tiles, p.dn_tiles);
+      // the first item of every CTA is its block index; later ones come
+      // from the shared counter
+      int w_next = static_cast<int>(blockIdx.x);
+      for (int i = 0; ok; ++i) {
+        const int slot = i % kQ;
+        if (!mbar_wait(&q_empty[slot], ((i / kQ) & 1) ^ 1u, s_abort)) {
+          ok = false;
+          break;
+        }
+        const int w = w_next < total_work ? w_next : -1;
+        s_item[slot] = w;
+        mbar_arrive(&q_full[slot]);
+        if (w < 0) break;
+        // the next item's number arrives while this one streams
+        w_next = static_cast<int>(gridDim.x) + atomicAdd(p.work, 1);
+        const Item it = item_of(w, n_gu, S, p.gu_tiles, p.dn_tiles);
         const Tile t = decode_tile<kChunk>(it.mt, 1, p.n_groups, s_prefix, s_offs);
         const int nb = (t.rows + kTokBox - 1) / kTokBox;
         const bool wide = nb > 2;
         const uint32_t tok_rows = wide ? 64u : static_cast<uint32_t>(nb * kTokBox);
         const uint32_t bytes = kW + kKsub * tok_rows * kBK * 2;
-        const int KB = it.gu ? KB_gu : KB_dn;
+        const int kb0 = it.gu ? it.s * KB_split : 0;
+        const int kb1 = it.gu ? kb0 + KB_split : KB_dn;
         const CUtensorMap* mW = it.gu ? &tmWgu : &tmWdn;
         const CUtensorMap* mT = it.gu ? (wide ? &tmX64 : &tmX16) : (wide ? &tmA64 : &tmA16);
         const int wrow = it.gu ? t.g * 2 * p.I + it.m * kGU : t.g * p.H + it.m * kM;
@@ -203,13 +265,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         };
-        int kb = 0;
+        int kb = kb0;
         if (!it.gu) {
           // Down item: put the first weight stages in flight, then wait until
           // every gate|up item of this token chunk has stored its act rows.
-          const int pre = KB < kStages ? KB : kStages;
+          const int pre = kb1 - kb0 < kStages ? kb1 - kb0 : kStages;
           int st0 = stage;
-          for (; kb < pre; ++kb) {
+          for (; kb < kb0 + pre; ++kb) {
             if (!mbar_wait(&empty[stage], phase ^ 1u, s_abort)) {
               ok = false;
               break;
@@ -234,13 +296,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_global();
           // the token loads of the pre-issued stages (their full barriers
           // already expect these bytes)
-          for (int i = 0; i < pre; ++i) {
-            const int s = (st0 + i) % kStages;
-            tokens(smem + kOffB + s * kTok, &full[s], i);
+          for (int i2 = 0; i2 < pre; ++i2) {
+            const int s = (st0 + i2) % kStages;
+            tokens(smem + kOffB + s * kTok, &full[s], kb0 + i2);
           }
           if (!ok) break;
         }
-        for (; kb < KB; ++kb) {
+        for (; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, s_abort)) {
             ok = false;
             break;
@@ -270,12 +332,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, aphase = 0;
       bool ok = true;
-      for (int w = blockIdx.x; ok && w < total_work; w += gridDim.x) {
-        const Item it = item_of(w, n_gu, p.gu_tiles, p.dn_tiles);
+      for (int i = 0; ok; ++i) {
+        const int slot = i % kQ;
+        if (!mbar_wait(&q_full[slot], (i / kQ) & 1, s_abort)) {
+          ok = false;
+          break;
+        }
+        const int w = s_item[slot];
+        mbar_arrive(&q_empty[slot]);
+        if (w < 0) break;
+        const Item it = item_of(w, n_gu, S, p.gu_tiles, p.dn_tiles);
         const Tile t = decode_tile<kChunk>(it.mt, 1, p.n_groups, s_prefix, s_offs);
         const int n = ((t.rows + 15) / 16) * 16;
         const uint32_t idesc = idesc_bf16_f32(kM, n);
-        const int KB = it.gu ? KB_gu : KB_dn;
+        const int KB = it.gu ? KB_split : KB_dn;
         if (!mbar_wait(&tempty[acc], aphase ^ 1u, s_abort)) {
           ok = false;
           break;
@@ -319,10 +389,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r_in = q * 32 + lane;
     int acc = 0;
     uint32_t aphase = 0;
-    for (int w = blockIdx.x; w < total_work; w += gridDim.x) {
-      const Item it = item_of(w, n_gu, p.gu_tiles, p.dn_tiles);
-      const Tile t = decode_tile<kChunk>(it.mt, 1, p.n_groups, s_prefix, s_offs);
+    for (int i = 0;; ++i) {
+      const int slot = i % kQ;
       int ok = 1;
+      if (lane == 0) ok = mbar_wait(&q_full[slot], (i / kQ) & 1, s_abort) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) fail(s_abort, p.status);
+        break;
+      }
+      int w = 0;
+      if (lane == 0) {
+        w = s_item[slot];
+        mbar_arrive(&q_empty[slot]);
+      }
+      w = __shfl_sync(0xffffffffu, w, 0);
+      if (w < 0) break;
+      const Item it = item_of(w, n_gu, S, p.gu_tiles, p.dn_tiles);
+      const Tile t = decode_tile<kChunk>(it.mt, 1, p.n_groups, s_prefix, s_offs);
       if (lane == 0) ok = mbar_wait(&tfull[acc], aphase, s_abort) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) {
@@ -332,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                           static_cast<uint32_t>(acc * kChunk);
-      if (it.gu) {
+      if (it.gu && S == 1) {
         const bool is_gate = q < 2;
         const int nl = (q & 1) * 32 + lane;
         const int col = it.m * kGU + nl;
@@ -361,6 +445,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         __threadfence();
         asm volatile("bar.sync 1, 128;" ::: "memory");
         if (warp == 2 && lane == 0) atomicAdd(p.done + it.mt, 1);
+      } else if (it.gu) {
+        // split item: fp32 partial [token][row] to this split's slot; the
+        // last split of the item to arrive finishes it
+        const int item = it.mt * p.gu_tiles + it.m;
+        float* mine = p.part + static_cast<size_t>(item * S + it.s) * (kChunk * kM);
+        for (int c0 = 0; c0 < t.rows; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(tb + c0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int cc = 0; cc < 16; ++cc)
+            if (c0 + cc < t.rows) mine[(c0 + cc) * kM + r_in] = __uint_as_float(v[cc]);
+        }
+        __threadfence();
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (warp == 2 && lane == 0) *s_flag = atomicAdd(p.split_cnt + item, 1);
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (*s_flag == S - 1) {
+          __threadfence();
+          if (q < 2) {
+            const float* base = p.part + static_cast<size_t>(item * S) * (kChunk * kM);
+            const int col = it.m * kGU + r_in;
+            for (int c = 0; c < t.rows; ++c) {
+              float g = 0.f, u = 0.f;
+              for (int s2 = 0; s2 < S; ++s2) {
+                g += __ldcg(base + static_cast<size_t>(s2) * (kChunk * kM) + c * kM + r_in);
+                u += __ldcg(base + static_cast<size_t>(s2) * (kChunk * kM) + c * kM + kGU + r_in);
+              }
+              const long long r = static_cast<long long>(t.row0) + c;
+              if (r < p.out_rows) p.act[r * p.I + col] = __float2bfloat16_rn(silu_f(g) * u);
+            }
+          }
+          fence_proxy_async_global();
+          __threadfence();
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+          if (warp == 2 && lane == 0) atomicAdd(p.done + it.mt, 1);
+        }
       } else {
         const int col = it.m * kM + r_in;
         for (int c0 = 0; c0 < t.rows; c0 += 16) {
@@ -418,14 +539,28 @@ cudaError_t launch_decode_ffn(const DecodeFfnArgs& a, cudaStream_t s) {
   p.act = static_cast<__nv_bfloat16*>(a.act);
   p.y = static_cast<__nv_bfloat16*>(a.y);
   p.done = a.done;
+  p.work = a.work;
+  p.split_cnt = a.split_cnt;
+  p.part = a.part;
   p.out_rows = a.rows;
   p.status = a.status;
   p.debug_flags = a.debug_flags;
+  if (a.chunk == 16) {
+    using Cfg = FfnCfg<16, 6>;
+    static bool attr_done[64] = {false};
+    cudaError_t e = set_smem_once(decode_ffn_kernel<16, 6>, static_cast<int>(Cfg::kSmemBytes),
+                                  attr_done);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(decode_ffn_kernel<16, 6>, dim3(a.sm_count), dim3(kThreads),
+                      Cfg::kSmemBytes, s, wgu, x16, x64, wdn, a16, a64, p);
+  }
+  using Cfg = FfnCfg<64, 4>;
   static bool attr_done[64] = {false};
-  cudaError_t e = set_smem_once(decode_ffn_kernel, static_cast<int>(kSmemBytes), attr_done);
+  cudaError_t e = set_smem_once(decode_ffn_kernel<64, 4>, static_cast<int>(Cfg::kSmemBytes),
+                                attr_done);
   if (e != cudaSuccess) return e;
-  return launch_pdl(decode_ffn_kernel, dim3(a.sm_count), dim3(kThreads), kSmemBytes, s, wgu, x16,
-                    x64, wdn, a16, a64, p);
+  return launch_pdl(decode_ffn_kernel<64, 4>, dim3(a.sm_count), dim3(kThreads), Cfg::kSmemBytes,
+                    s, wgu, x16, x64, wdn, a16, a64, p);
 }
 
 }  // namespace moe

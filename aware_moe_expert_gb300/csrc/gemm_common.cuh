@@ -78,6 +78,21 @@ __device__ __forceinline__ void build_tile_table(const int32_t* offsets, int G, 
     }
     return;
   }
+  // every offset in flight at once (lane-strided), then per-lane runs from
+  // shared memory
+  constexpr int kPer = (kMaxGroups + 1 + 31) / 32;
+  int ov[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int g = lane + 32 * i;
+    ov[i] = g <= G ? offsets[g] : 0;
+  }
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int g = lane + 32 * i;
+    if (g <= G) s_offs[g] = ov[i];
+  }
+  __syncwarp();
   const int per = (G + 31) / 32;
   const int g0 = lane * per;
   int local = 0;
@@ -85,9 +100,8 @@ __device__ __forceinline__ void build_tile_table(const int32_t* offsets, int G, 
   for (int i = 0; i < per; ++i) {
     const int g = g0 + i;
     if (g < G) {
-      const int a = offsets[g], b = offsets[g + 1];
+      const int a = s_offs[g], b = s_offs[g + 1];
       bad |= (a < 0) || (b < a);
-      s_offs[g] = a;
       local += b > a ? (b - a + TR - 1) / TR : 0;
     }
   }
@@ -102,14 +116,13 @@ __device__ __forceinline__ void build_tile_table(const int32_t* offsets, int G, 
     const int g = g0 + i;
     if (g < G) {
       s_prefix[g] = run;
-      const int a = offsets[g], b = offsets[g + 1];
+      const int a = s_offs[g], b = s_offs[g + 1];
       run += b > a ? (b - a + TR - 1) / TR : 0;
     }
   }
   if (lane == 31) {
-    const int last = offsets[G];
+    const int last = s_offs[G];
     bad |= static_cast<long long>(last) > out_rows;
-    s_offs[G] = last;
     s_prefix[G] = incl;
   }
   bad = __any_sync(0xffffffffu, bad);

@@ -150,7 +150,11 @@ struct DecodeFfnArgs {
   int I;
   void* act;                 // bf16 [rows, I] (scratch)
   void* y;                   // bf16 [rows, H]
-  int32_t* done;             // per 64-row chunk counters, zero before the launch
+  int chunk;                 // tokens per item: 64, or 16 when T <= 16
+  int32_t* done;             // per token-chunk counters, zero before the launch
+  int32_t* work;             // dynamic-schedule counter, zero before the launch
+  int32_t* split_cnt;        // [kFfnPartSlots / 2] split arrivals, zero before the launch
+  float* part;               // [kFfnPartSlots][chunk][128] fp32 (split gate|up partial sums)
   long long rows;
   int32_t* status;
   uint32_t debug_flags;
@@ -158,6 +162,7 @@ struct DecodeFfnArgs {
 };
 
 cudaError_t launch_decode_ffn(const DecodeFfnArgs& a, cudaStream_t s);
+constexpr int kFfnPartSlots = 256;
 bool decode_ffn_supports(int H, int I_sub);
 
 // bf16 [rows, cols] row-major tensor map: box of 64 columns x box_rows rows,

@@ -71,6 +71,10 @@ Layout layout_of(const moe_layer_desc& d) {
   if (!router_on_tensor_cores(d)) {
     int vs = 0;
     l.router_slices = moe::router_slices(d.T, d.H, static_cast<int>(E_r), &vs);
+  } else {
+    int bn = 0, S = 1;
+    moe::router_gemm_shape(d.T, d.H, static_cast<int>(E_r), &bn, &S);
+    l.router_slices = S > 1 ? S : 0;
   }
   l.router_partial = take(static_cast<size_t>(l.router_slices) * T * E_r * 4);
   l.topk_idx = take(n_cap * 4);
@@ -181,8 +185,10 @@ int decode_chunk(const moe_layer_desc* d) {
 // Router logits into dst: tcgen05 GEMM for T >= 128 with E_r in {64,128,256},
 // else the CUDA-core kernel.
 // Finished logits (with bias) into dst on the tensor cores.
+// splits > 1: the K-split partial sums go to dst + s * T * E_r (no bias).
 moe_status do_logits_gemm(const moe_layer_desc* d, const void* x, const void* router_w,
-                          float* dst, int32_t* status, cudaStream_t s) {
+                          float* dst, int32_t* status, cudaStream_t s, int splits = 1,
+                          int bn = 0) {
   const int E_r = E_r_of(d);
   GemmArgs g{};
   g.epi = moe::EPI_F32;
@@ -207,7 +213,9 @@ moe_status do_logits_gemm(const moe_layer_desc* d, const void* x, const void* ro
   g.max_rows_hint = d->T;
   // small batches: 64-column tiles for more CTAs; large ones: one n-tile,
   // so x is read once
-  g.bn_hint = d->T < 4096 ? 64 : 0;
+  g.bn_hint = bn > 0 ? bn : (d->T < 4096 ? 64 : 0);
+  g.k_splits = splits;
+  g.split_stride = static_cast<long long>(d->T) * E_r;
   return cuda_status(moe::launch_gemm(g, s));
 }
 
@@ -223,9 +231,21 @@ moe_status do_route(const moe_layer_desc* d, const void* x, const void* router_w
   float* lout = nullptr;
   if (P == nullptr) {
     if (router_on_tensor_cores(*d)) {
-      float* dst = logits_out != nullptr ? logits_out : at<float>(ws, l.logits);
-      MOE_TRY(do_logits_gemm(d, x, router_w, dst, status, s));
-      P = dst;
+      int bn = 0, splits = 1;
+      moe::router_gemm_shape(d->T, d->H, E_r, &bn, &splits);
+      if (splits > 1) {
+        // K-split partial sums; the top-k kernel adds them in order, then the bias
+        float* part = at<float>(ws, l.router_partial);
+        MOE_TRY(do_logits_gemm(d, x, router_w, part, status, s, splits, bn));
+        P = part;
+        S = splits;
+        bias = d->expert_bias;
+        lout = logits_out;
+      } else {
+        float* dst = logits_out != nullptr ? logits_out : at<float>(ws, l.logits);
+        MOE_TRY(do_logits_gemm(d, x, router_w, dst, status, s, 1, bn));
+        P = dst;
+      }
     } else if (moe::route_cluster_supports(d->H, E_r)) {
       return cuda_status(moe::launch_route_cluster(
           x, router_w, d->expert_bias, d->n_sub, kpt, d->T, d->H, E_r, d->k_max, d->score,
@@ -615,11 +635,8 @@ moe_status moe_route(const moe_layer_desc* desc, const void* x, const void* rout
     MOE_TRY(check_ptrs4({logits_in}));
   } else {
     MOE_TRY(check_ptrs({x, router_w}));
-    if (logits_out != nullptr) {
-      MOE_TRY(check_ptrs({logits_out}));
-    } else {
-      MOE_TRY(check_ws(workspace));
-    }
+    if (logits_out != nullptr) MOE_TRY(check_ptrs({logits_out}));
+    MOE_TRY(check_ws(workspace));
   }
   return do_route(desc, x, router_w, logits_in, k_per_token, logits_out, topk_idx, topk_w,
                   dev_status, workspace, static_cast<cudaStream_t>(stream));

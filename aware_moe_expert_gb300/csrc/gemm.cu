@@ -60,6 +60,8 @@ struct KParams {
   long long ld_out;
   long long out_rows;
   int out_cols;      // EPI_F32: valid output columns
+  int k_splits;      // EPI_F32: the hidden dimension split S ways, partial sums to
+  long long split_stride;  // out + s * split_stride (elements); 1: no split
   const float* bias;
   int bias_div;
   int32_t* status;
@@ -141,8 +143,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
-  const int total_work = *s_total * p.n_tiles;
-  const int KB = p.K / BK;
+  // EPI_F32 may split K: n-tile index nt * S + s, split s covers k-blocks
+  // [s * KB / S, (s + 1) * KB / S)
+  const int S = EPI == EPI_F32 ? p.k_splits : 1;
+  const int n_tiles_eff = p.n_tiles * S;
+  const int total_work = *s_total * n_tiles_eff;
+  const int KB = p.K / BK / S;
   const int G = p.offsets == nullptr ? 1 : p.n_groups;
 
   if (warp == 0) {
@@ -153,9 +159,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool skip = (p.debug_flags & MOE_DEBUG_SKIP_FIRST_LOAD) != 0u;
       bool ok = true;
       for (int w = blockIdx.x; ok && w < total_work; w += gridDim.x) {
-        const Tile t = decode_tile(w, p.n_tiles, G, s_prefix, s_offs);
-        const int b_row = t.g * p.b_group_rows + t.nt * p.bn_out;
-        for (int kb = 0; kb < KB; ++kb) {
+        const Tile t = decode_tile(w, n_tiles_eff, G, s_prefix, s_offs);
+        const int split = t.nt % S, nt = t.nt / S;
+        const int b_row = t.g * p.b_group_rows + nt * p.bn_out;
+        for (int kb = split * KB; kb < (split + 1) * KB; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, s_abort)) {
             ok = false;
             break;
@@ -212,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t bd = sdesc_sw128(smem_u32(smem + C::kOffB + stage * C::kBBytes));
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            umma_bf16(d, ad + 2u * k, bd + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
+            umma_bf16(d, ad + 2u * k, bd + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);  // kb from 0
           umma_commit(&empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
@@ -239,7 +246,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t aphase = 0;
     for (int w = blockIdx.x; w < total_work; w += gridDim.x) {
-      const Tile t = decode_tile(w, p.n_tiles, G, s_prefix, s_offs);
+      Tile t = decode_tile(w, n_tiles_eff, G, s_prefix, s_offs);
+      const int split = t.nt % S;
+      t.nt /= S;
       int ok = 1;
       if (lane == 0) ok = mbar_wait(&tfull[acc], aphase, s_abort) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -305,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         const int col0 = t.nt * p.bn_out;
-        float* orow = static_cast<float*>(p.out) + grow * p.ld_out + col0;
+        float* orow = static_cast<float*>(p.out) + split * p.split_stride + grow * p.ld_out + col0;
 #pragma unroll 1
         for (int c = 0; c < BN_MMA; c += 32) {
           uint32_t v[32];
@@ -381,7 +390,10 @@ cudaError_t run_gemm(const GemmArgs& g, cudaStream_t s) {
   kp.ld_out = g.ld_out;
   kp.out_rows = g.out_rows;
   kp.out_cols = g.n_out;
-  kp.bias = g.bias;
+  kp.k_splits = EPI == EPI_F32 && g.k_splits > 1 ? g.k_splits : 1;
+  kp.split_stride = g.split_stride;
+  if (g.K % (BK * kp.k_splits) != 0) return cudaErrorInvalidValue;
+  kp.bias = kp.k_splits > 1 ? nullptr : g.bias;
   kp.bias_div = g.bias_div > 0 ? g.bias_div : 1;
   kp.status = g.status;
   kp.debug_flags = g.debug_flags;
@@ -390,7 +402,7 @@ cudaError_t run_gemm(const GemmArgs& g, cudaStream_t s) {
     m_tiles = (g.dense_rows + BM - 1) / BM;
   else
     m_tiles = (g.max_rows_hint + BM - 1) / BM + g.n_groups;
-  const long long work = m_tiles * kp.n_tiles;
+  const long long work = m_tiles * kp.n_tiles * kp.k_splits;
   if (work <= 0) return cudaSuccess;
   const int grid = static_cast<int>(work < g.sm_count ? work : g.sm_count);
   auto kern = grouped_gemm_kernel<BN_MMA, EPI, STAGES>;
@@ -434,6 +446,15 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, long long rows, int cols, 
 }
 
 bool gemm_supports_f32_router(int E_r) { return E_r == 64 || E_r == 128 || E_r == 256; }
+
+void router_gemm_shape(int T, int H, int E_r, int* bn, int* splits) {
+  *bn = T < 4096 ? 64 : E_r;
+  const long long base = static_cast<long long>((T + BM - 1) / BM) * (E_r / *bn);
+  const int KB = H / BK;
+  int S = 1;
+  while (S < 8 && base * S * 2 <= 128 && KB % (S * 2) == 0) S *= 2;
+  *splits = S;
+}
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s) {
   // CTA pairs stage a third fewer bytes per SM and k-block (12-17% less time

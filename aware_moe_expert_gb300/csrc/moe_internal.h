@@ -103,6 +103,8 @@ struct GemmArgs {
   int sm_count;
   int max_rows_hint;         // upper bound of total rows (grid sizing)
   int bn_hint;               // EPI_F32: output columns per tile (64/128/256), 0 = all
+  int k_splits;              // EPI_F32: K split S ways (S divides K / 64); partial sums of
+  long long split_stride;    //   split s at out + s * split_stride, no bias; 0/1 = no split
   bool force_pair;           // grouped SWIGLU/BF16: use the CTA-pair kernel
 };
 
@@ -169,5 +171,10 @@ bool decode_ffn_supports(int H, int I_sub);
 // 128-byte swizzle, zero fill out of bounds.
 bool make_tmap_bf16(CUtensorMap* m, const void* base, long long rows, int cols, int box_rows);
 bool gemm_supports_f32_router(int E_r);
+// Output columns per tile and K splits of the tensor-core router GEMM for T
+// tokens: small batches take 64-column tiles, and K is split until about 128
+// tiles exist (the split partial sums go to a workspace and the top-k kernel
+// adds them in order).
+void router_gemm_shape(int T, int H, int E_r, int* bn, int* splits);
 
 }  // namespace moe

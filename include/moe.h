@@ -104,7 +104,9 @@ size_t moe_workspace_size(const moe_layer_desc* desc);
  *   topk_w       fp32 [T, k_max]: gate weight of each selected unit, 0 after k_t.
  *                softmax: exp(L_u - max L) / sum over ALL units; sigmoid:
  *                1/(1+exp(-L_u)); renorm divides by the selected sum; then
- *                times route_scale. */
+ *                times route_scale.
+ *   workspace    moe_workspace_size(desc) bytes; unused (may be null) when
+ *                logits_in is given. */
 moe_status moe_route(const moe_layer_desc* desc, const void* x, const void* router_w,
                      const float* logits_in, const int32_t* k_per_token, float* logits_out,
                      int32_t* topk_idx, float* topk_w, int32_t* dev_status, void* workspace,

@@ -282,10 +282,15 @@ moe_status do_gate_up(const moe_layer_desc* d, const void* x, const int32_t* sor
   const long long n_cap = static_cast<long long>(d->T) * d->k_max;
   if (n_cap == 0) return MOE_OK;
   void* xperm = at<void>(ws, l.xperm);
-  MOE_TRY(cuda_status(moe::launch_gather_rows(x, sorted_token, offsets, E_r, d->T, d->H,
-                                              static_cast<int>(n_cap), xperm, status,
-                                              sm_count(), s)));
-  if (use_decode_path(d, d->I_sub, true)) {
+  const bool decode = use_decode_path(d, d->I_sub, true);
+  const bool pair = (d->debug_flags & MOE_DEBUG_FORCE_PAIR) != 0u;
+  // the single-CTA prefill kernel gathers its A rows itself; the other
+  // kernels read the permuted copy
+  if (decode || pair)
+    MOE_TRY(cuda_status(moe::launch_gather_rows(x, sorted_token, offsets, E_r, d->T, d->H,
+                                                static_cast<int>(n_cap), xperm, status,
+                                                sm_count(), s)));
+  if (decode) {
     moe::DecodeGemmArgs a{};
     a.gate_up = true;
     a.w = w_gate_up;
@@ -324,7 +329,12 @@ moe_status do_gate_up(const moe_layer_desc* d, const void* x, const int32_t* sor
   g.out_rows = n_cap;
   g.status = status;
   g.debug_flags = d->debug_flags;
-  g.force_pair = (d->debug_flags & MOE_DEBUG_FORCE_PAIR) != 0u;
+  g.force_pair = pair;
+  if (!pair) {
+    g.gather_x = x;
+    g.gather_tok = sorted_token;
+    g.gather_rows = d->T;
+  }
   g.sm_count = sm_count();
   g.max_rows_hint = static_cast<int>(n_cap);
   return cuda_status(moe::launch_gemm(g, s));

@@ -45,6 +45,7 @@ namespace {
 constexpr int BM = kTileRows;
 constexpr int BK = 64;
 constexpr int kThreads = 192;
+constexpr int kGatherThreads = 128;   // warps 6..9 of the row-gathering variant
 constexpr uint32_t kABytes = BM * BK * 2;
 
 struct KParams {
@@ -60,6 +61,9 @@ struct KParams {
   long long ld_out;
   long long out_rows;
   int out_cols;      // EPI_F32: valid output columns
+  const uint4* gx;           // GATHER: A rows are x[gtok[r]] (bf16 [*, K]), 16-byte vectors
+  const int32_t* gtok;       // GATHER: token of every permuted row
+  int gx_rows;               // GATHER: rows of x (tokens outside are reported and skipped)
   int k_splits;      // EPI_F32: the hidden dimension split S ways, partial sums to
   long long split_stride;  // out + s * split_stride (elements); 1: no split
   const float* bias;
@@ -91,8 +95,12 @@ struct Cfg {
   static_assert(BN_MMA % 16 == 0 && BN_MMA >= 16 && BN_MMA <= 256, "tcgen05 N for M = 128");
 };
 
-template <int BN_MMA, int EPI, int STAGES>
-__global__ void __launch_bounds__(kThreads, 1)
+// GATHER: four more warps copy the A rows of every k-block straight from x
+// (row r of the tile is token gtok[row0 + r]) into the swizzled A stage with
+// cp.async, so no permuted copy of x is materialised; the producer then loads
+// only B.
+template <int BN_MMA, int EPI, int STAGES, bool GATHER = false>
+__global__ void __launch_bounds__(GATHER ? kThreads + kGatherThreads : kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmOut, const KParams p) {
@@ -117,7 +125,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
+      // GATHER: the producer's arrive (B bytes) plus one cp.async arrive per gather thread
+      mbar_init(&full[s], GATHER ? 1 + kGatherThreads : 1);
       mbar_init(&empty[s], 1);
     }
     mbar_init(&tfull[0], 1);
@@ -129,7 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmA);
+    if (!GATHER) tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     if (EPI != EPI_F32) tma_prefetch_desc(&tmOut);
   }
@@ -172,8 +181,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             uint8_t* sa = smem + C::kOffA + stage * kABytes;
             uint8_t* sb = smem + C::kOffB + stage * C::kBBytes;
-            mbar_expect_tx(&full[stage], C::kStageBytes);
-            tma_load_2d(sa, &tmA, &full[stage], kb * BK, t.row0);
+            mbar_expect_tx(&full[stage], GATHER ? C::kBBytes : C::kStageBytes);
+            if (!GATHER) tma_load_2d(sa, &tmA, &full[stage], kb * BK, t.row0);
             if (EPI == EPI_SWIGLU) {
               tma_load_2d(sb, &tmB, &full[stage], kb * BK, b_row);
               tma_load_2d(sb + (BN_MMA / 2) * BK * 2, &tmB, &full[stage], kb * BK,
@@ -239,6 +248,76 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(done, 0u, nullptr);
     }
     __syncwarp();
+  } else if (GATHER && warp >= 6) {
+    // A-row gather: thread g copies 16-byte chunk (g % 8) of rows g / 8 + 16 i
+    // (i < 8) of every k-block; the chunk lands at chunk ^ (row % 8) of its
+    // 128-byte row (the 128-byte swizzle the MMA descriptors expect).  The
+    // copies of a stage are one cp.async group; once a group is LAG groups
+    // old the thread waits for it, orders it for the tensor cores' async-proxy
+    // reads (fence.proxy.async) and arrives on that stage's `full` barrier.
+    // LAG = STAGES - 2 keeps that arrival independent of the MMA's progress on
+    // the stage just before, so the tensor pipe is never held by it.
+    constexpr int LAG = STAGES - 2;
+    const int g = threadIdx.x - kThreads;
+    const int chunk = g & 7, rg = g >> 3;
+    const uint32_t dst_off = static_cast<uint32_t>(rg * 128 + ((chunk ^ (rg & 7)) << 4));
+    const size_t nv = static_cast<size_t>(p.K) / 8;
+    int stage = 0, astage = 0, pending = 0;
+    uint32_t phase = 0;
+    bool ok = true, bad = false;
+    for (int w = blockIdx.x; ok && w < total_work; w += gridDim.x) {
+      const Tile t = decode_tile(w, n_tiles_eff, G, s_prefix, s_offs);
+      const uint4* src[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = rg + 16 * i;
+        int tok = -1;
+        if (r < t.rows) {
+          tok = __ldg(p.gtok + t.row0 + r);
+          if (tok < 0 || tok >= p.gx_rows) {
+            bad = true;
+            tok = -1;
+          }
+        }
+        src[i] = tok >= 0 ? p.gx + static_cast<size_t>(tok) * nv + chunk : nullptr;
+      }
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!mbar_wait(&empty[stage], phase ^ 1u, s_abort)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sa = smem_u32(smem + C::kOffA + stage * kABytes) + dst_off;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (src[i] != nullptr)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa + i * 16 * 128),
+                         "l"(src[i] + kb * (BK / 8))
+                         : "memory");
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        if (++pending > LAG) {
+          asm volatile("cp.async.wait_group %0;" ::"n"(LAG) : "memory");
+          fence_proxy_async_smem();
+          mbar_arrive(&full[astage]);
+          if (++astage == STAGES) astage = 0;
+          --pending;
+        }
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    if (ok) {
+      fence_proxy_async_smem();
+      for (; pending > 0; --pending) {
+        mbar_arrive(&full[astage]);
+        if (++astage == STAGES) astage = 0;
+      }
+    } else {
+      fail(s_abort, p.status);
+    }
+    if (bad) report(p.status, MOE_ERR_BAD_INDEX);
   } else {
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     const int r_in = q * 32 + lane;
@@ -366,12 +445,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- host side
 
-template <int BN_MMA, int EPI, int STAGES>
+template <int BN_MMA, int EPI, int STAGES, bool GATHER = false>
 cudaError_t run_gemm(const GemmArgs& g, cudaStream_t s) {
   using C = Cfg<BN_MMA, STAGES>;
   const int box_b = EPI == EPI_SWIGLU ? BN_MMA / 2 : BN_MMA;  // output columns per n-tile
   CUtensorMap ta, tb, to;
-  if (!make_tmap_bf16(&ta, g.a, g.a_rows, g.K, BM)) return cudaErrorInvalidValue;
+  if (GATHER) {
+    if (g.gather_x == nullptr || g.gather_tok == nullptr) return cudaErrorInvalidValue;
+    if (!make_tmap_bf16(&ta, g.gather_x, 1, g.K, 1)) return cudaErrorInvalidValue;  // unused
+  } else if (!make_tmap_bf16(&ta, g.a, g.a_rows, g.K, BM)) {
+    return cudaErrorInvalidValue;
+  }
   if (!make_tmap_bf16(&tb, g.b, g.b_rows, g.K, box_b)) return cudaErrorInvalidValue;
   if (EPI == EPI_F32)
     to = tb;  // unused
@@ -390,6 +474,9 @@ cudaError_t run_gemm(const GemmArgs& g, cudaStream_t s) {
   kp.ld_out = g.ld_out;
   kp.out_rows = g.out_rows;
   kp.out_cols = g.n_out;
+  kp.gx = static_cast<const uint4*>(g.gather_x);
+  kp.gtok = g.gather_tok;
+  kp.gx_rows = g.gather_rows;
   kp.k_splits = EPI == EPI_F32 && g.k_splits > 1 ? g.k_splits : 1;
   kp.split_stride = g.split_stride;
   if (g.K % (BK * kp.k_splits) != 0) return cudaErrorInvalidValue;
@@ -405,13 +492,14 @@ cudaError_t run_gemm(const GemmArgs& g, cudaStream_t s) {
   const long long work = m_tiles * kp.n_tiles * kp.k_splits;
   if (work <= 0) return cudaSuccess;
   const int grid = static_cast<int>(work < g.sm_count ? work : g.sm_count);
-  auto kern = grouped_gemm_kernel<BN_MMA, EPI, STAGES>;
+  auto kern = grouped_gemm_kernel<BN_MMA, EPI, STAGES, GATHER>;
   // The shared-memory opt-in is set once per device, so that launches made
   // while a stream is being captured into a CUDA graph issue no other call.
   static bool attr_done[64] = {false};
   cudaError_t e = set_smem_once(kern, static_cast<int>(C::kSmemBytes), attr_done);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(grid), dim3(kThreads), C::kSmemBytes, s, ta, tb, to, kp);
+  return launch_pdl(kern, dim3(grid), dim3(GATHER ? kThreads + kGatherThreads : kThreads),
+                    C::kSmemBytes, s, ta, tb, to, kp);
 }
 
 }  // namespace
@@ -472,6 +560,10 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s) {
   }
   switch (g.epi) {
     case EPI_SWIGLU:
+      if (g.gather_x != nullptr) {
+        if (g.n_out % 128 == 0) return run_gemm<256, EPI_SWIGLU, 4, true>(g, s);
+        return run_gemm<128, EPI_SWIGLU, 6, true>(g, s);
+      }
       if (g.n_out % 128 == 0) return run_gemm<256, EPI_SWIGLU, 4>(g, s);
       return run_gemm<128, EPI_SWIGLU, 6>(g, s);
     case EPI_BF16:

@@ -106,6 +106,9 @@ struct GemmArgs {
   int k_splits;              // EPI_F32: K split S ways (S divides K / 64); partial sums of
   long long split_stride;    //   split s at out + s * split_stride, no bias; 0/1 = no split
   bool force_pair;           // grouped SWIGLU/BF16: use the CTA-pair kernel
+  const void* gather_x;      // grouped SWIGLU, single-CTA kernel: A row r is
+  const int32_t* gather_tok; //   gather_x[gather_tok[r]] (no permuted copy); nullptr: A
+  int gather_rows;           //   rows of gather_x
 };
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s);

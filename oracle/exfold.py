@@ -1,0 +1,151 @@
+"""Plain CPU oracle of decode expert-pool folding (routing-metadata rewrite).
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path may import this module:
+only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py`` (its CPU baseline
+and its ``--impl reference`` arm) call it.  It shares no code with the CUDA
+library and imports nothing from it.
+
+Source: "ExFold: Unified Expert Folding for Training-Free MoE Prefill-Decode
+Acceleration" (arXiv 2608.24938), sections "Unified Expert Folding",
+"Phase-Specific Selection and Unified Folding" and "Phase-Specific Routing and
+Folding" (pp. 4, 12-13).  Decode cost follows the distinct experts a batch
+activates; ExFold bounds that set to a pool of D experts and folds every route
+to an expert outside the pool into a retained target: the excluded
+contribution alpha_e E_e(x) is approximated by alpha_e S[e, tau] E_tau(x), the
+target tau being the pool member with the smallest calibrated projection loss
+L[e, tau], so the scalar only changes the target's router weight.  Routes of a
+token that land on the same target are coalesced, so each retained target runs
+once per token.  The pool is either dynamic (ranked by the batch's aggregate
+routed contribution) or static (fixed in advance).
+
+What it computes (the plainest reading; every choice is also a test pin or a
+listed reading):
+
+  1. pool (dynamic): score_u = h_u * sum of the routed weights of unit u over
+     the batch; the D best units by score (larger first, lower index on ties)
+     form the pool; units nobody routes to (score 0 is never positive) join
+     only if fewer than D units carry weight, again by lower index.
+     The sum is formed in fp32 in a fixed order: tokens in blocks of 64, each
+     block summed token by token and slot by slot, the block sums added in
+     block order (the order the GPU uses; fp32 because the sum decides an
+     integer, the pool).
+  2. target map: tau(u) = u for a pool member; otherwise the pool member p with
+     the smallest L[u, p] (lower index on ties), with scale S[u, tau(u)].
+  3. remap: route (t, j) of unit u and weight w becomes (tau(u), w * S[u, tau])
+     (fp32 product); a pool member keeps its weight unchanged.
+  4. coalesce: per token, routes with the same target are merged in slot order
+     (fp32 sum in slot order) at the position of their first occurrence; the
+     token's new budget is the number of distinct targets.
+
+Readings (where the page is silent): the pages' experts are this layer's
+routing units (sub-experts when the experts are split); the per-unit
+magnitude h (the page ranks by router score times output magnitude) defaults
+to 1; S and L are calibration tables the caller supplies (synthetic here:
+calibration data are out of scope).
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import numpy as np
+
+SCORE_BLOCK = 64   # tokens per fp32 partial sum of the pool score
+
+
+def pool_scores(topk_idx: np.ndarray, topk_w: np.ndarray, k_per_token, E_r: int,
+                unit_scale: Optional[np.ndarray] = None) -> np.ndarray:
+    """fp32 aggregate routed weight per unit, times h_u (step 1's score).
+
+    Order: tokens in blocks of SCORE_BLOCK, inside a block token by token and
+    slot by slot; block sums added in block order; then the product with h_u.
+    """
+    T = topk_idx.shape[0]
+    total = np.zeros(E_r, dtype=np.float32)
+    for b0 in range(0, T, SCORE_BLOCK):
+        part = np.zeros(E_r, dtype=np.float32)
+        for t in range(b0, min(T, b0 + SCORE_BLOCK)):
+            for j in range(int(k_per_token[t])):
+                u = int(topk_idx[t, j])
+                part[u] = np.float32(part[u] + np.float32(topk_w[t, j]))
+        for u in range(E_r):
+            total[u] = np.float32(total[u] + part[u])
+    if unit_scale is not None:
+        total = (total * np.asarray(unit_scale, dtype=np.float32)).astype(np.float32)
+    return total
+
+
+def select_pool(scores: np.ndarray, D: int) -> np.ndarray:
+    """The D best units: score descending, lower index first on ties.
+
+    Scores are compared as fp32 numbers (-0 equals +0; a NaN score ranks
+    below every number)."""
+    E_r = scores.shape[0]
+    s = np.asarray(scores, dtype=np.float64)
+    key = np.where(np.isnan(s), -np.inf, s)
+    key = np.where(key == 0.0, 0.0, key)
+    order = sorted(range(E_r), key=lambda u: (-key[u], u))
+    return np.array(sorted(order[:min(D, E_r)]), dtype=np.int64)
+
+
+def target_map(pool: np.ndarray, S: np.ndarray, L: np.ndarray, E_r: int):
+    """tau(u) and its scale: a pool member maps to itself with scale 1,
+    any other unit to the pool member of least L[u, p] (lower p on ties)."""
+    in_pool = np.zeros(E_r, dtype=bool)
+    in_pool[pool] = True
+    tau = np.empty(E_r, dtype=np.int64)
+    scale = np.empty(E_r, dtype=np.float32)
+    for u in range(E_r):
+        if in_pool[u]:
+            tau[u], scale[u] = u, np.float32(1.0)
+            continue
+        best = None
+        for p in sorted(int(v) for v in pool):
+            if best is None or L[u, p] < L[u, best]:
+                best = p
+        tau[u] = best
+        scale[u] = np.float32(S[u, best])
+    return tau, scale
+
+
+def fold_routes(topk_idx: np.ndarray, topk_w: np.ndarray, k_per_token, tau: np.ndarray,
+                scale: np.ndarray, in_pool: np.ndarray):
+    """Steps 3-4: remap every route to its target and coalesce per token.
+
+    Returns (idx [T, k_max] with -1 after the new budget, w [T, k_max] with 0
+    there, k_new [T])."""
+    T, k_max = topk_idx.shape
+    idx_out = np.full((T, k_max), -1, dtype=np.int64)
+    w_out = np.zeros((T, k_max), dtype=np.float32)
+    k_out = np.zeros(T, dtype=np.int64)
+    for t in range(T):
+        targets, weights = [], []
+        for j in range(int(k_per_token[t])):
+            u = int(topk_idx[t, j])
+            w = np.float32(topk_w[t, j])
+            if not in_pool[u]:
+                w = np.float32(w * scale[u])
+            v = int(tau[u])
+            if v in targets:
+                i = targets.index(v)
+                weights[i] = np.float32(weights[i] + w)
+            else:
+                targets.append(v)
+                weights.append(w)
+        k_out[t] = len(targets)
+        idx_out[t, :len(targets)] = targets
+        w_out[t, :len(targets)] = weights
+    return idx_out, w_out, k_out
+
+
+def fold_decode(topk_idx: np.ndarray, topk_w: np.ndarray, k_per_token, E_r: int, D: int,
+                S: np.ndarray, L: np.ndarray, pool: Optional[np.ndarray] = None,
+                unit_scale: Optional[np.ndarray] = None):
+    """The whole rewrite: (idx, w, k_new, pool).  pool=None: dynamic pool of D."""
+    if pool is None:
+        pool = select_pool(pool_scores(topk_idx, topk_w, k_per_token, E_r, unit_scale), D)
+    pool = np.array(sorted(int(p) for p in pool), dtype=np.int64)
+    in_pool = np.zeros(E_r, dtype=bool)
+    in_pool[pool] = True
+    tau, scale = target_map(pool, S, L, E_r)
+    idx, w, k = fold_routes(topk_idx, topk_w, k_per_token, tau, scale, in_pool)
+    return idx, w, k, pool

@@ -31,7 +31,7 @@ EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_gate_up", "moe
            "moe_grouped_ffn", "moe_shared_ffn", "moe_combine", "moe_layer_forward",
            "moe_get_device_status", "moe_status_string", "moe_permute_static",
            "moe_cg_workspace_size", "moe_pack_proxy_rows", "moe_route_cg",
-           "moe_layer_forward_cg")
+           "moe_layer_forward_cg", "moe_fold_decode", "moe_layer_forward_fold")
 
 
 class MoeLayerDesc(ctypes.Structure):
@@ -48,6 +48,11 @@ class MoeCgRouter(ctypes.Structure):
     _fields_ = [("m", ctypes.c_int32), ("r", ctypes.c_int32),
                 ("router_w_expert", ctypes.c_void_p), ("proxy_w", ctypes.c_void_p),
                 ("kappa", ctypes.c_void_p)]
+
+
+class MoeFoldDesc(ctypes.Structure):
+    _fields_ = [("D", ctypes.c_int32), ("pool", ctypes.c_void_p),
+                ("unit_scale", ctypes.c_void_p), ("S", ctypes.c_void_p), ("L", ctypes.c_void_p)]
 
 
 class MoeError(RuntimeError):
@@ -88,6 +93,10 @@ def lib() -> ctypes.CDLL:
                                             i32p, vp, i32p, vp, vp]),
             "moe_layer_forward_cg": (ctypes.c_int, [D, ctypes.POINTER(MoeCgRouter), vp, vp, vp,
                                                     i32p, vp, i32p, vp, vp]),
+            "moe_fold_decode": (ctypes.c_int, [D, ctypes.POINTER(MoeFoldDesc), i32p, vp, i32p,
+                                               i32p, vp, i32p, i32p, i32p, vp, vp]),
+            "moe_layer_forward_fold": (ctypes.c_int, [D, ctypes.POINTER(MoeFoldDesc), vp, vp,
+                                                      vp, vp, i32p, vp, i32p, vp, vp]),
             "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         }
         for name, (res, args) in sig.items():
@@ -284,6 +293,43 @@ def moe_layer_forward_cg(desc, cg, x, w_gate_up, w_down, k_per_token, out, dev_s
                                       _ptr(w_gate_up), _ptr(w_down), _ptr(k_per_token),
                                       _ptr(out), _ptr(dev_status), _ptr(workspace),
                                       _stream(stream))
+
+
+@dataclass
+class FoldDesc:
+    """Python mirror of moe_fold_desc (decode expert-pool folding)."""
+    D: int
+    S: torch.Tensor                          # fp32 [E_r, E_r]
+    L: torch.Tensor                          # fp32 [E_r, E_r]
+    pool: Optional[torch.Tensor] = None      # int32 [D]: static pool; None: dynamic
+    unit_scale: Optional[torch.Tensor] = None
+
+    def c(self) -> MoeFoldDesc:
+        f = MoeFoldDesc()
+        f.D = int(self.D)
+        f.pool = _ptr(self.pool)
+        f.unit_scale = _ptr(self.unit_scale)
+        f.S = _ptr(self.S)
+        f.L = _ptr(self.L)
+        return f
+
+
+def moe_fold_decode(desc, fold, topk_idx, topk_w, k_per_token, topk_idx_out, topk_w_out, k_out,
+                    pool_out, dev_status, workspace, stream=None) -> int:
+    d, f = desc.c(), fold.c()
+    return lib().moe_fold_decode(ctypes.byref(d), ctypes.byref(f), _ptr(topk_idx), _ptr(topk_w),
+                                 _ptr(k_per_token), _ptr(topk_idx_out), _ptr(topk_w_out),
+                                 _ptr(k_out), _ptr(pool_out), _ptr(dev_status), _ptr(workspace),
+                                 _stream(stream))
+
+
+def moe_layer_forward_fold(desc, fold, x, router_w, w_gate_up, w_down, k_per_token, out,
+                           dev_status, workspace, stream=None) -> int:
+    d, f = desc.c(), fold.c()
+    return lib().moe_layer_forward_fold(ctypes.byref(d), ctypes.byref(f), _ptr(x), _ptr(router_w),
+                                        _ptr(w_gate_up), _ptr(w_down), _ptr(k_per_token),
+                                        _ptr(out), _ptr(dev_status), _ptr(workspace),
+                                        _stream(stream))
 
 
 def moe_get_device_status(dev_status, stream=None) -> int:

@@ -23,7 +23,8 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 // Byte offsets of every workspace region for one desc.
 struct Layout {
   size_t logits, router_partial, topk_idx, topk_w, counts, offsets, sorted_token, inv_row, bitmap,
-      wprefix, xperm, act, yperm, act_sh, ysh, split_word, partial, chunk_done, ffn_part, total;
+      wprefix, xperm, act, yperm, act_sh, ysh, split_word, partial, chunk_done, ffn_part,
+      fold_ws, fold_idx, fold_w, fold_k, total;
   int router_slices;   // slices of the CUDA-core router (0: the tensor-core router runs)
   int max_split;       // K splits the decode gate|up kernel may use (1: none)
   int max_split_down;  // K splits the decode down kernel may use
@@ -106,6 +107,11 @@ Layout layout_of(const moe_layer_desc& d) {
   const size_t need_gu = l.max_split > 1 ? l.max_split * per_gu : 0;
   const size_t need_dn = l.max_split_down > 1 ? l.max_split_down * per_dn : 0;
   l.partial = take(need_gu > need_dn ? need_gu : need_dn);
+  // decode expert-pool folding: block scores and target map, folded routing
+  l.fold_ws = take(moe::fold_workspace_bytes(d.T, static_cast<int>(E_r)));
+  l.fold_idx = take(n_cap * 4);
+  l.fold_w = take(n_cap * 4);
+  l.fold_k = take(T * 4);
   l.total = o;
   return l;
 }
@@ -504,6 +510,28 @@ moe_status do_combine(const moe_layer_desc* d, const void* y_perm, const void* y
                                          d->k_max, static_cast<int>(n_cap), out, status, s));
 }
 
+// ---------------------------------------------------------------- expert-pool folding
+
+moe_status validate_fold(const moe_layer_desc* d, const moe_fold_desc* f) {
+  MOE_TRY(validate(d));
+  if (f == nullptr) return MOE_ERR_INVALID_ARGUMENT;
+  if (f->D < 1 || f->D > E_r_of(d)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  MOE_TRY(check_ptrs4({f->S, f->L}));
+  if (f->pool != nullptr) MOE_TRY(check_ptrs4({f->pool}));
+  if (f->unit_scale != nullptr) MOE_TRY(check_ptrs4({f->unit_scale}));
+  return MOE_OK;
+}
+
+moe_status do_fold(const moe_layer_desc* d, const moe_fold_desc* f, const int32_t* topk_idx,
+                   const float* topk_w, const int32_t* kpt, int32_t* idx_out, float* w_out,
+                   int32_t* k_out, int32_t* pool_out, int32_t* status, void* ws, cudaStream_t s) {
+  const Layout l = layout_of(*d);
+  return cuda_status(moe::launch_fold_decode(topk_idx, topk_w, kpt, d->T, d->k_max, E_r_of(d),
+                                             f->D, f->pool, f->unit_scale, f->S, f->L, idx_out,
+                                             w_out, k_out, pool_out, at<void>(ws, l.fold_ws),
+                                             status, s));
+}
+
 // ---------------------------------------------------------------- proxy router
 
 moe_status validate_cg(const moe_layer_desc* d, const moe_cg_router* cg) {
@@ -830,6 +858,55 @@ moe_status moe_layer_forward_cg(const moe_layer_desc* desc, const moe_cg_router*
   MOE_TRY(do_grouped_ffn(desc, x, sorted_token, offsets, w_gate_up, w_down, yperm, dev_status,
                          workspace, s));
   return do_combine(desc, yperm, ysh, inv_row, topk_w, k_per_token, out, dev_status, s);
+}
+
+moe_status moe_fold_decode(const moe_layer_desc* desc, const moe_fold_desc* fold,
+                           const int32_t* topk_idx, const float* topk_w,
+                           const int32_t* k_per_token, int32_t* topk_idx_out,
+                           float* topk_w_out, int32_t* k_out, int32_t* pool_out,
+                           int32_t* dev_status, void* workspace, void* stream) {
+  MOE_TRY(validate_fold(desc, fold));
+  if (desc->T == 0) return MOE_OK;
+  MOE_TRY(check_ptrs4({topk_idx, topk_w, k_per_token, topk_idx_out, topk_w_out, k_out,
+                       dev_status}));
+  if (pool_out != nullptr) MOE_TRY(check_ptrs4({pool_out}));
+  MOE_TRY(check_ws(workspace));
+  return do_fold(desc, fold, topk_idx, topk_w, k_per_token, topk_idx_out, topk_w_out, k_out,
+                 pool_out, dev_status, workspace, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_layer_forward_fold(const moe_layer_desc* desc, const moe_fold_desc* fold,
+                                  const void* x, const void* router_w, const void* w_gate_up,
+                                  const void* w_down, const int32_t* k_per_token, void* out,
+                                  int32_t* dev_status, void* workspace, void* stream) {
+  MOE_TRY(validate_fold(desc, fold));
+  if (desc->T == 0) return MOE_OK;
+  MOE_TRY(check_ptrs({x, router_w, w_gate_up, w_down, out}));
+  MOE_TRY(check_ptrs4({k_per_token, dev_status}));
+  MOE_TRY(check_ws(workspace));
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Layout l = layout_of(*desc);
+  int32_t* topk_idx = at<int32_t>(workspace, l.topk_idx);
+  float* topk_w = at<float>(workspace, l.topk_w);
+  int32_t* fidx = at<int32_t>(workspace, l.fold_idx);
+  float* fw = at<float>(workspace, l.fold_w);
+  int32_t* fk = at<int32_t>(workspace, l.fold_k);
+  int32_t* counts = at<int32_t>(workspace, l.counts);
+  int32_t* offsets = at<int32_t>(workspace, l.offsets);
+  int32_t* sorted_token = at<int32_t>(workspace, l.sorted_token);
+  int32_t* inv_row = at<int32_t>(workspace, l.inv_row);
+  void* yperm = at<void>(workspace, l.yperm);
+  void* ysh = desc->I_shared > 0 ? at<void>(workspace, l.ysh) : nullptr;
+  MOE_TRY(do_route(desc, x, router_w, nullptr, k_per_token, nullptr, topk_idx, topk_w,
+                   dev_status, workspace, s));
+  MOE_TRY(do_fold(desc, fold, topk_idx, topk_w, k_per_token, fidx, fw, fk, nullptr, dev_status,
+                  workspace, s));
+  MOE_TRY(do_permute(desc, fidx, fk, counts, offsets, sorted_token, inv_row, dev_status,
+                     workspace, s));
+  if (ysh != nullptr) MOE_TRY(do_shared(desc, x, ysh, dev_status, workspace, s));
+  MOE_TRY(do_grouped_ffn(desc, x, sorted_token, offsets, w_gate_up, w_down, yperm, dev_status,
+                         workspace, s));
+  return do_combine(desc, yperm, ysh, inv_row, fw, fk, out, dev_status, s);
 }
 
 moe_status moe_get_device_status(const int32_t* dev_status, void* stream) {

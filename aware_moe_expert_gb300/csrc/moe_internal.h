@@ -62,6 +62,17 @@ cudaError_t launch_cg_select(const float* partial, int S, int R, bool compact,
                              int r, int k_max, int n_experts, float* proxy_out, int32_t* topk_idx,
                              float* topk_w, int32_t* status, cudaStream_t s);
 
+// ---- fold.cu: decode expert-pool folding
+// Workspace bytes: ceil(T/64) * E_r fp32 block scores + target map.
+size_t fold_workspace_bytes(int T, int E_r);
+// pool_in == nullptr: dynamic pool of D units; S, L: fp32 [E_r, E_r];
+// unit_scale nullable; pool_out nullable ([D], ascending).
+cudaError_t launch_fold_decode(const int32_t* topk_idx, const float* topk_w,
+                               const int32_t* k_per_token, int T, int k_max, int E_r, int D,
+                               const int32_t* pool_in, const float* unit_scale, const float* S,
+                               const float* L, int32_t* idx_out, float* w_out, int32_t* k_out,
+                               int32_t* pool_out, void* ws, int32_t* status, cudaStream_t s);
+
 // ---- permute.cu
 cudaError_t launch_permute(const int32_t* topk_idx, const int32_t* k_per_token, int T,
                            int k_max, int E_r, uint32_t* bitmap, int32_t* wprefix,

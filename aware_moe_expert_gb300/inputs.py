@@ -150,6 +150,19 @@ def make_cg_inputs(wl: Workload, device="cpu", seed: Optional[int] = None, r: in
             "kappa": allocation_table(wl.k_max, wl.native_m, wl.n_sub).to(dev)}
 
 
+def make_fold_tables(E_r: int, device="cpu", seed: int = 11):
+    """Synthetic calibration tables for decode expert-pool folding (the pages'
+    tables come from calibration data, out of scope here): S [E_r, E_r] scalar
+    projectors ~ N(1, 0.25^2) clipped to [-4, 4] with S[u, u] = 1, and L
+    [E_r, E_r] projection losses ~ U(0, 1) with L[u, u] = 0; fp32."""
+    g = torch.Generator().manual_seed(seed)
+    S = (1.0 + 0.25 * torch.randn(E_r, E_r, generator=g)).clamp_(-4.0, 4.0)
+    S.fill_diagonal_(1.0)
+    L = torch.rand(E_r, E_r, generator=g)
+    L.fill_diagonal_(0.0)
+    return S.float().contiguous().to(device), L.float().contiguous().to(device)
+
+
 def make_logits(T: int, E_r: int, device="cpu", seed: int = 7, kind: str = "normal"):
     """Float32 logits for routing-only tests.
 

@@ -55,6 +55,8 @@ def parse():
                    help="linear: the expanded linear gate over all units (the default); "
                         "cg: the training-free proxy router (original router + gate neurons)")
     p.add_argument("--cg-r", type=int, default=8, help="gate neurons per sub-expert (--router cg)")
+    p.add_argument("--fold", type=int, default=0,
+                   help="decode expert-pool folding to a dynamic pool of D units (0: off)")
     p.add_argument("--force-pair", action="store_true",
                    help="run grouped prefill GEMMs on the CTA-pair kernel (debug flag)")
     return p.parse_args()
@@ -177,6 +179,14 @@ def run_ours(args, wl, rank, world, local):
                                       proxy_w, st0), "moe_pack_proxy_rows")
         cg = B.CgRouter(m=wl.native_m, r=args.cg_r, router_w_expert=ci["router_w_expert"],
                         proxy_w=proxy_w, kappa=ci["kappa"])
+    fold = None
+    if args.fold > 0:
+        from aware_moe_expert_gb300.inputs import make_fold_tables
+        S_t, L_t = make_fold_tables(E_r, dev, seed=wl.seed + 5)
+        fold = B.FoldDesc(D=args.fold, S=S_t, L=L_t)
+        fidx = torch.empty(T, k_max, dtype=torch.int32, device=dev)
+        fw = torch.empty(T, k_max, dtype=torch.float32, device=dev)
+        fk = torch.empty(T, dtype=torch.int32, device=dev)
     ws_bytes = B.moe_workspace_size(desc) if cg is None else B.moe_cg_workspace_size(desc, cg)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -201,7 +211,15 @@ def run_ours(args, wl, rank, world, local):
         B.check(B.moe_route(desc, d["x"], d["router_w"], None, d["k_per_token"], None, idx, w,
                             st, ws, sp), "moe_route")
 
+    def call_fold(sp):
+        B.check(B.moe_fold_decode(desc, fold, idx, w, d["k_per_token"], fidx, fw, fk, None, st,
+                                  ws, sp), "moe_fold_decode")
+
     def call_permute(sp):
+        if fold is not None:
+            B.check(B.moe_permute(desc, fidx, fk, counts, offsets, st_tok, inv, st, ws, sp),
+                    "moe_permute")
+            return
         B.check(B.moe_permute(desc, idx, d["k_per_token"], counts, offsets, st_tok, inv, st, ws,
                               sp), "moe_permute")
 
@@ -220,9 +238,15 @@ def run_ours(args, wl, rank, world, local):
                                   st, ws, sp), "moe_grouped_ffn")
 
     def call_combine(sp):
+        if fold is not None:
+            B.check(B.moe_combine(desc, y, ysh, inv, fw, fk, out, st, sp), "moe_combine")
+            return
         B.check(B.moe_combine(desc, y, ysh, inv, w, d["k_per_token"], out, st, sp), "moe_combine")
 
-    calls = [("route", call_route), ("permute", call_permute)]
+    calls = [("route", call_route)]
+    if fold is not None:
+        calls.append(("fold", call_fold))
+    calls.append(("permute", call_permute))
     if ysh is not None:
         calls.append(("shared_ffn", call_shared))
     calls += [("gate_up", call_gate_up), ("down", call_down), ("grouped_ffn", call_grouped_ffn),
@@ -236,6 +260,11 @@ def run_ours(args, wl, rank, world, local):
     ws_fused = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
 
     def layer_step(sp):
+        if fold is not None:
+            B.check(B.moe_layer_forward_fold(desc, fold, d["x"], d["router_w"], d["w_gate_up"],
+                                             d["w_down"], d["k_per_token"], out_fused, st,
+                                             ws_fused, sp), "moe_layer_forward_fold")
+            return
         if cg is not None:
             B.check(B.moe_layer_forward_cg(desc, cg, d["x"], d["w_gate_up"], d["w_down"],
                                            d["k_per_token"], out_fused, st, ws_fused, sp),
@@ -428,7 +457,8 @@ def run_ours(args, wl, rank, world, local):
                 "kernel": "moe_gate_up (row gather + grouped gate|up GEMM, SwiGLU epilogue)",
                 "algorithmic_flops": alg, "peak_source": peaks["source"] + " bf16_tflops (burst)"}
 
-    n_launch = launches_per_step(wl, T, args.path) + (2 if cg is not None else 0)
+    n_launch = launches_per_step(wl, T, args.path, fold=fold is not None) + \
+        (2 if cg is not None else 0)
     us = ms * 1000.0
     res = {
         "metric": METRIC,
@@ -444,6 +474,9 @@ def run_ours(args, wl, rank, world, local):
                      "n_sub": wl.n_sub, "E_r": E_r, "I_sub": I_sub, "I_shared": wl.I_shared,
                      "k_choices": list(wl.k_choices), "k_per": wl.k_per, "score": wl.score,
                      "parallelism": f"replicas{world}",
+                     "fold": (None if fold is None else
+                              f"decode expert-pool folding: dynamic pool of {args.fold} units, "
+                              "synthetic S/L tables"),
                      "router": ("linear gate over all units" if cg is None else
                                 f"proxy router: top-{wl.native_m} experts, {args.cg_r} gate "
                                 f"neurons per sub-expert, even allocation table"),
@@ -470,7 +503,7 @@ def run_ours(args, wl, rank, world, local):
     return res, d
 
 
-def launches_per_step(wl, T, path=0):
+def launches_per_step(wl, T, path=0, fold=False):
     """Kernels libmoe enqueues per moe_layer_forward (mirrors the host
     sequencing in csrc/api.cu: router + top-k (one cluster launch on CUDA
     cores, or the tensor-core GEMM and the top-k kernel), permutation (fused
@@ -483,12 +516,13 @@ def launches_per_step(wl, T, path=0):
     tc_router = T >= 128 and wl.E_r in (64, 128, 256)
     cluster_router = not tc_router and wl.H <= 12288
     decode_ffn = decode and wl.H % 128 == 0 and wl.I_sub % 128 == 0
-    fused_front = cluster_router and T <= 8          # logits + top-k + permutation (+ gather)
+    fused_front = cluster_router and T <= 8 and not fold   # logits + top-k + permutation (+ gather)
     if fused_front:
         n = 1
     else:
         n = 1 if cluster_router else 2               # logits (+ top-k)
         n += 1 if (T + 31) // 32 <= 8 else 3        # permutation (one CTA, or bitmap/scan/scatter)
+    n += 3 if fold else 0                            # fold: scores, pool, remap
     n += 2 if wl.I_shared else 0                     # shared expert gate|up, down
     if decode_ffn:
         n += 1 if fused_front else 2                 # (row gather +) fused decode FFN kernel

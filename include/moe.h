@@ -186,6 +186,50 @@ moe_status moe_permute_static(const moe_layer_desc* desc, const int32_t* topk_id
                               void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Decode expert-pool folding ("ExFold: Unified Expert Folding for Training-Free
+ * MoE Prefill-Decode Acceleration", arXiv 2608.24938, "Phase-Specific Routing
+ * and Folding").  Decode time follows the distinct units a batch activates;
+ * folding keeps a pool of D units and remaps every other route to its pool
+ * target tau(u) = argmin_{p in pool} L[u, p] (lower index on ties), its weight
+ * scaled by S[u, tau(u)].  Routes of a token that reach one target are merged
+ * (fp32 sum in slot order) at the position of their first occurrence, so each
+ * target runs once; the token's budget becomes the number of targets.
+ * Dynamic pool: the D units with the largest score h_u * sum of their routed
+ * weights over the batch (fp32, tokens in blocks of 64 added in order; score
+ * descending, lower index on ties).  Static pool: the caller's D units.
+ */
+typedef struct {
+  int32_t D;                  /* pool size, 1..E_r                                      */
+  const int32_t* pool;        /* nullable device int32 [D]: a static pool of distinct
+                                 units (else MOE_ERR_BAD_INDEX); null: dynamic pool      */
+  const float* unit_scale;    /* nullable device fp32 [E_r]: h_u of the dynamic score
+                                 (null: 1)                                               */
+  const float* S;             /* device fp32 [E_r, E_r]: S[u, v] scales a route folded
+                                 from unit u into unit v (calibration data)              */
+  const float* L;             /* device fp32 [E_r, E_r]: loss of folding u into v        */
+} moe_fold_desc;
+
+/* Rewrites routing (topk_idx, topk_w, k_per_token: as from moe_route) into
+ *   topk_idx_out int32 [T, k_max]  targets, first-occurrence order, -1 after k_out[t]
+ *   topk_w_out   fp32 [T, k_max]   merged weights, 0 after k_out[t]
+ *   k_out        int32 [T]         the new budgets (<= the old ones)
+ *   pool_out     nullable int32 [D]: the pool, ascending.
+ * The outputs feed moe_permute / moe_combine like moe_route's.  Workspace:
+ * moe_workspace_size(desc) bytes. */
+moe_status moe_fold_decode(const moe_layer_desc* desc, const moe_fold_desc* fold,
+                           const int32_t* topk_idx, const float* topk_w,
+                           const int32_t* k_per_token, int32_t* topk_idx_out,
+                           float* topk_w_out, int32_t* k_out, int32_t* pool_out,
+                           int32_t* dev_status, void* workspace, void* stream);
+
+/* The whole layer with folding: route -> fold -> permute -> [shared FFN] ->
+ * grouped FFN -> combine.  out bf16 [T, H].  Workspace: moe_workspace_size. */
+moe_status moe_layer_forward_fold(const moe_layer_desc* desc, const moe_fold_desc* fold,
+                                  const void* x, const void* router_w, const void* w_gate_up,
+                                  const void* w_down, const int32_t* k_per_token, void* out,
+                                  int32_t* dev_status, void* workspace, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Training-free proxy router (MoE-Prism §III-B2, "Training-Free Proxy Gating",
  * Fig. 7 left).  The original router scores the n_experts original experts and
  * keeps its native m of them per token (selection, normalisation and scaling

@@ -30,7 +30,8 @@ listed reading):
      block order (the order the GPU uses; fp32 because the sum decides an
      integer, the pool).
   2. target map: tau(u) = u for a pool member; otherwise the pool member p with
-     the smallest L[u, p] (lower index on ties), with scale S[u, tau(u)].
+     the smallest L[u, p] (lower index on ties, a NaN loss counting as +inf),
+     with scale S[u, tau(u)].
   3. remap: route (t, j) of unit u and weight w becomes (tau(u), w * S[u, tau])
      (fp32 product); a pool member keeps its weight unchanged.
   4. coalesce: per token, routes with the same target are merged in slot order
@@ -89,7 +90,8 @@ def select_pool(scores: np.ndarray, D: int) -> np.ndarray:
 
 def target_map(pool: np.ndarray, S: np.ndarray, L: np.ndarray, E_r: int):
     """tau(u) and its scale: a pool member maps to itself with scale 1,
-    any other unit to the pool member of least L[u, p] (lower p on ties)."""
+    any other unit to the pool member of least L[u, p] (lower p on ties; a
+    NaN loss counts as +inf)."""
     in_pool = np.zeros(E_r, dtype=bool)
     in_pool[pool] = True
     tau = np.empty(E_r, dtype=np.int64)
@@ -98,9 +100,12 @@ def target_map(pool: np.ndarray, S: np.ndarray, L: np.ndarray, E_r: int):
         if in_pool[u]:
             tau[u], scale[u] = u, np.float32(1.0)
             continue
+        def loss(p):
+            v = float(L[u, p])
+            return np.inf if np.isnan(v) else v
         best = None
         for p in sorted(int(v) for v in pool):
-            if best is None or L[u, p] < L[u, best]:
+            if best is None or loss(p) < loss(best):
                 best = p
         tau[u] = best
         scale[u] = np.float32(S[u, best])

@@ -198,3 +198,16 @@ def test_static_pool_and_unit_scale():
     routed = F.pool_scores(idx, w, k, 12)
     if (routed[[0, 5, 9]] > 0).all():
         assert pool2.tolist() == [0, 5, 9]
+
+
+def test_nan_loss_is_never_preferred():
+    """A NaN projection loss counts as +inf: the finite least loss wins even
+    when the NaN belongs to the lowest-index pool member; all-NaN falls back
+    to the lowest index."""
+    E_r = 5
+    L = np.ones((E_r, E_r), dtype=np.float32)
+    S = np.ones((E_r, E_r), dtype=np.float32)
+    L[3, 0], L[3, 1], L[3, 2] = np.nan, 0.7, 0.4
+    L[4, :3] = np.nan
+    tau, _ = F.target_map(np.array([0, 1, 2]), S, L, E_r)
+    assert tau[3] == 2 and tau[4] == 0

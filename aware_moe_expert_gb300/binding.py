@@ -31,7 +31,8 @@ EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_gate_up", "moe
            "moe_grouped_ffn", "moe_shared_ffn", "moe_combine", "moe_layer_forward",
            "moe_get_device_status", "moe_status_string", "moe_permute_static",
            "moe_cg_workspace_size", "moe_pack_proxy_rows", "moe_route_cg",
-           "moe_layer_forward_cg", "moe_fold_decode", "moe_layer_forward_fold")
+           "moe_layer_forward_cg", "moe_fold_decode", "moe_layer_forward_fold",
+           "moe_cost_lookup", "moe_tier_schedule")
 
 
 class MoeLayerDesc(ctypes.Structure):
@@ -53,6 +54,16 @@ class MoeCgRouter(ctypes.Structure):
 class MoeFoldDesc(ctypes.Structure):
     _fields_ = [("D", ctypes.c_int32), ("pool", ctypes.c_void_p),
                 ("unit_scale", ctypes.c_void_p), ("S", ctypes.c_void_p), ("L", ctypes.c_void_p)]
+
+
+class MoeTierRequest(ctypes.Structure):
+    _fields_ = [("arrival", ctypes.c_double), ("n_tokens", ctypes.c_int32), ("k", ctypes.c_int32)]
+
+
+class MoeCostTable(ctypes.Structure):
+    _fields_ = [("n_count", ctypes.c_int32), ("n_points", ctypes.c_void_p),
+                ("k_count", ctypes.c_int32), ("k_points", ctypes.c_void_p),
+                ("t_us", ctypes.c_void_p)]
 
 
 class MoeError(RuntimeError):
@@ -97,6 +108,11 @@ def lib() -> ctypes.CDLL:
                                                i32p, vp, i32p, i32p, i32p, vp, vp]),
             "moe_layer_forward_fold": (ctypes.c_int, [D, ctypes.POINTER(MoeFoldDesc), vp, vp,
                                                       vp, vp, i32p, vp, i32p, vp, vp]),
+            "moe_cost_lookup": (ctypes.c_double, [ctypes.POINTER(MoeCostTable), ctypes.c_double,
+                                                  ctypes.c_double]),
+            "moe_tier_schedule": (ctypes.c_int32, [ctypes.POINTER(MoeTierRequest), ctypes.c_int32,
+                                                   ctypes.c_int32, ctypes.POINTER(MoeCostTable),
+                                                   vp, vp, vp, ctypes.c_int32]),
             "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         }
         for name, (res, args) in sig.items():
@@ -330,6 +346,49 @@ def moe_layer_forward_fold(desc, fold, x, router_w, w_gate_up, w_down, k_per_tok
                                         _ptr(w_gate_up), _ptr(w_down), _ptr(k_per_token),
                                         _ptr(out), _ptr(dev_status), _ptr(workspace),
                                         _stream(stream))
+
+
+class CostTable:
+    """Host mirror of moe_cost_table: T(n, k) in microseconds at token buckets
+    n_points and budget buckets k_points (t_us[k_index][n_index])."""
+
+    def __init__(self, n_points, k_points, t_us):
+        import numpy as np
+        self.n = np.ascontiguousarray(n_points, dtype=np.int32)
+        self.k = np.ascontiguousarray(k_points, dtype=np.int32)
+        self.t = np.ascontiguousarray(t_us, dtype=np.float64).reshape(len(self.k), len(self.n))
+
+    def c(self) -> MoeCostTable:
+        c = MoeCostTable()
+        c.n_count, c.k_count = len(self.n), len(self.k)
+        c.n_points = self.n.ctypes.data
+        c.k_points = self.k.ctypes.data
+        c.t_us = self.t.ctypes.data
+        return c
+
+
+def moe_cost_lookup(table: CostTable, n: float, k: float) -> float:
+    c = table.c()
+    return float(lib().moe_cost_lookup(ctypes.byref(c), float(n), float(k)))
+
+
+def moe_tier_schedule(requests, M: int, table: CostTable):
+    """requests: sequence of (arrival, n_tokens, k).  Returns (batch_of,
+    batch_k, batch_tokens) as lists, or raises on an error code."""
+    import numpy as np
+    n = len(requests)
+    arr = (MoeTierRequest * max(n, 1))()
+    for i, (a, tok, k) in enumerate(requests):
+        arr[i].arrival, arr[i].n_tokens, arr[i].k = float(a), int(tok), int(k)
+    batch_of = np.zeros(max(n, 1), dtype=np.int32)
+    bk = np.zeros(max(n, 1), dtype=np.int32)
+    bt = np.zeros(max(n, 1), dtype=np.int32)
+    c = table.c()
+    nb = lib().moe_tier_schedule(arr, n, int(M), ctypes.byref(c), batch_of.ctypes.data,
+                                 bk.ctypes.data, bt.ctypes.data, max(n, 1))
+    if nb < 0:
+        raise MoeError(1, f"moe_tier_schedule returned {nb}")
+    return batch_of[:n].tolist(), bk[:nb].tolist(), bt[:nb].tolist()
 
 
 def moe_get_device_status(dev_status, stream=None) -> int:

@@ -18,7 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "libmoe.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
 SOURCES = ["api.cu", "route.cu", "permute.cu", "gemm.cu", "gemm_decode.cu", "ffn_decode.cu",
-           "combine.cu", "noalloc.cu", "gemm_pair.cu", "cg_router.cu", "fold.cu"]
+           "combine.cu", "noalloc.cu", "gemm_pair.cu", "cg_router.cu", "fold.cu",
+           "scheduler.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include")]
@@ -37,7 +38,7 @@ def build(verbose: bool = False, extra_flags=None) -> str:
     flags = FLAGS + list(extra_flags or [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
         cmd = [nvcc, *ARCH, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:

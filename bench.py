@@ -57,6 +57,11 @@ def parse():
     p.add_argument("--cg-r", type=int, default=8, help="gate neurons per sub-expert (--router cg)")
     p.add_argument("--fold", type=int, default=0,
                    help="decode expert-pool folding to a dynamic pool of D units (0: off)")
+    p.add_argument("--tiered", action="store_true",
+                   help="offline queue experiment: profile T(n, k) on this GPU, then time a "
+                        "synthetic request queue batched FIFO at the batch-max budget, by "
+                        "quality tiers (Eq. 5) at the batch-max budget, and FIFO at every "
+                        "request's own budget")
     p.add_argument("--force-pair", action="store_true",
                    help="run grouped prefill GEMMs on the CTA-pair kernel (debug flag)")
     return p.parse_args()
@@ -618,6 +623,120 @@ def run_reference(args, wl, rank, world):
                     "d2h_bytes_per_step": 0}}
 
 
+def run_tiered(args, wl, rank, world, local):
+    """Quality-tiered batching on the prefill-shaped workload.
+
+    1. T(n, k): moe_layer_forward with every token at budget k, n tokens,
+       CUDA-event mean of timed calls with L2 flushed before each.
+    2. A seeded synthetic offline queue (request sizes and budgets drawn
+       uniformly) is batched three ways under the token budget M = T of the
+       workload: FIFO by arrival at the batch-max budget; by quality tiers with
+       Eq. (5) (moe_tier_schedule, the library's host scheduler) at the
+       batch-max budget; FIFO at every request's own budget (this library's
+       layer runs per-token budgets natively).  Each batch is run and timed.
+    """
+    import torch
+    from aware_moe_expert_gb300 import binding as B
+    from aware_moe_expert_gb300.inputs import make_layer_inputs
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    d = make_layer_inputs(wl, dev, seed=wl.seed + 1000 * rank)
+    M = wl.T
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    descs, wss, outs = {}, {}, {}
+
+    def run_batch(k_vec, reps):
+        n = int(k_vec.numel())
+        if n not in descs:
+            descs[n] = B.desc_for(wl, T=n, expert_bias=d["expert_bias"])
+            wss[n] = torch.empty(B.moe_workspace_size(descs[n]), dtype=torch.uint8, device=dev)
+            outs[n] = torch.empty(n, wl.H, dtype=torch.bfloat16, device=dev)
+        x = d["x"][:n]
+        times = []
+        with torch.cuda.stream(stream):
+            for r in range(reps + 1):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                B.check(B.moe_layer_forward(descs[n], x, d["router_w"], d["w_gate_up"],
+                                            d["w_down"], k_vec, outs[n], st, wss[n],
+                                            stream.cuda_stream), "moe_layer_forward")
+                e1.record(stream)
+                times.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        return float(np.mean([a.elapsed_time(b) for a, b in times[1:]])) * 1000.0
+
+    k_points = sorted(set(wl.k_choices))
+    n_points = [M // 16, M // 8, M // 4, M // 2, M]
+    t_us = [[run_batch(torch.full((n,), k, dtype=torch.int32, device=dev), 3) for n in n_points]
+            for k in k_points]
+    table = B.CostTable(n_points, k_points, t_us)
+
+    rng = np.random.default_rng(wl.seed + 77)
+    n_req = 64
+    reqs = [(float(i), int(rng.integers(M // 64, M // 8 + 1)), int(rng.choice(k_points)))
+            for i in range(n_req)]
+    total_tok = sum(r[1] for r in reqs)
+
+    def fifo(reqs_):
+        out, cur, tok = [], [], 0
+        for i in range(len(reqs_)):
+            if cur and tok + reqs_[i][1] > M:
+                out.append(cur)
+                cur, tok = [], 0
+            cur.append(i)
+            tok += reqs_[i][1]
+        if cur:
+            out.append(cur)
+        return out
+
+    def time_batches(batches, batch_max):
+        tot = 0.0
+        for b in batches:
+            if batch_max:
+                kk = max(reqs[i][2] for i in b)
+                ks = [kk] * sum(reqs[i][1] for i in b)
+            else:
+                ks = [reqs[i][2] for i in b for _ in range(reqs[i][1])]
+            tot += run_batch(torch.tensor(ks, dtype=torch.int32, device=dev), 2)
+        return tot
+
+    f_batches = fifo(reqs)
+    batch_of, bk, _ = B.moe_tier_schedule(reqs, M, table)
+    t_batches = [[] for _ in bk]
+    order = sorted(range(n_req), key=lambda i: (reqs[i][2], reqs[i][0], i))
+    for i in order:
+        t_batches[batch_of[i]].append(i)
+    t_fifo_max = time_batches(f_batches, True)
+    t_tiered = time_batches(t_batches, True)
+    t_exact = time_batches(f_batches, False)
+    served = lambda batches: sum(max(reqs[i][2] for i in b) * reqs[j][1]  # noqa: E731
+                                 for b in batches for j in b)
+    exact_assign = sum(r[1] * r[2] for r in reqs)
+    return {
+        "metric": "MoE-layer tokens/s over an offline request queue (quality-tiered batching)",
+        "unit": "tokens/s", "higher_is_better": True, "n_gpus": world, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "token_budget_M": M, "requests": n_req,
+                   "request_tokens": [M // 64, M // 8], "k_choices": k_points},
+        "cost_table_us": {"n_points": n_points, "k_points": k_points,
+                          "t_us": [[round(v, 2) for v in row] for row in t_us]},
+        "value": round(total_tok / (t_tiered * 1e-6), 1),
+        "fifo_batch_max_k": {"tokens_per_s": round(total_tok / (t_fifo_max * 1e-6), 1),
+                             "batches": len(f_batches),
+                             "served_assignments": served(f_batches)},
+        "tiered_batch_max_k": {"tokens_per_s": round(total_tok / (t_tiered * 1e-6), 1),
+                               "batches": len(t_batches),
+                               "served_assignments": served(t_batches)},
+        "fifo_exact_k": {"tokens_per_s": round(total_tok / (t_exact * 1e-6), 1),
+                         "batches": len(f_batches), "served_assignments": exact_assign},
+    }
+
+
 def main():
     args = parse()
     from aware_moe_expert_gb300 import workloads as WL
@@ -628,6 +747,11 @@ def main():
     if args.impl == "reference":
         res = run_reference(args, wl, rank, world)
         if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    if args.tiered:
+        res = run_tiered(args, wl, rank, world, local)
+        if rank == 0:
             print(json.dumps(res), flush=True)
         return
     res, d = run_ours(args, wl, rank, world, local)

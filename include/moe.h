@@ -230,6 +230,47 @@ moe_status moe_layer_forward_fold(const moe_layer_desc* desc, const moe_fold_des
                                   int32_t* dev_status, void* workspace, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Quality-tiered batching (host only; MoE-Prism §III-C2 "Temporal Separation
+ * via Quality-Tiered Batching", Eq. (5)).  For dispatches that run a whole
+ * batch at one budget (the batch maximum), requests are grouped by budget:
+ * the queue is sorted by (k, arrival), batches are filled in FIFO order up to
+ * M prompt tokens tier by tier, and a residual batch (n_cur tokens at budget
+ * k) is promoted to the next tier's budget k_next and merged with the n_next
+ * tokens of that tier's leading requests that still fit iff
+ *     (n_cur + n_next) / T(n_cur + n_next, k_next) >= n_cur / T(n_cur, k),
+ * else it is dispatched at k.  T(n, k) is a table profiled on the deployment
+ * GPU at token and budget buckets, interpolated between them.
+ */
+typedef struct {
+  double arrival;     /* arrival time (any unit); FIFO order inside a tier        */
+  int32_t n_tokens;   /* prompt tokens, >= 1                                      */
+  int32_t k;          /* requested routing budget                                 */
+} moe_tier_request;
+
+typedef struct {
+  int32_t n_count;            /* token buckets, >= 1                              */
+  const int32_t* n_points;    /* host, strictly increasing                        */
+  int32_t k_count;            /* budget buckets, >= 1                             */
+  const int32_t* k_points;    /* host, strictly increasing                        */
+  const double* t_us;         /* host [k_count][n_count]: layer time at each bucket */
+} moe_cost_table;
+
+/* T(n, k): linear in n between buckets (end segments extended linearly; one
+ * bucket scales proportionally), linear in k between buckets, k clamped to
+ * the profiled range.  Returns -1 for a malformed table.  Host only. */
+double moe_cost_lookup(const moe_cost_table* table, double n, double k);
+
+/* Schedules n_req host requests under token budget M.  Writes, in dispatch
+ * order, batch_of[i] (batch index of request i), and when non-null batch_k[b]
+ * (the budget batch b runs at) and batch_tokens[b].  Returns the number of
+ * batches, -1 on bad arguments (M < 1, a request with < 1 token, a malformed
+ * table), -2 if more than max_batches would be needed.  A request larger than
+ * M forms a batch of its own.  Host only: no device memory, no stream. */
+int32_t moe_tier_schedule(const moe_tier_request* reqs, int32_t n_req, int32_t M,
+                          const moe_cost_table* table, int32_t* batch_of, int32_t* batch_k,
+                          int32_t* batch_tokens, int32_t max_batches);
+
+/* ---------------------------------------------------------------------------
  * Training-free proxy router (MoE-Prism §III-B2, "Training-Free Proxy Gating",
  * Fig. 7 left).  The original router scores the n_experts original experts and
  * keeps its native m of them per token (selection, normalisation and scaling

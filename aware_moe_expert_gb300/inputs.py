@@ -163,6 +163,21 @@ def make_fold_tables(E_r: int, device="cpu", seed: int = 11):
     return S.float().contiguous().to(device), L.float().contiguous().to(device)
 
 
+def make_paths(topk_idx: torch.Tensor, topk_w: torch.Tensor):
+    """Synthetic composed paths from a routing (a path router is trained, out
+    of scope): a token's selected units in slot order are the targets; even
+    slots are their own source, odd slots take the previous slot's unit as
+    source, so consecutive paths share an expansion; the path weight is the
+    unit's gate weight.  Returns (src_idx, tgt_idx, beta), -1 / 0 after k_t
+    (slots past k_t are -1 in topk_idx)."""
+    tgt = topk_idx.clone()
+    src = topk_idx.clone()
+    src[:, 1::2] = topk_idx[:, 0:-1:2] if topk_idx.shape[1] % 2 == 0 else topk_idx[:, 0:-2:2]
+    src = torch.where(tgt >= 0, src, torch.full_like(src, -1))
+    beta = torch.where(tgt >= 0, topk_w, torch.zeros_like(topk_w))
+    return src.contiguous(), tgt.contiguous(), beta.contiguous()
+
+
 def make_logits(T: int, E_r: int, device="cpu", seed: int = 7, kind: str = "normal"):
     """Float32 logits for routing-only tests.
 

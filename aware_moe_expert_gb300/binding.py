@@ -32,7 +32,7 @@ EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_gate_up", "moe
            "moe_get_device_status", "moe_status_string", "moe_permute_static",
            "moe_cg_workspace_size", "moe_pack_proxy_rows", "moe_route_cg",
            "moe_layer_forward_cg", "moe_fold_decode", "moe_layer_forward_fold",
-           "moe_cost_lookup", "moe_tier_schedule")
+           "moe_cost_lookup", "moe_tier_schedule", "moe_layer_forward_paths")
 
 
 class MoeLayerDesc(ctypes.Structure):
@@ -113,6 +113,8 @@ def lib() -> ctypes.CDLL:
             "moe_tier_schedule": (ctypes.c_int32, [ctypes.POINTER(MoeTierRequest), ctypes.c_int32,
                                                    ctypes.c_int32, ctypes.POINTER(MoeCostTable),
                                                    vp, vp, vp, ctypes.c_int32]),
+            "moe_layer_forward_paths": (ctypes.c_int, [D, vp, vp, vp, i32p, i32p, vp, i32p, vp,
+                                                       i32p, vp, vp]),
             "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         }
         for name, (res, args) in sig.items():
@@ -389,6 +391,15 @@ def moe_tier_schedule(requests, M: int, table: CostTable):
     if nb < 0:
         raise MoeError(1, f"moe_tier_schedule returned {nb}")
     return batch_of[:n].tolist(), bk[:nb].tolist(), bt[:nb].tolist()
+
+
+def moe_layer_forward_paths(desc, x, w_gate_up, w_down, src_idx, tgt_idx, beta, n_paths, out,
+                            dev_status, workspace, stream=None) -> int:
+    d = desc.c()
+    return lib().moe_layer_forward_paths(ctypes.byref(d), _ptr(x), _ptr(w_gate_up), _ptr(w_down),
+                                         _ptr(src_idx), _ptr(tgt_idx), _ptr(beta),
+                                         _ptr(n_paths), _ptr(out), _ptr(dev_status),
+                                         _ptr(workspace), _stream(stream))
 
 
 def moe_get_device_status(dev_status, stream=None) -> int:

@@ -19,7 +19,7 @@ OUT = os.path.join(PKG, "libmoe.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
 SOURCES = ["api.cu", "route.cu", "permute.cu", "gemm.cu", "gemm_decode.cu", "ffn_decode.cu",
            "combine.cu", "noalloc.cu", "gemm_pair.cu", "cg_router.cu", "fold.cu",
-           "scheduler.cpp"]
+           "paths.cu", "scheduler.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include")]

@@ -24,7 +24,8 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 struct Layout {
   size_t logits, router_partial, topk_idx, topk_w, counts, offsets, sorted_token, inv_row, bitmap,
       wprefix, xperm, act, yperm, act_sh, ysh, split_word, partial, chunk_done, ffn_part,
-      fold_ws, fold_idx, fold_w, fold_k, total;
+      fold_ws, fold_idx, fold_w, fold_k, p_srcs, p_nsrc, p_slot, p_counts, p_offsets, p_sorted,
+      p_inv, p_row, p_act, total;
   int router_slices;   // slices of the CUDA-core router (0: the tensor-core router runs)
   int max_split;       // K splits the decode gate|up kernel may use (1: none)
   int max_split_down;  // K splits the decode down kernel may use
@@ -112,6 +113,18 @@ Layout layout_of(const moe_layer_desc& d) {
   l.fold_idx = take(n_cap * 4);
   l.fold_w = take(n_cap * 4);
   l.fold_k = take(T * 4);
+  // path-composed execution: unique sources, their permutation, the
+  // expansion row of every path, and the path-ordered expansion rows (in the
+  // permuted-x region when it is wide enough: x_perm is free by then)
+  l.p_srcs = take(n_cap * 4);
+  l.p_nsrc = take(T * 4);
+  l.p_slot = take(n_cap * 4);
+  l.p_counts = take(E_r * 4);
+  l.p_offsets = take((E_r + 1) * 4);
+  l.p_sorted = take(n_cap * 4);
+  l.p_inv = take(n_cap * 4);
+  l.p_row = take(n_cap * 4);
+  l.p_act = d.I_sub <= d.H ? l.xperm : take(n_cap * d.I_sub * 2);
   l.total = o;
   return l;
 }
@@ -532,6 +545,49 @@ moe_status do_fold(const moe_layer_desc* d, const moe_fold_desc* f, const int32_
                                              status, s));
 }
 
+// ---------------------------------------------------------------- composed paths
+
+moe_status do_layer_paths(const moe_layer_desc* d, const void* x, const void* w_gate_up,
+                          const void* w_down, const int32_t* src_idx, const int32_t* tgt_idx,
+                          const float* beta, const int32_t* n_paths, void* out,
+                          int32_t* status, void* ws, cudaStream_t s) {
+  const Layout l = layout_of(*d);
+  const int E_r = E_r_of(d);
+  const long long n_cap = static_cast<long long>(d->T) * d->k_max;
+  int32_t* srcs = at<int32_t>(ws, l.p_srcs);
+  int32_t* nsrc = at<int32_t>(ws, l.p_nsrc);
+  int32_t* slot = at<int32_t>(ws, l.p_slot);
+  int32_t* offs_s = at<int32_t>(ws, l.p_offsets);
+  int32_t* sorted_s = at<int32_t>(ws, l.p_sorted);
+  int32_t* inv_s = at<int32_t>(ws, l.p_inv);
+  int32_t* counts = at<int32_t>(ws, l.counts);
+  int32_t* offsets = at<int32_t>(ws, l.offsets);
+  int32_t* sorted_token = at<int32_t>(ws, l.sorted_token);
+  int32_t* inv_row = at<int32_t>(ws, l.inv_row);
+  int32_t* row_of = at<int32_t>(ws, l.p_row);
+  void* act_s = at<void>(ws, l.act);
+  void* act_p = at<void>(ws, l.p_act);
+  void* yperm = at<void>(ws, l.yperm);
+  // expansions: one per (token, distinct source)
+  MOE_TRY(cuda_status(moe::launch_paths_sources(src_idx, n_paths, d->T, d->k_max, E_r, srcs,
+                                                nsrc, slot, status, s)));
+  MOE_TRY(do_permute(d, srcs, nsrc, at<int32_t>(ws, l.p_counts), offs_s, sorted_s, inv_s, status,
+                     ws, s));
+  MOE_TRY(do_gate_up(d, x, sorted_s, offs_s, w_gate_up, act_s, status, ws, s));
+  // projections: one per path, grouped by target, reading its source's row
+  MOE_TRY(do_permute(d, tgt_idx, n_paths, counts, offsets, sorted_token, inv_row, status, ws, s));
+  MOE_TRY(cuda_status(moe::launch_paths_rows(n_paths, slot, inv_s, inv_row, d->T, d->k_max,
+                                             row_of, s)));
+  MOE_TRY(cuda_status(moe::launch_gather_rows(act_s, row_of, offsets, E_r,
+                                              static_cast<int>(n_cap), d->I_sub,
+                                              static_cast<int>(n_cap), act_p, status, sm_count(),
+                                              s)));
+  MOE_TRY(do_down(d, act_p, offsets, w_down, yperm, status, ws, s));
+  void* ysh = d->I_shared > 0 ? at<void>(ws, l.ysh) : nullptr;
+  if (ysh != nullptr) MOE_TRY(do_shared(d, x, ysh, status, ws, s));
+  return do_combine(d, yperm, ysh, inv_row, beta, n_paths, out, status, s);
+}
+
 // ---------------------------------------------------------------- proxy router
 
 moe_status validate_cg(const moe_layer_desc* d, const moe_cg_router* cg) {
@@ -907,6 +963,21 @@ moe_status moe_layer_forward_fold(const moe_layer_desc* desc, const moe_fold_des
   MOE_TRY(do_grouped_ffn(desc, x, sorted_token, offsets, w_gate_up, w_down, yperm, dev_status,
                          workspace, s));
   return do_combine(desc, yperm, ysh, inv_row, fw, fk, out, dev_status, s);
+}
+
+moe_status moe_layer_forward_paths(const moe_layer_desc* desc, const void* x,
+                                   const void* w_gate_up, const void* w_down,
+                                   const int32_t* src_idx, const int32_t* tgt_idx,
+                                   const float* beta, const int32_t* n_paths, void* out,
+                                   int32_t* dev_status, void* workspace, void* stream) {
+  MOE_TRY(validate(desc));
+  if (desc->T == 0) return MOE_OK;
+  if (desc->I_sub % 8 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  MOE_TRY(check_ptrs({x, w_gate_up, w_down, out}));
+  MOE_TRY(check_ptrs4({src_idx, tgt_idx, beta, n_paths, dev_status}));
+  MOE_TRY(check_ws(workspace));
+  return do_layer_paths(desc, x, w_gate_up, w_down, src_idx, tgt_idx, beta, n_paths, out,
+                        dev_status, workspace, static_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_get_device_status(const int32_t* dev_status, void* stream) {

@@ -73,6 +73,17 @@ cudaError_t launch_fold_decode(const int32_t* topk_idx, const float* topk_w,
                                const float* L, int32_t* idx_out, float* w_out, int32_t* k_out,
                                int32_t* pool_out, void* ws, int32_t* status, cudaStream_t s);
 
+// ---- paths.cu: path-composed execution
+// Distinct sources per token (first-occurrence order), their count, and each
+// path's source position (all [T, k_max] / [T]).
+cudaError_t launch_paths_sources(const int32_t* src_idx, const int32_t* n_paths, int T, int k_max,
+                                 int E_r, int32_t* srcs, int32_t* n_src, int32_t* slot,
+                                 int32_t* status, cudaStream_t s);
+// row_of[target-sorted position of path (t, j)] = source-sorted row of its expansion
+cudaError_t launch_paths_rows(const int32_t* n_paths, const int32_t* slot, const int32_t* inv_src,
+                              const int32_t* inv_tgt, int T, int k_max, int32_t* row_of,
+                              cudaStream_t s);
+
 // ---- permute.cu
 cudaError_t launch_permute(const int32_t* topk_idx, const int32_t* k_per_token, int T,
                            int k_max, int E_r, uint32_t* bitmap, int32_t* wprefix,

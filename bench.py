@@ -62,6 +62,10 @@ def parse():
                         "synthetic request queue batched FIFO at the batch-max budget, by "
                         "quality tiers (Eq. 5) at the batch-max budget, and FIFO at every "
                         "request's own budget")
+    p.add_argument("--paths", action="store_true",
+                   help="path-composed execution with source-grouped reuse: time "
+                        "moe_layer_forward_paths on the seeded path recipe against the same "
+                        "pipeline with diagonal paths and against moe_layer_forward")
     p.add_argument("--force-pair", action="store_true",
                    help="run grouped prefill GEMMs on the CTA-pair kernel (debug flag)")
     return p.parse_args()
@@ -737,6 +741,91 @@ def run_tiered(args, wl, rank, world, local):
     }
 
 
+def run_paths(args, wl, rank, world, local):
+    """Path-composed execution (each path = expansion of a source unit, then
+    projection of a target unit; paths of a token that share a source share
+    one expansion).  Paths come from the layer's own routing through the
+    seeded recipe of the input generator (consecutive slots share a source).
+    Three CUDA graphs, timed the same way as the main bench: composed paths,
+    the same pipeline with diagonal paths (every path its own source), and
+    moe_layer_forward (routing included there, excluded from the other two)."""
+    import torch
+    from aware_moe_expert_gb300 import binding as B
+    from aware_moe_expert_gb300.inputs import make_layer_inputs, make_paths
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    d = make_layer_inputs(wl, dev, seed=wl.seed + 1000 * rank)
+    desc = B.desc_for(wl, expert_bias=d["expert_bias"], w_shared_gate_up=d.get("w_shared_gate_up"),
+                      w_shared_down=d.get("w_shared_down"))
+    T, H, k_max = wl.T, wl.H, wl.k_max
+    ws = torch.empty(B.moe_workspace_size(desc), dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    idx = torch.empty(T, k_max, dtype=torch.int32, device=dev)
+    w = torch.empty(T, k_max, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    B.check(B.moe_route(desc, d["x"], d["router_w"], None, d["k_per_token"], None, idx, w, st, ws,
+                        stream.cuda_stream))
+    torch.cuda.synchronize(dev)
+    src, tgt, beta = make_paths(idx, w)
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    kk = d["k_per_token"]
+
+    def f_paths(sp, s_=src):
+        B.check(B.moe_layer_forward_paths(desc, d["x"], d["w_gate_up"], d["w_down"], s_, tgt,
+                                          beta, kk, out, st, ws, sp), "moe_layer_forward_paths")
+
+    def f_diag(sp):
+        f_paths(sp, tgt)
+
+    def f_layer(sp):
+        B.check(B.moe_layer_forward(desc, d["x"], d["router_w"], d["w_gate_up"], d["w_down"], kk,
+                                    out, st, ws, sp), "moe_layer_forward")
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+    res = {}
+    for name, fn in (("paths", f_paths), ("diagonal_paths", f_diag), ("layer", f_layer)):
+        with torch.cuda.stream(stream):
+            fn(stream.cuda_stream)
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+            fn(torch.cuda.current_stream().cuda_stream)
+        evs = []
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup + args.steps):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+                if i >= args.warmup:
+                    evs.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        res[name] = float(np.mean([a.elapsed_time(b) for a, b in evs])) * 1000.0
+        del g
+    if B.moe_get_device_status(st) != 0:
+        raise RuntimeError("device status after the path runs")
+    srcs = src.cpu().numpy()
+    kn = kk.cpu().numpy()
+    n_exp = int(sum(len(set(srcs[t, :kn[t]].tolist())) for t in range(T)))
+    n_paths = int(kn.sum())
+    unit = "µs/layer" if wl.phase == "decode" else "tokens/s"
+    val = (lambda us: round(us, 2)) if wl.phase == "decode" else \
+        (lambda us: round(T / (us * 1e-6), 1))
+    return {"metric": "path-composed MoE layer with source-grouped reuse", "unit": unit,
+            "higher_is_better": wl.phase != "decode", "n_gpus": world, "dtype": "bf16",
+            "data": "synthetic", "steps": args.steps, "warmup": args.warmup,
+            "config": {"workload": wl.name, "T": T,
+                       "paths": "seeded recipe: consecutive slots share a source"},
+            "value": val(res["paths"]),
+            "diagonal_paths": val(res["diagonal_paths"]),
+            "plain_layer_with_routing": val(res["layer"]),
+            "us": {k: round(v, 2) for k, v in res.items()},
+            "expansions": n_exp, "paths": n_paths,
+            "expansion_flops_saved": 4.0 * H * wl.I_sub * (n_paths - n_exp)}
+
+
 def main():
     args = parse()
     from aware_moe_expert_gb300 import workloads as WL
@@ -749,8 +838,8 @@ def main():
         if res is not None:
             print(json.dumps(res), flush=True)
         return
-    if args.tiered:
-        res = run_tiered(args, wl, rank, world, local)
+    if args.tiered or args.paths:
+        res = (run_tiered if args.tiered else run_paths)(args, wl, rank, world, local)
         if rank == 0:
             print(json.dumps(res), flush=True)
         return

@@ -230,6 +230,30 @@ moe_status moe_layer_forward_fold(const moe_layer_desc* desc, const moe_fold_des
                                   int32_t* dev_status, void* workspace, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Path-composed execution with source-grouped reuse ("PCoMoE: Shifting MoE
+ * Inference from Monolithic Expert Selection to Fine-Grained Path
+ * Composition", arXiv 2609.01024, "Source-Grouped Compute Reuse", Fig. 8).
+ * A SwiGLU unit splits into an expansion U_u(h) = SiLU(h Wg_u) * (h Wu_u)
+ * and a projection D_u(z) = z Wd_u; a path (i, j) is D_j(U_i(h)), and
+ *     out_t = sum_{j < n_paths[t]} beta[t,j] * D_{tgt[t,j]}(U_{src[t,j]}(x_t))
+ *             (+ the shared expert, weight 1, when desc->I_shared > 0),
+ * with U_i evaluated once per distinct source of a token (paths listed in
+ * slot order; diagonal paths i == j are the plain layer).
+ *   src_idx, tgt_idx  int32 [T, k_max]: units of each path's expansion and
+ *                     projection; a token's targets must be distinct
+ *                     (MOE_ERR_BAD_INDEX otherwise), its sources may repeat
+ *   beta              fp32 [T, k_max]: path weights
+ *   n_paths           int32 [T], each in [1, k_max]
+ *   out               bf16 [T, H]
+ * Path selection (a learned compatibility bias) is the caller's.  Workspace:
+ * moe_workspace_size(desc) bytes.  Requires I_sub % 8 == 0. */
+moe_status moe_layer_forward_paths(const moe_layer_desc* desc, const void* x,
+                                   const void* w_gate_up, const void* w_down,
+                                   const int32_t* src_idx, const int32_t* tgt_idx,
+                                   const float* beta, const int32_t* n_paths, void* out,
+                                   int32_t* dev_status, void* workspace, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Quality-tiered batching (host only; MoE-Prism §III-C2 "Temporal Separation
  * via Quality-Tiered Batching", Eq. (5)).  For dispatches that run a whole
  * batch at one budget (the batch maximum), requests are grouped by budget:

@@ -72,9 +72,11 @@ def unique_sources(src_idx: np.ndarray, n_paths: Sequence[int]):
 
 def paths_forward(x: np.ndarray, w_gate_up: Callable[[int], np.ndarray],
                   w_down: Callable[[int], np.ndarray], src_idx: np.ndarray,
-                  tgt_idx: np.ndarray, beta: np.ndarray, n_paths: Sequence[int]):
+                  tgt_idx: np.ndarray, beta: np.ndarray, n_paths: Sequence[int],
+                  w_shared_gate_up=None, w_shared_down=None):
     """Source-grouped execution: one expansion per (token, unique source),
-    one projection per path.  Returns (out [T, H], expansions evaluated)."""
+    one projection per path, plus a shared expert with weight 1 when given.
+    Returns (out [T, H], expansions evaluated)."""
     T = x.shape[0]
     srcs, n_src, slot = unique_sources(src_idx, n_paths)
     out = np.zeros((T, x.shape[1]))      # the projection maps back to H
@@ -85,4 +87,6 @@ def paths_forward(x: np.ndarray, w_gate_up: Callable[[int], np.ndarray],
         for j in range(int(n_paths[t])):
             out[t] += float(beta[t, j]) * projection(z[int(slot[t, j])],
                                                      w_down(int(tgt_idx[t, j])))[0]
+    if w_shared_gate_up is not None:
+        out += projection(expansion(x, w_shared_gate_up), w_shared_down)
     return out, n_exp

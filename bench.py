@@ -516,9 +516,9 @@ def launches_per_step(wl, T, path=0, fold=False):
     """Kernels libmoe enqueues per moe_layer_forward (mirrors the host
     sequencing in csrc/api.cu: router + top-k (one cluster launch on CUDA
     cores, or the tensor-core GEMM and the top-k kernel), permutation (fused
-    into the router launch for <= 8 tokens), [shared expert], gate|up (+ the
-    split-K reduction of the weight-stationary family), down (+ its split
-    reduction), combine)."""
+    into the router launch for <= 8 tokens), [folding], [shared expert],
+    gate|up (+ the split-K reduction of the weight-stationary family), down
+    (+ its split reduction), combine)."""
     n_cap = T * wl.k_max
     decode = path == 2 or (path == 0 and n_cap <= 64 * wl.E_r)
     budget = 256 << 20
@@ -531,12 +531,14 @@ def launches_per_step(wl, T, path=0, fold=False):
     else:
         n = 1 if cluster_router else 2               # logits (+ top-k)
         n += 1 if (T + 31) // 32 <= 8 else 3        # permutation (one CTA, or bitmap/scan/scatter)
-    n += 3 if fold else 0                            # fold: scores, pool, remap
+    n += 4 if fold else 0                            # fold: scores, pool, target map, remap
     n += 2 if wl.I_shared else 0                     # shared expert gate|up, down
     if decode_ffn:
         n += 1 if fused_front else 2                 # (row gather +) fused decode FFN kernel
     else:
-        n += 2                                       # row gather + gate|up GEMM
+        # gate|up GEMM; the decode family reads a gathered copy of x, the
+        # prefill kernel gathers its rows itself
+        n += 2 if decode else 1
         if decode and wl.I_sub % 64 == 0:
             n += 1 if budget // max(n_cap * 2 * wl.I_sub * 4, 1) >= 2 else 0
         n += 1                                       # down GEMM

@@ -73,6 +73,29 @@ def draw_k(wl: Workload, device="cpu", seed: Optional[int] = None) -> torch.Tens
     return k.to(torch.int32).contiguous().to(device)
 
 
+def draw_k_normal(T: int, mu: float, sigma: float, k_max: int, seed: int = 7,
+                  device="cpu") -> torch.Tensor:
+    """Budgets k = clip(round(x), 1, k_max), x ~ N(mu, sigma^2), one draw per
+    token: the k-target generator of MoE-Prism §IV-B2, Eq. (7)."""
+    g = torch.Generator().manual_seed(seed)
+    x = mu + sigma * torch.randn(T, generator=g, dtype=torch.float64)
+    return torch.round(x).clamp_(1, k_max).to(torch.int32).contiguous().to(device)
+
+
+def apply_k_mode(k: torch.Tensor, mode: str, n_sub: int, k_max: int) -> torch.Tensor:
+    """Budgets actually executed in a comparison mode:
+    "exact" every token its own k; "batch_max" every token the batch maximum
+    (what a uniform-k grouped kernel runs, MoE-Prism §III-C1); "coarse"
+    n_sub * ceil(k / n_sub) (whole experts, MoE-Prism §V-D1), at most k_max."""
+    if mode == "exact":
+        return k
+    if mode == "batch_max":
+        return torch.full_like(k, int(k.max().item()))
+    if mode == "coarse":
+        return torch.clamp(((k + n_sub - 1) // n_sub) * n_sub, max=k_max).to(k.dtype)
+    raise ValueError(f"unknown k mode {mode!r}")
+
+
 def draw_bias(wl: Workload, seed: Optional[int] = None) -> Optional[torch.Tensor]:
     seed = wl.seed if seed is None else seed
     g = _gen(seed, "bias", "cpu")

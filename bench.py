@@ -55,6 +55,12 @@ def parse():
                    help="linear: the expanded linear gate over all units (the default); "
                         "cg: the training-free proxy router (original router + gate neurons)")
     p.add_argument("--cg-r", type=int, default=8, help="gate neurons per sub-expert (--router cg)")
+    p.add_argument("--k-mode", default="exact", choices=["exact", "batch_max", "coarse"],
+                   help="budgets executed: each token's own (exact), the batch maximum for every "
+                        "token (what uniform-k kernels run), or whole experts n_sub*ceil(k/n_sub)")
+    p.add_argument("--k-normal", default=None,
+                   help="MU,SIGMA: draw budgets k = clip(round(N(MU, SIGMA^2)), 1, k_max) per "
+                        "token instead of the workload's uniform draw")
     p.add_argument("--fold", type=int, default=0,
                    help="decode expert-pool folding to a dynamic pool of D units (0: off)")
     p.add_argument("--tiered", action="store_true",
@@ -172,6 +178,13 @@ def run_ours(args, wl, rank, world, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     d = make_layer_inputs(wl, dev, seed=wl.seed + 1000 * rank)
+    if args.k_normal is not None:
+        from aware_moe_expert_gb300.inputs import draw_k_normal
+        mu, sigma = (float(v) for v in args.k_normal.split(","))
+        d["k_per_token"] = draw_k_normal(wl.T, mu, sigma, wl.k_max, seed=wl.seed + 9, device=dev)
+    if args.k_mode != "exact":
+        from aware_moe_expert_gb300.inputs import apply_k_mode
+        d["k_per_token"] = apply_k_mode(d["k_per_token"], args.k_mode, wl.n_sub, wl.k_max)
     desc = B.desc_for(wl, expert_bias=d["expert_bias"], w_shared_gate_up=d.get("w_shared_gate_up"),
                       w_shared_down=d.get("w_shared_down"))
     desc.path = args.path
@@ -482,6 +495,7 @@ def run_ours(args, wl, rank, world, local):
     res["config"] = {"workload": wl.name, "T": T, "H": H, "experts": wl.n_experts,
                      "n_sub": wl.n_sub, "E_r": E_r, "I_sub": I_sub, "I_shared": wl.I_shared,
                      "k_choices": list(wl.k_choices), "k_per": wl.k_per, "score": wl.score,
+                     "k_mode": args.k_mode, "k_normal": args.k_normal,
                      "parallelism": f"replicas{world}",
                      "fold": (None if fold is None else
                               f"decode expert-pool folding: dynamic pool of {args.fold} units, "

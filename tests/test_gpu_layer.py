@@ -163,3 +163,25 @@ def test_layer_forward_equals_component_calls(name, T):
     B.check(B.moe_combine(desc, y, None, inv, w, d["k_per_token"], out2, st))
     assert B.moe_get_device_status(st) == 0
     assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+
+
+@pytest.mark.parametrize("mode", ["batch_max", "coarse"])
+@pytest.mark.parametrize("name,T", [("tiny", None), ("qwen_decode", 64)])
+def test_layer_comparison_budget_modes(name, T, mode):
+    """The comparison modes run the same kernels on other budgets: every token
+    at the batch maximum (uniform-k execution) or at whole experts
+    n_sub * ceil(k / n_sub); the layer still matches the oracle."""
+    from aware_moe_expert_gb300.inputs import apply_k_mode
+    wl = WL.ALL[name] if T is None else WL.ALL[name].with_T(T)
+    d = make_layer_inputs(wl, DEV)
+    d["k_per_token"] = apply_k_mode(d["k_per_token"], mode, wl.n_sub, wl.k_max)
+    desc = B.desc_for(wl, expert_bias=d["expert_bias"])
+    layer = B.MoeLayer(desc, DEV)
+    out = layer.forward(d["x"], d["router_w"], d["w_gate_up"], d["w_down"], d["k_per_token"])
+    assert layer.device_status() == 0
+    Lg = torch.empty(wl.T, wl.E_r, dtype=torch.float32, device=DEV)
+    idx = torch.empty(wl.T, wl.k_max, dtype=torch.int32, device=DEV)
+    w = torch.empty(wl.T, wl.k_max, dtype=torch.float32, device=DEV)
+    B.check(B.moe_route(desc, d["x"], d["router_w"], None, d["k_per_token"], Lg, idx, w,
+                        layer.status, layer.workspace))
+    _compare(wl, d, desc, out, Lg, idx, np.arange(wl.T))

@@ -459,3 +459,18 @@ def test_distinct_units_counts_nonzero_units():
     idx = np.array([[2, 0, -1], [2, 5, 1]], dtype=np.int32)
     counts, *_ = O.permute(idx, [2, 3], 6)
     assert O.distinct_units(counts) == 4
+
+
+def test_budget_generators_and_modes():
+    """Eq. (7) draws stay in [1, k_max] and follow the mean; the comparison
+    modes give the batch maximum everywhere, or n_sub * ceil(k / n_sub)."""
+    import torch
+    from aware_moe_expert_gb300.inputs import apply_k_mode, draw_k_normal
+    k = draw_k_normal(20000, 6.0, 2.0, 8, seed=3)
+    assert int(k.min()) >= 1 and int(k.max()) <= 8
+    assert abs(float(k.double().mean()) - 5.85) < 0.1   # E[clip(round(N(6,4)),1,8)] ~ 5.85
+    base = torch.tensor([1, 2, 3, 4, 5, 7, 8], dtype=torch.int32)
+    assert apply_k_mode(base, "batch_max", 4, 8).tolist() == [8] * 7
+    assert apply_k_mode(base, "coarse", 4, 8).tolist() == [4, 4, 4, 4, 8, 8, 8]
+    assert apply_k_mode(base, "coarse", 2, 7).tolist() == [2, 2, 4, 4, 6, 7, 7]
+    assert [O.coarse_k(int(v), 4) for v in base] == [4, 4, 4, 4, 8, 8, 8]

@@ -31,22 +31,33 @@ __global__ void __launch_bounds__(256) combine_kernel(
   const int t = static_cast<int>(gid / nv);
   const int v = static_cast<int>(gid - static_cast<long long>(t) * nv);
   if (t >= T) return;
-  const int k = min(max(kpt[t], 0), k_max);
   const int32_t* ir = inv_row + static_cast<size_t>(t) * k_max;
   const float* tw = topk_w + static_cast<size_t>(t) * k_max;
+  // the first four slots' indices are loaded with k_t (slots past k_t are
+  // read but not used), so the row loads wait for one round trip, not two
+  int r[4];
+  float w[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    r[q] = q < k_max ? __ldg(ir + q) : -1;
+    w[q] = q < k_max ? __ldg(tw + q) : 0.f;
+  }
+  const int k = min(max(kpt[t], 0), k_max);
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
   bool bad = false;
   for (int j0 = 0; j0 < k; j0 += 4) {
-    int r[4];
-    float w[4];
     uint4 y[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int j = j0 + q;
-      r[q] = j < k ? __ldg(ir + j) : -1;
-      w[q] = j < k ? __ldg(tw + j) : 0.f;
+      if (j0 > 0) {
+        r[q] = j < k ? __ldg(ir + j) : -1;
+        w[q] = j < k ? __ldg(tw + j) : 0.f;
+      } else if (j >= k) {
+        r[q] = -1;
+      }
       if (j < k && (r[q] < 0 || r[q] >= n_rows)) {
         bad = true;
         r[q] = -1;

@@ -121,8 +121,8 @@ __global__ void __launch_bounds__(GATHER ? kThreads + kGatherThreads : kThreads,
   int* s_offs = reinterpret_cast<int*>(smem + C::kOffOffs);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  pdl_wait_and_trigger();
-
+  // set-up that reads nothing written upstream runs before the grid
+  // dependency wait, overlapping the previous kernel's tail
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       // GATHER: the producer's arrive (B bytes) plus one cp.async arrive per gather thread
@@ -142,12 +142,13 @@ __global__ void __launch_bounds__(GATHER ? kThreads + kGatherThreads : kThreads,
     tma_prefetch_desc(&tmB);
     if (EPI != EPI_F32) tma_prefetch_desc(&tmOut);
   }
-  if (warp == 2) build_tile_table(p.offsets, p.n_groups, p.dense_rows, p.out_rows, s_prefix, s_offs,
-                                  s_total, p.status, lane);
   if (warp == 1) {
     tmem_alloc(s_tmem, C::kTmemCols);
     tmem_relinquish();
   }
+  pdl_wait_and_trigger();
+  if (warp == 2) build_tile_table(p.offsets, p.n_groups, p.dense_rows, p.out_rows, s_prefix, s_offs,
+                                  s_total, p.status, lane);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

@@ -134,8 +134,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* s_offs = reinterpret_cast<int*>(smem + C::kOffOffs);
   float* s_xchg = reinterpret_cast<float*>(smem + C::kOffX);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  pdl_wait_and_trigger();
-
+  // set-up that reads nothing written upstream runs before the grid
+  // dependency wait, overlapping the previous kernel's tail
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
@@ -154,13 +154,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmX);
     tma_prefetch_desc(&tmX64);
   }
-  if (warp == 2)
-    build_tile_table<CHUNK>(p.offsets, p.n_groups, 0, p.out_rows, s_prefix, s_offs, s_total,
-                             p.status, lane);
   if (warp == 1) {
     tmem_alloc(s_tmem, kTmemCols);
     tmem_relinquish();
   }
+  pdl_wait_and_trigger();
+  if (warp == 2)
+    build_tile_table<CHUNK>(p.offsets, p.n_groups, 0, p.out_rows, s_prefix, s_offs, s_total,
+                             p.status, lane);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

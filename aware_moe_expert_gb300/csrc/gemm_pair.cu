@@ -116,7 +116,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
-  pdl_wait_and_trigger();
+  // set-up that reads nothing written upstream runs before the grid
+  // dependency wait, overlapping the previous kernel's tail
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -136,13 +137,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmOut);
   }
-  if (warp == 2)
-    build_tile_table<2 * BM>(p.offsets, p.n_groups, p.dense_rows, p.out_rows, s_prefix, s_offs,
-                             s_total, p.status, lane);
   if (warp == 1) {
     tmem_alloc_pair(s_tmem, kTmemCols);
     tmem_relinquish_pair();
   }
+  pdl_wait_and_trigger();
+  if (warp == 2)
+    build_tile_table<2 * BM>(p.offsets, p.n_groups, p.dense_rows, p.out_rows, s_prefix, s_offs,
+                             s_total, p.status, lane);
   tc_fence_before();
   __syncthreads();
   cluster_sync_all();

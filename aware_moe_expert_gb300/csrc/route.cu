@@ -110,68 +110,70 @@ __device__ __forceinline__ float key_to_logit(uint32_t key) {
   return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
 }
 
+// Descending compare-exchange of two packed (key << 32 | ~unit) entries.
+__device__ __forceinline__ void cas_desc(unsigned long long& a, unsigned long long& b) {
+  const unsigned long long hi = a > b ? a : b, lo = a > b ? b : a;
+  a = hi;
+  b = lo;
+}
+
+// Sorts a lane's IPL entries in descending order (Batcher's odd-even merge
+// networks for 2, 4 and 8 entries: 1, 5 and 19 compare-exchanges).
+template <int IPL>
+__device__ __forceinline__ void lane_sort_desc(unsigned long long (&e)[IPL]) {
+  if constexpr (IPL == 2) {
+    cas_desc(e[0], e[1]);
+  } else if constexpr (IPL == 4) {
+    cas_desc(e[0], e[1]); cas_desc(e[2], e[3]);
+    cas_desc(e[0], e[2]); cas_desc(e[1], e[3]);
+    cas_desc(e[1], e[2]);
+  } else if constexpr (IPL == 8) {
+    cas_desc(e[0], e[1]); cas_desc(e[2], e[3]); cas_desc(e[4], e[5]); cas_desc(e[6], e[7]);
+    cas_desc(e[0], e[2]); cas_desc(e[1], e[3]); cas_desc(e[4], e[6]); cas_desc(e[5], e[7]);
+    cas_desc(e[1], e[2]); cas_desc(e[5], e[6]);
+    cas_desc(e[0], e[4]); cas_desc(e[1], e[5]); cas_desc(e[2], e[6]); cas_desc(e[3], e[7]);
+    cas_desc(e[2], e[4]); cas_desc(e[3], e[5]);
+    cas_desc(e[1], e[2]); cas_desc(e[3], e[4]); cas_desc(e[5], e[6]);
+  } else {
+    static_assert(IPL == 1, "IPL is 1, 2, 4 or 8");
+  }
+}
+
 // The k best of the 32 * IPL units a warp holds (lane l holds units l,
 // l + 32, ...; key[i] = order_key of unit lane + 32 i, units >= E_r absent),
 // best first, ties to the lower index.  Lane j < k returns
-// (key << 32) | ~u of the j-th unit; other lanes return 0.  buf: 32 words of
-// this warp's shared memory.
+// (key << 32) | ~u of the j-th unit; other lanes return 0.
 //
-// 1. Radix select of the k-th largest key: bit by bit from the top, keep the
-//    candidate threshold if at least k keys reach it (ballot counts; stops
-//    early once exactly k do).
-// 2. Every unit above the threshold is selected, plus the lowest-index units
-//    equal to it until k are taken.
-// 3. The k selected units are packed into buf, each lane j < k counts the
-//    selected units that order before its own (its rank), and the units are
-//    stored back at their ranks.
+// Every unit is packed as (key << 32) | ~u, so the packed order is the
+// selection order (larger key first, then lower index); absent units pack
+// as 0, below every unit.  Each lane sorts its entries; then k rounds take
+// the warp's largest head (two 32-bit warp max reductions: key, then ~u among
+// the heads with that key) and the lane that held it drops its head.
 template <int IPL>
 __device__ __forceinline__ unsigned long long warp_select_topk(const uint32_t (&key)[IPL],
-                                                               int E_r, int k, int lane,
-                                                               unsigned long long* buf) {
-  if (k <= 0) return 0ull;
-  uint32_t thr = 0u;
-  int at_thr = E_r;   // units with key >= thr
-  for (int b = 31; b >= 0 && at_thr != k; --b) {
-    const uint32_t cand = thr | (1u << b);
-    int c = 0;
-#pragma unroll
-    for (int i = 0; i < IPL; ++i) c += __popc(__ballot_sync(0xffffffffu, key[i] >= cand));
-    if (c >= k) {
-      thr = cand;
-      at_thr = c;
-    }
-  }
-  int above = 0;
-#pragma unroll
-  for (int i = 0; i < IPL; ++i) above += __popc(__ballot_sync(0xffffffffu, key[i] > thr));
-  const int need = k - above;   // units taken from those equal to thr
-  const uint32_t lt = (1u << lane) - 1u;
-  int taken_eq = 0, packed = 0;
+                                                               int E_r, int k, int lane) {
+  unsigned long long e[IPL];
 #pragma unroll
   for (int i = 0; i < IPL; ++i) {
     const int u = lane + 32 * i;
-    const bool eq = u < E_r && key[i] == thr;
-    const uint32_t meq = __ballot_sync(0xffffffffu, eq);
-    const bool sel = key[i] > thr || (eq && taken_eq + __popc(meq & lt) < need);
-    taken_eq += __popc(meq);
-    const uint32_t msel = __ballot_sync(0xffffffffu, sel);
-    if (sel)
-      buf[packed + __popc(msel & lt)] =
-          (static_cast<unsigned long long>(key[i]) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(u));
-    packed += __popc(msel);
+    e[i] = u < E_r ? (static_cast<unsigned long long>(key[i]) << 32) |
+                         static_cast<uint32_t>(~static_cast<uint32_t>(u))
+                   : 0ull;
   }
-  __syncwarp();
-  unsigned long long mine = 0ull;
-  int rank = 0;
-  if (lane < k) {
-    mine = buf[lane];
-    for (int m = 0; m < k; ++m) rank += buf[m] > mine ? 1 : 0;
+  lane_sort_desc<IPL>(e);
+  unsigned long long best = 0ull;
+  for (int j = 0; j < k; ++j) {
+    const uint32_t hk = static_cast<uint32_t>(e[0] >> 32);
+    const uint32_t mk = __reduce_max_sync(0xffffffffu, hk);
+    const uint32_t lo = hk == mk ? static_cast<uint32_t>(e[0]) : 0u;
+    const uint32_t ml = __reduce_max_sync(0xffffffffu, lo);
+    const unsigned long long win = (static_cast<unsigned long long>(mk) << 32) | ml;
+    if (lane == j) best = win;
+    const bool pop = e[0] == win;
+#pragma unroll
+    for (int i = 0; i + 1 < IPL; ++i) e[i] = pop ? e[i + 1] : e[i];
+    if (pop) e[IPL - 1] = 0ull;
   }
-  __syncwarp();
-  if (lane < k) buf[rank] = mine;
-  __syncwarp();
-  const unsigned long long best = lane < k ? buf[lane] : 0ull;
-  __syncwarp();
   return best;
 }
 
@@ -186,8 +188,7 @@ __device__ __forceinline__ int warp_topk(const float* __restrict__ P, int S, siz
                                          const float* __restrict__ bias, int n_sub,
                                          float* __restrict__ lout, int kt, int E_r, int k_max,
                                          int score, int renorm, float route_scale,
-                                         int32_t* status, int lane, unsigned long long* buf,
-                                         int* out_u, float* out_w) {
+                                         int32_t* status, int lane, int* out_u, float* out_w) {
   int k = kt;
   if (k < 1 || k > k_max) {
     if (lane == 0) report(status, MOE_ERR_K_RANGE);
@@ -251,7 +252,7 @@ __device__ __forceinline__ int warp_topk(const float* __restrict__ P, int S, siz
     for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
   }
 
-  const unsigned long long best = warp_select_topk<IPL>(key, E_r, k, lane, buf);
+  const unsigned long long best = warp_select_topk<IPL>(key, E_r, k, lane);
   int my_u = -1;
   float my_s = 0.f;
   if (lane < k) {
@@ -276,7 +277,6 @@ __global__ void __launch_bounds__(256) topk_gate_kernel(
     float* __restrict__ logits_out, const int32_t* __restrict__ kpt, int T, int E_r,
     int k_max, int score, int renorm, float route_scale, int32_t* __restrict__ topk_idx,
     float* __restrict__ topk_w, int32_t* status) {
-  __shared__ unsigned long long sbuf[8][32];
   pdl_wait_and_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
@@ -287,7 +287,7 @@ __global__ void __launch_bounds__(256) topk_gate_kernel(
   warp_topk<IPL>(P + row, S, static_cast<size_t>(T) * E_r, bias, n_sub,
                  logits_out != nullptr ? logits_out + row : nullptr,
                  kpt != nullptr ? kpt[t] : k_max, E_r, k_max, score,
-                 renorm, route_scale, status, lane, sbuf[warp], &u, &w);
+                 renorm, route_scale, status, lane, &u, &w);
   if (lane < k_max) {
     const size_t o = static_cast<size_t>(t) * k_max + lane;
     topk_idx[o] = u;
@@ -340,7 +340,7 @@ struct ClusterRouteParams {
 };
 
 struct ClusterSmem {
-  uint32_t pitch, rows, stage, red, all, buf, bits, off, sorted, wt, total;
+  uint32_t pitch, rows, stage, red, all, bits, off, sorted, wt, total;
 };
 
 // Staged rows per buffer: MT * 16 unit rows, then the eight token rows, each
@@ -359,9 +359,6 @@ __host__ __device__ inline ClusterSmem cluster_smem(int E_r, int MT, int kc, int
   b = (b + 15) & ~15u;
   o.all = b;
   b += kClTok * E_r * 4;
-  b = (b + 7) & ~7u;
-  o.buf = b;
-  b += kClWarps * 32 * 8;
   o.bits = b;
   b += 256 * 4;
   o.off = b;
@@ -420,7 +417,6 @@ __global__ void __launch_bounds__(kClThreads, 1) route_cluster_kernel(const Clus
   const ClusterSmem L = cluster_smem(p.E_r, p.MT, p.kc, p.ns);
   float* s_red = reinterpret_cast<float*>(csm + L.red);
   float* s_all = reinterpret_cast<float*>(csm + L.all);
-  unsigned long long* sbuf = reinterpret_cast<unsigned long long*>(csm + L.buf);
   uint32_t* s_bits = reinterpret_cast<uint32_t*>(csm + L.bits);
   int32_t* s_off = reinterpret_cast<int32_t*>(csm + L.off);
   int32_t* s_sorted = reinterpret_cast<int32_t*>(csm + L.sorted);
@@ -549,7 +545,7 @@ __global__ void __launch_bounds__(kClThreads, 1) route_cluster_kernel(const Clus
       k = warp_topk<IPL>(s_all + warp * E_r, 1, 0, p.bias, p.n_sub,
                          p.logits_out != nullptr ? p.logits_out + row : nullptr,
                          p.kpt != nullptr ? p.kpt[t] : p.k_max, E_r, p.k_max, p.score,
-                         p.renorm, p.route_scale, p.status, lane, sbuf + warp * 32, &my_u, &w);
+                         p.renorm, p.route_scale, p.status, lane, &my_u, &w);
       if (lane < p.k_max) {
         const size_t o = static_cast<size_t>(t) * p.k_max + lane;
         p.topk_idx[o] = my_u;

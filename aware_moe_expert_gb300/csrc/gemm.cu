@@ -39,6 +39,7 @@
 namespace moe {
 
 bool make_tmap_bf16(CUtensorMap* m, const void* base, long long rows, int cols, int box_rows);
+bool make_tmap_f32(CUtensorMap* m, const void* base, long long rows, int cols, int box_rows);
 
 namespace {
 
@@ -70,6 +71,8 @@ struct KParams {
   int bias_div;
   int32_t* status;
   uint32_t debug_flags;
+  int f32_tma;       // EPI_F32: full 32-row slabs leave through TMA stores (tmOut: fp32
+                     //   [S * out_rows, ld_out], 32 x 32 boxes); 0: per-thread stores only
 };
 
 template <int BN_MMA, int STAGES>
@@ -140,7 +143,7 @@ __global__ void __launch_bounds__(GATHER ? kThreads + kGatherThreads : kThreads,
   if (warp == 0 && lane == 0) {
     if (!GATHER) tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if (EPI != EPI_F32) tma_prefetch_desc(&tmOut);
+    if (EPI != EPI_F32 || p.f32_tma) tma_prefetch_desc(&tmOut);
   }
   if (warp == 1) {
     tmem_alloc(s_tmem, C::kTmemCols);
@@ -395,11 +398,42 @@ __global__ void __launch_bounds__(GATHER ? kThreads + kGatherThreads : kThreads,
       } else {
         const int col0 = t.nt * p.bn_out;
         float* orow = static_cast<float*>(p.out) + split * p.split_stride + grow * p.ld_out + col0;
+        // a warp whose 32 rows are all real writes each 32 x 32 fp32 block
+        // through shared memory with one TMA store (128-byte swizzle, as for
+        // bf16); other rows use per-thread stores
+        const bool full_slab = p.f32_tma && q * 32 + 32 <= t.rows &&
+                               static_cast<long long>(t.row0) + q * 32 + 32 <= p.out_rows &&
+                               col0 + BN_MMA <= p.out_cols;
 #pragma unroll 1
         for (int c = 0; c < BN_MMA; c += 32) {
           uint32_t v[32];
           tmem_ld32(tbase + c, v);
           tmem_ld_wait();
+          if (full_slab) {
+            uint32_t lo[16], hi[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              float a = __uint_as_float(v[i]), b = __uint_as_float(v[16 + i]);
+              if (p.bias != nullptr) {
+                a += p.bias[(col0 + c + i) / p.bias_div];
+                b += p.bias[(col0 + c + 16 + i) / p.bias_div];
+              }
+              lo[i] = __float_as_uint(a);
+              hi[i] = __float_as_uint(b);
+            }
+            if (lane == 0) bulk_wait_read_all();   // the previous block has left the buffer
+            __syncwarp();
+            stage_row_32(sbuf, lane, 0, lo);
+            stage_row_32(sbuf, lane, 4, hi);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmOut, sbuf, col0 + c,
+                           static_cast<int>(split * p.out_rows + t.row0 + q * 32));
+              bulk_commit();
+            }
+            continue;
+          }
           if (valid) {
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
@@ -430,10 +464,8 @@ __global__ void __launch_bounds__(GATHER ? kThreads + kGatherThreads : kThreads,
         aphase ^= 1u;
       }
     }
-    if (EPI != EPI_F32) {
-      if (lane == 0) bulk_wait_all();  // stores done before the CTA (and its smem) goes
-      __syncwarp();
-    }
+    if (lane == 0) bulk_wait_all();  // stores done before the CTA (and its smem) goes
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -458,10 +490,17 @@ cudaError_t run_gemm(const GemmArgs& g, cudaStream_t s) {
     return cudaErrorInvalidValue;
   }
   if (!make_tmap_bf16(&tb, g.b, g.b_rows, g.K, box_b)) return cudaErrorInvalidValue;
-  if (EPI == EPI_F32)
-    to = tb;  // unused
-  else if (!make_tmap_bf16(&to, g.out, g.out_rows, static_cast<int>(g.ld_out), 32))
+  bool f32_tma = false;
+  if (EPI == EPI_F32) {
+    // fp32 [S * out_rows, ld_out] when the split slices are contiguous
+    const int S = g.k_splits > 1 ? g.k_splits : 1;
+    const bool contiguous = S == 1 || g.split_stride == g.out_rows * g.ld_out;
+    f32_tma = contiguous &&
+              make_tmap_f32(&to, g.out, g.out_rows * S, static_cast<int>(g.ld_out), 32);
+    if (!f32_tma) to = tb;  // unused
+  } else if (!make_tmap_bf16(&to, g.out, g.out_rows, static_cast<int>(g.ld_out), 32)) {
     return cudaErrorInvalidValue;
+  }
   KParams kp;
   kp.offsets = g.offsets;
   kp.n_groups = g.offsets == nullptr ? 1 : g.n_groups;
@@ -485,6 +524,7 @@ cudaError_t run_gemm(const GemmArgs& g, cudaStream_t s) {
   kp.bias_div = g.bias_div > 0 ? g.bias_div : 1;
   kp.status = g.status;
   kp.debug_flags = g.debug_flags;
+  kp.f32_tma = f32_tma ? 1 : 0;
   long long m_tiles;
   if (g.offsets == nullptr)
     m_tiles = (g.dense_rows + BM - 1) / BM;
@@ -528,6 +568,23 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, long long rows, int cols, 
   cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// fp32 [rows, cols] row-major, boxes of 32 columns (128 bytes) x box_rows.
+bool make_tmap_f32(CUtensorMap* m, const void* base, long long rows, int cols, int box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr || rows <= 0 || cols % 32 != 0 ||
+      (reinterpret_cast<uintptr_t>(base) & 15u) != 0)
+    return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 4};
+  cuuint32_t box[2] = {32u, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

@@ -208,7 +208,7 @@ __device__ __forceinline__ int warp_topk(const float* __restrict__ P, int S, siz
     }
   }
   // add the remaining partial rows in slice order, SB slices' loads in flight
-  constexpr int SB = IPL >= 8 ? 2 : 16 / IPL;
+  constexpr int SB = IPL >= 4 ? 2 : 8 / IPL;
   for (int s0 = 1; s0 < S; s0 += SB) {
     float pv[SB][IPL];
 #pragma unroll

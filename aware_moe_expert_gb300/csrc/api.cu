@@ -303,9 +303,9 @@ moe_status do_gate_up(const moe_layer_desc* d, const void* x, const int32_t* sor
   void* xperm = at<void>(ws, l.xperm);
   const bool decode = use_decode_path(d, d->I_sub, true);
   const bool pair = (d->debug_flags & MOE_DEBUG_FORCE_PAIR) != 0u;
-  // the single-CTA prefill kernel gathers its A rows itself; the other
-  // kernels read the permuted copy
-  if (decode || pair)
+  // the prefill kernels (single CTAs or CTA pairs) gather their A rows
+  // themselves; the decode kernels read the permuted copy
+  if (decode)
     MOE_TRY(cuda_status(moe::launch_gather_rows(x, sorted_token, offsets, E_r, d->T, d->H,
                                                 static_cast<int>(n_cap), xperm, status,
                                                 sm_count(), s)));
@@ -349,11 +349,9 @@ moe_status do_gate_up(const moe_layer_desc* d, const void* x, const int32_t* sor
   g.status = status;
   g.debug_flags = d->debug_flags;
   g.force_pair = pair;
-  if (!pair) {
-    g.gather_x = x;
-    g.gather_tok = sorted_token;
-    g.gather_rows = d->T;
-  }
+  g.gather_x = x;
+  g.gather_tok = sorted_token;
+  g.gather_rows = d->T;
   g.sm_count = sm_count();
   g.max_rows_hint = static_cast<int>(n_cap);
   return cuda_status(moe::launch_gemm(g, s));

@@ -603,11 +603,10 @@ void router_gemm_shape(int T, int H, int E_r, int* bn, int* splits) {
 }
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t s) {
-  // CTA pairs stage a third fewer bytes per SM and k-block (12-17% less time
-  // per executed row on GB300) but tile 256 rows of one unit at a time; a
-  // routed batch leaves many units with a partial tile, which costs twice as
-  // much padding as with 128-row tiles, and the host cannot see the row
-  // counts.  Dense GEMMs use pairs when the padding allows it.
+  // CTA pairs stage a third fewer bytes per SM and k-block.  Routed GEMMs run
+  // on them when the caller asks (force_pair; the pair kernel tiles each
+  // unit's remainder of <= 128 rows with M = 128, so padding stays as with
+  // single CTAs); dense GEMMs use pairs when the 256-row padding allows it.
   if (gemm_pair_supports(g.epi, g.n_out)) {
     bool pair = g.force_pair && g.offsets != nullptr;
     if (g.offsets == nullptr) {

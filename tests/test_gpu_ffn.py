@@ -39,11 +39,13 @@ def _weights(E_r, H, I_sub, n_sub, seed):
     (1, 2048, 128, 2, 384, 16, 0.0),    # one token (decode: split-K over few items)
     (8, 2048, 128, 2, 384, 16, 0.0),    # eight tokens
     (400, 512, 4, 2, 256, 4, 4.0),      # > 128 rows on a unit: decode chunks of 128 tokens
+    (1500, 256, 8, 1, 128, 4, 1.5),     # units of hundreds of rows: 256-row pair tiles + tails
+    (2000, 256, 16, 1, 128, 6, 0.7),    # remainders on both sides of 128 rows
 ])
 def test_grouped_ffn_rows_match_oracle(T, H, n_experts, n_sub, I_sub, k_max, skew, path):
-    """Every kernel family (prefill tiles on one CTA or on CTA pairs, decode
-    swap-AB) on the same inputs; shapes a family does not support fall back
-    to another one."""
+    """Every kernel family (prefill tiles on one CTA or on CTA pairs with
+    256-row and 128-row tiles, decode swap-AB) on the same inputs; shapes a
+    family does not support fall back to another one."""
     debug = 0
     if path == "pair":
         path, debug = B.PATH_PREFILL, B.DEBUG_FORCE_PAIR

@@ -269,22 +269,30 @@ __global__ void __launch_bounds__(GATHER ? kThreads + kGatherThreads : kThreads,
     int stage = 0, astage = 0, pending = 0;
     uint32_t phase = 0;
     bool ok = true, bad = false;
-    for (int w = blockIdx.x; ok && w < total_work; w += gridDim.x) {
+    // the token indices of an item are loaded one item ahead, so the first
+    // copies of an item do not wait for them
+    auto load_tokens = [&](int w, int (&tk)[8]) {
       const Tile t = decode_tile(w, n_tiles_eff, G, s_prefix, s_offs);
-      const uint4* src[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int r = rg + 16 * i;
-        int tok = -1;
-        if (r < t.rows) {
-          tok = __ldg(p.gtok + t.row0 + r);
-          if (tok < 0 || tok >= p.gx_rows) {
-            bad = true;
-            tok = -1;
-          }
+        tk[i] = r < t.rows ? __ldg(p.gtok + t.row0 + r) : -1;
+      }
+    };
+    int tk[8];
+    if (static_cast<int>(blockIdx.x) < total_work) load_tokens(blockIdx.x, tk);
+    for (int w = blockIdx.x; ok && w < total_work; w += gridDim.x) {
+      const uint4* src[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        int tok = tk[i];
+        if (tok != -1 && (tok < 0 || tok >= p.gx_rows)) {
+          bad = true;
+          tok = -1;
         }
         src[i] = tok >= 0 ? p.gx + static_cast<size_t>(tok) * nv + chunk : nullptr;
       }
+      if (w + static_cast<int>(gridDim.x) < total_work) load_tokens(w + gridDim.x, tk);
       for (int kb = 0; kb < KB; ++kb) {
         if (!mbar_wait(&empty[stage], phase ^ 1u, s_abort)) {
           ok = false;

@@ -84,6 +84,25 @@ def dist_info():
     return rank, world, local
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest of every rank's value (the slowest replica sets the job's
+    time); the value itself with one rank.  Needs the default process group
+    when world > 1 (NCCL on the GPUs, gloo in the CPU tests)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank: int, world: int, ms: float) -> float:
+    """Whole-job throughput: every replica processes its own batch (weak
+    scaling), all of them within the slowest replica's time."""
+    return tokens_per_rank * world / (ms * 1e-3)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -382,12 +401,7 @@ def run_ours(args, wl, rank, world, local):
     if code != 0:
         raise RuntimeError(f"device status {B.STATUS_NAMES.get(code, code)}")
     step_ms = np.array([ev0[i].elapsed_time(ev1[i]) for i in range(args.steps)])
-    ms = float(step_ms.mean())
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(float(step_ms.mean()), world, dev)
     per = np.array([[evp[i][j].elapsed_time(evp[i][j + 1]) for j in range(n_parts)]
                     for i in range(args.steps)])
     parts = {n: float(per[:, j].mean() * 1000.0) for j, (n, _) in enumerate(g_parts)}
@@ -480,11 +494,7 @@ def run_ours(args, wl, rank, world, local):
             e2e_ms = run_pipelined(args.steps)
             e2e_mode = ("pipelined: step i+1's copy in and step i-1's copy out overlap step i "
                         "on two copy streams; K steps timed first copy to last")
-        if world > 1:
-            import torch.distributed as dist
-            tt = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e2e_ms = float(tt.item())
+        e2e_ms = max_over_ranks(e2e_ms, world, dev)
         h2d = T * H * 2 + T * 4
         d2h = T * H * 2
         e2e = (e2e_ms, h2d, d2h, e2e_mode)
@@ -538,7 +548,7 @@ def run_ours(args, wl, rank, world, local):
     if wl.phase == "decode":
         res.update({"value": round(us, 2), "unit": "µs/layer", "higher_is_better": False})
     else:
-        res.update({"value": round(T * world / (ms * 1e-3), 1), "unit": "tokens/s",
+        res.update({"value": round(job_tokens_per_s(T, world, ms), 1), "unit": "tokens/s",
                     "higher_is_better": True})
     res["config"] = {"workload": wl.name, "T": T, "H": H, "experts": wl.n_experts,
                      "n_sub": wl.n_sub, "E_r": E_r, "I_sub": I_sub, "I_shared": wl.I_shared,
@@ -566,7 +576,7 @@ def run_ours(args, wl, rank, world, local):
             res["e2e"] = {"value": round(e2e_ms * 1000.0, 2), "unit": "µs/layer",
                           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "mode": e2e_mode}
         else:
-            res["e2e"] = {"value": round(T * world / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+            res["e2e"] = {"value": round(job_tokens_per_s(T, world, e2e_ms), 1), "unit": "tokens/s",
                           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "mode": e2e_mode}
     clocks = cs.summary()
     res["clocks"] = clocks

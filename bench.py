@@ -299,19 +299,21 @@ def run_ours(args, wl, rank, world, local):
 
     out_fused = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
     ws_fused = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    weight_sets = [d]     # decode: rotating copies of the weights, added below
 
-    def layer_step(sp):
+    def layer_step(sp, c=0):
+        wt = weight_sets[c]
         if fold is not None:
-            B.check(B.moe_layer_forward_fold(desc, fold, d["x"], d["router_w"], d["w_gate_up"],
-                                             d["w_down"], d["k_per_token"], out_fused, st,
+            B.check(B.moe_layer_forward_fold(desc, fold, d["x"], wt["router_w"], wt["w_gate_up"],
+                                             wt["w_down"], d["k_per_token"], out_fused, st,
                                              ws_fused, sp), "moe_layer_forward_fold")
             return
         if cg is not None:
-            B.check(B.moe_layer_forward_cg(desc, cg, d["x"], d["w_gate_up"], d["w_down"],
+            B.check(B.moe_layer_forward_cg(desc, cg, d["x"], wt["w_gate_up"], wt["w_down"],
                                            d["k_per_token"], out_fused, st, ws_fused, sp),
                     "moe_layer_forward_cg")
             return
-        B.check(B.moe_layer_forward(desc, d["x"], d["router_w"], d["w_gate_up"], d["w_down"],
+        B.check(B.moe_layer_forward(desc, d["x"], wt["router_w"], wt["w_gate_up"], wt["w_down"],
                                     d["k_per_token"], out_fused, st, ws_fused, sp),
                 "moe_layer_forward")
 
@@ -336,18 +338,45 @@ def run_ours(args, wl, rank, world, local):
         with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
             fn(torch.cuda.current_stream().cuda_stream)
         return g
-    g_full = capture(layer_step)
     g_parts = [(n, capture(f)) for n, f in calls]
 
-    # L2 handling: flush with a 2x-L2 write between steps unless the step
-    # streams far more than L2 anyway.
+    # L2 handling.  Decode: the K timed steps are K layer calls in one CUDA
+    # graph over rotating copies of the weights, enough copies that the
+    # activated weights of consecutive calls span at least 4x L2 (no flush,
+    # no host launch gap between layers; time / K per layer).  Prefill: one
+    # layer per graph replay, L2 flushed between steps (2x-L2 write) unless
+    # the step streams far more than L2 anyway.  The per-call breakdown uses
+    # the flush whenever the activated weights are below 4x L2.
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     w_active = D * 3 * H * I_sub * 2 + (3 * H * wl.I_shared * 2 if wl.I_shared else 0)
-    flush = w_active < 4 * l2
-    flush_buf = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev) if flush else None
+    rotate = wl.phase == "decode"
+    flush_parts = w_active < 4 * l2
+    flush = flush_parts and not rotate
+    flush_buf = (torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+                 if flush_parts else None)
+    if rotate:
+        keys = [k for k in ("router_w", "w_gate_up", "w_down", "w_shared_gate_up",
+                            "w_shared_down") if d.get(k) is not None]
+        per_copy = sum(d[k].numel() * d[k].element_size() for k in keys)
+        n_copies = max(2, -(-4 * l2 // max(w_active, 1)))
+        while n_copies > 2 and n_copies * per_copy > (24 << 30):
+            n_copies -= 1
+        for _ in range(n_copies - 1):
+            weight_sets.append({k: d[k].clone() for k in keys})
+    g_full = capture(layer_step)
+    g_all = None
+    if rotate:
+        def all_steps(sp):
+            for i in range(args.steps):
+                layer_step(sp, i % len(weight_sets))
+        g_all = capture(all_steps)
 
     def maybe_flush():
         if flush:
+            flush_buf.zero_()
+
+    def flush_for_parts():
+        if flush_parts:
             flush_buf.zero_()
 
     ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -356,9 +385,13 @@ def run_ours(args, wl, rank, world, local):
     evp = [[torch.cuda.Event(enable_timing=True) for _ in range(n_parts + 1)]
            for _ in range(args.steps)]
     with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            maybe_flush()
-            g_full.replay()
+        if rotate:
+            for _ in range(-(-args.warmup // args.steps)):
+                g_all.replay()
+        else:
+            for _ in range(args.warmup):
+                maybe_flush()
+                g_full.replay()
     torch.cuda.synchronize(dev)
     if world > 1:
         import torch.distributed as dist
@@ -369,11 +402,16 @@ def run_ours(args, wl, rank, world, local):
     with ClockSampler(local, smi_path) as cs:
         t_wall0 = time.perf_counter()
         with torch.cuda.stream(stream):
-            for i in range(args.steps):
-                maybe_flush()
-                ev0[i].record(stream)
-                g_full.replay()
-                ev1[i].record(stream)
+            if rotate:
+                ev0[0].record(stream)
+                g_all.replay()
+                ev1[0].record(stream)
+            else:
+                for i in range(args.steps):
+                    maybe_flush()
+                    ev0[i].record(stream)
+                    g_full.replay()
+                    ev1[i].record(stream)
         torch.cuda.synchronize(dev)
         t_wall = time.perf_counter() - t_wall0
         if world > 1:
@@ -383,7 +421,7 @@ def run_ours(args, wl, rank, world, local):
         # per-call breakdown, same number of steps
         with torch.cuda.stream(stream):
             for i in range(args.steps):
-                maybe_flush()
+                flush_for_parts()
                 evp[i][0].record(stream)
                 for j, (_, g) in enumerate(g_parts):
                     g.replay()
@@ -393,14 +431,20 @@ def run_ours(args, wl, rank, world, local):
         t_extra = time.perf_counter()
         with torch.cuda.stream(stream):
             while time.perf_counter() - t_extra < 1.5:
-                for _ in range(20):
-                    maybe_flush()
-                    g_full.replay()
+                if rotate:
+                    g_all.replay()
+                else:
+                    for _ in range(20):
+                        maybe_flush()
+                        g_full.replay()
                 torch.cuda.synchronize(dev)
     code = B.moe_get_device_status(st, sp)
     if code != 0:
         raise RuntimeError(f"device status {B.STATUS_NAMES.get(code, code)}")
-    step_ms = np.array([ev0[i].elapsed_time(ev1[i]) for i in range(args.steps)])
+    if rotate:
+        step_ms = np.array([ev0[0].elapsed_time(ev1[0]) / args.steps])
+    else:
+        step_ms = np.array([ev0[i].elapsed_time(ev1[i]) for i in range(args.steps)])
     ms = max_over_ranks(float(step_ms.mean()), world, dev)
     per = np.array([[evp[i][j].elapsed_time(evp[i][j + 1]) for j in range(n_parts)]
                     for i in range(args.steps)])
@@ -408,13 +452,14 @@ def run_ours(args, wl, rank, world, local):
     del g_full, g_parts
 
     # end to end through the public call with host buffers: every step copies
-    # its inputs (x, k) from pinned host memory and its output back.  Steps
-    # are pipelined on three streams when L2 is not flushed between steps:
-    # step i+1's host->device copy and step i-1's device->host copy run on
-    # their own streams while step i computes (double-buffered device
-    # tensors); the timed region spans all K steps, first copy to last.  With
-    # the L2 flush (small decode batches) each step runs copy -> layer -> copy
-    # in order, timed one by one, the flush outside the timed region.
+    # its inputs (x, k) from pinned host memory and its output back (decode
+    # steps rotate over the weight copies).  Unless L2 is flushed between
+    # steps, the steps are pipelined on three streams: step i+1's
+    # host->device copy and step i-1's device->host copy run on their own
+    # streams while step i computes (double-buffered device tensors); the
+    # timed region spans all K steps, first copy to last.  With the flush each
+    # step runs copy -> layer -> copy in order and is timed alone, the flush
+    # outside the timed region.
     e2e = None
     if not args.no_e2e:
         layer = B.MoeLayer(desc, dev)
@@ -429,13 +474,14 @@ def run_ours(args, wl, rank, world, local):
         s_in = torch.cuda.Stream(dev)
         s_out = torch.cuda.Stream(dev)
 
-        def forward(b):
+        def forward(b, i=0):
+            wt = weight_sets[i % len(weight_sets)]   # decode: the rotating copies
             if cg is not None:
-                B.check(B.moe_layer_forward_cg(desc, cg, dx[b], d["w_gate_up"], d["w_down"],
+                B.check(B.moe_layer_forward_cg(desc, cg, dx[b], wt["w_gate_up"], wt["w_down"],
                                                dk[b], dout[b], layer.status, layer.workspace, sp))
             else:
-                B.check(B.moe_layer_forward(desc, dx[b], d["router_w"], d["w_gate_up"],
-                                            d["w_down"], dk[b], dout[b], layer.status,
+                B.check(B.moe_layer_forward(desc, dx[b], wt["router_w"], wt["w_gate_up"],
+                                            wt["w_down"], dk[b], dout[b], layer.status,
                                             layer.workspace, sp))
 
         def run_serial(n):
@@ -448,7 +494,7 @@ def run_ours(args, wl, rank, world, local):
                     ev[i][0].record(stream)
                     dx[0].copy_(hx, non_blocking=True)
                     dk[0].copy_(hk, non_blocking=True)
-                    forward(0)
+                    forward(0, i)
                     hout[0].copy_(dout[0], non_blocking=True)
                     ev[i][1].record(stream)
             torch.cuda.synchronize(dev)
@@ -474,7 +520,7 @@ def run_ours(args, wl, rank, world, local):
                 if i >= 2:
                     stream.wait_event(ev_out[i - 2])    # dout[b] copied out
                 with torch.cuda.stream(stream):
-                    forward(b)
+                    forward(b, i)
                     ev_comp[i].record(stream)
                 s_out.wait_event(ev_comp[i])
                 with torch.cuda.stream(s_out):
@@ -485,6 +531,8 @@ def run_ours(args, wl, rank, world, local):
             torch.cuda.synchronize(dev)
             return t0.elapsed_time(t1) / n
 
+        h2d = T * H * 2 + T * 4
+        d2h = T * H * 2
         if flush:
             run_serial(args.warmup)
             e2e_ms = run_serial(args.steps)
@@ -495,8 +543,6 @@ def run_ours(args, wl, rank, world, local):
             e2e_mode = ("pipelined: step i+1's copy in and step i-1's copy out overlap step i "
                         "on two copy streams; K steps timed first copy to last")
         e2e_ms = max_over_ranks(e2e_ms, world, dev)
-        h2d = T * H * 2 + T * 4
-        d2h = T * H * 2
         e2e = (e2e_ms, h2d, d2h, e2e_mode)
         if layer.device_status(sp) != 0:
             raise RuntimeError("device status after e2e")
@@ -561,7 +607,10 @@ def run_ours(args, wl, rank, world, local):
                      "router": ("linear gate over all units" if cg is None else
                                 f"proxy router: top-{wl.native_m} experts, {args.cg_r} gate "
                                 f"neurons per sub-expert, even allocation table"),
-                     "l2": (f"flushed between steps ({2 * l2 >> 20} MiB write)" if flush else
+                     "l2": (f"{len(weight_sets)} rotating weight copies, K layer calls in one "
+                            f"CUDA graph ({len(weight_sets) * w_active / 2**20:.0f} MiB of "
+                            f"activated weights across copies vs {l2 >> 20} MiB L2)" if rotate else
+                            f"flushed between steps ({2 * l2 >> 20} MiB write)" if flush else
                             f"inputs larger than L2 ({w_active / 2**20:.0f} MiB of active weights "
                             f"per step vs {l2 >> 20} MiB L2)")}
     res["realised"] = {"n_assign": n_assign, "distinct_units": D, "k_mean": n_assign / T}

@@ -185,3 +185,42 @@ def test_layer_comparison_budget_modes(name, T, mode):
     B.check(B.moe_route(desc, d["x"], d["router_w"], None, d["k_per_token"], Lg, idx, w,
                         layer.status, layer.workspace))
     _compare(wl, d, desc, out, Lg, idx, np.arange(wl.T))
+
+
+@pytest.mark.parametrize("path", [B.PATH_AUTO, B.PATH_PREFILL, B.PATH_DECODE])
+def test_zero_tokens_is_a_no_op(path):
+    """T = 0 through the layer and every component call: MOE_OK, no device
+    error, nothing written."""
+    wl = WL.TINY.with_T(1)
+    d = make_layer_inputs(wl, DEV)
+    desc = B.desc_for(wl, expert_bias=d["expert_bias"])
+    desc.T = 0
+    desc.path = path
+    ws = torch.empty(max(B.moe_workspace_size(desc), 256), dtype=torch.uint8, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    one_i = torch.zeros(1, dtype=torch.int32, device=DEV)
+    one_f = torch.zeros(1, dtype=torch.float32, device=DEV)
+    sentinel = torch.full((4, wl.H), 7.0, dtype=torch.bfloat16, device=DEV)
+    B.check(B.moe_layer_forward(desc, sentinel, d["router_w"], d["w_gate_up"], d["w_down"],
+                                one_i, sentinel, st, ws))
+    B.check(B.moe_route(desc, sentinel, d["router_w"], None, one_i, None, one_i, one_f, st, ws))
+    B.check(B.moe_permute(desc, one_i, one_i, one_i, one_i, one_i, one_i, st, ws))
+    B.check(B.moe_combine(desc, sentinel, None, one_i, one_f, one_i, sentinel, st))
+    assert B.moe_get_device_status(st) == 0
+    assert bool((sentinel == 7.0).all())
+
+
+@pytest.mark.parametrize("T", [129, 1000, 4097])
+def test_layer_prefill_ragged_token_counts(T):
+    """Token counts that leave partial 128-row router tiles and ragged unit
+    tails on the prefill path (tensor-core router, gathering grouped GEMM);
+    every token up to 1000, else a seeded sample plus the first and last."""
+    wl = replace(WL.QWEN_DECODE, name="qwen-shape-prefill-ragged", phase="prefill", T=T)
+    wl, d, desc, out, Lg, idx = _run_layer(wl, path=B.PATH_PREFILL)
+    if T <= 1000:
+        tokens = np.arange(T)
+    else:
+        rng = np.random.default_rng(T)
+        tokens = np.unique(np.concatenate([[0, T - 1], rng.choice(T, 256, replace=False)]))
+    fro, n_tied = _compare(wl, d, desc, out, Lg, idx, tokens)
+    assert fro <= 5e-3

@@ -238,10 +238,13 @@ moe_status do_logits_gemm(const moe_layer_desc* d, const void* x, const void* ro
   return cuda_status(moe::launch_gemm(g, s));
 }
 
+// bitmap_done (nullable): ask the top-k kernel to write the permutation's
+// bitmap as well (layer forward, T > 256); *bitmap_done says whether it did.
 moe_status do_route(const moe_layer_desc* d, const void* x, const void* router_w,
                     const float* logits_in, const int32_t* kpt, float* logits_out,
                     int32_t* topk_idx, float* topk_w, int32_t* status, void* ws,
-                    cudaStream_t s) {
+                    cudaStream_t s, bool* bitmap_done = nullptr) {
+  if (bitmap_done != nullptr) *bitmap_done = false;
   const int E_r = E_r_of(d);
   const Layout l = layout_of(*d);
   const float* P = logits_in;   // what the top-k kernel sums
@@ -279,18 +282,25 @@ moe_status do_route(const moe_layer_desc* d, const void* x, const void* router_w
       lout = logits_out;
     }
   }
+  uint32_t* bm = nullptr;
+  if (bitmap_done != nullptr && d->T >= moe::kPermuteBitmapMinT) {
+    bm = at<uint32_t>(ws, l.bitmap);
+    *bitmap_done = true;
+  }
   return cuda_status(moe::launch_topk_gate(P, S, bias, d->n_sub, lout, kpt, d->T, E_r, d->k_max,
                                            d->score, d->renorm, d->route_scale, topk_idx, topk_w,
-                                           status, s));
+                                           status, s, bm));
 }
 
 moe_status do_permute(const moe_layer_desc* d, const int32_t* topk_idx, const int32_t* kpt,
                       int32_t* counts, int32_t* offsets, int32_t* sorted_token,
-                      int32_t* inv_row, int32_t* status, void* ws, cudaStream_t s) {
+                      int32_t* inv_row, int32_t* status, void* ws, cudaStream_t s,
+                      bool bitmap_ready = false) {
   const Layout l = layout_of(*d);
   return cuda_status(moe::launch_permute(topk_idx, kpt, d->T, d->k_max, E_r_of(d),
                                          at<uint32_t>(ws, l.bitmap), at<int32_t>(ws, l.wprefix),
-                                         counts, offsets, sorted_token, inv_row, status, s));
+                                         counts, offsets, sorted_token, inv_row, status, s,
+                                         bitmap_ready));
 }
 
 moe_status do_gate_up(const moe_layer_desc* d, const void* x, const int32_t* sorted_token,
@@ -842,10 +852,11 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, const vo
         desc->k_max, desc->score, desc->renorm, desc->route_scale, nullptr, topk_idx, topk_w,
         dev_status, &f, s)));
   } else {
+    bool bitmap_done = false;
     MOE_TRY(do_route(desc, x, router_w, nullptr, k_per_token, nullptr, topk_idx, topk_w,
-                     dev_status, workspace, s));
+                     dev_status, workspace, s, &bitmap_done));
     MOE_TRY(do_permute(desc, topk_idx, k_per_token, counts, offsets, sorted_token, inv_row,
-                       dev_status, workspace, s));
+                       dev_status, workspace, s, bitmap_done));
   }
   if (ysh != nullptr) MOE_TRY(do_shared(desc, x, ysh, dev_status, workspace, s));
   MOE_TRY(do_grouped_ffn(desc, x, sorted_token, offsets, w_gate_up, w_down, yperm, dev_status,

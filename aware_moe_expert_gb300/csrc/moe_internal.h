@@ -19,11 +19,14 @@ cudaError_t launch_router_logits_small(const void* x, const void* router_w, int 
 // Top-k_t and gates from the sum of S partial logit arrays [S, T, E_r] (S = 1:
 // finished logits) plus bias[u / n_sub] (nullable); logits_out (nullable)
 // receives the summed logits; k_per_token == nullptr keeps k_max per token.
+// bitmap (nullable): also write the permutation's unit membership bitmap
+// ([E_r][ceil(T/32)] uint32, the layout launch_permute builds), so that
+// launch_permute can be told it is ready.
 cudaError_t launch_topk_gate(const float* partial, int S, const float* bias, int n_sub,
                              float* logits_out, const int32_t* k_per_token, int T, int E_r,
                              int k_max, int score, int renorm, float route_scale,
                              int32_t* topk_idx, float* topk_w, int32_t* status,
-                             cudaStream_t s);
+                             cudaStream_t s, uint32_t* bitmap = nullptr);
 
 // Logits and top-k_t of clusters of eight tokens in one launch (mma.sync
 // tiles, H % 16 == 0, E_r <= 256).  With `fuse` (T <= 8 only) the same launch also
@@ -85,10 +88,14 @@ cudaError_t launch_paths_rows(const int32_t* n_paths, const int32_t* slot, const
                               cudaStream_t s);
 
 // ---- permute.cu
+// bitmap_ready: the top-k kernel already wrote `bitmap` (T > 256 only).
 cudaError_t launch_permute(const int32_t* topk_idx, const int32_t* k_per_token, int T,
                            int k_max, int E_r, uint32_t* bitmap, int32_t* wprefix,
                            int32_t* counts, int32_t* offsets, int32_t* sorted_token,
-                           int32_t* inv_row, int32_t* status, cudaStream_t s);
+                           int32_t* inv_row, int32_t* status, cudaStream_t s,
+                           bool bitmap_ready = false);
+// T above which launch_permute builds the bitmap (below: one CTA, no bitmap)
+constexpr int kPermuteBitmapMinT = 257;
 // also zeroes zero_ptr[0, zero_n) (counters for the kernel that follows)
 cudaError_t launch_gather_rows(const void* x, const int32_t* sorted_token,
                                const int32_t* offsets, int E_r, int T, int H, int n_cap,

@@ -259,8 +259,10 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(
 cudaError_t launch_permute(const int32_t* topk_idx, const int32_t* k_per_token, int T,
                            int k_max, int E_r, uint32_t* bitmap, int32_t* wprefix,
                            int32_t* counts, int32_t* offsets, int32_t* sorted_token,
-                           int32_t* inv_row, int32_t* status, cudaStream_t s) {
+                           int32_t* inv_row, int32_t* status, cudaStream_t s,
+                           bool bitmap_ready) {
   const int W = (T + 31) / 32;
+  static_assert(kPermuteBitmapMinT == 8 * 32 + 1, "the one-CTA path takes W <= 8");
   if (W > 0 && W <= 8) {
     const int smem = (2 * E_r * W + 256 + 257) * 4;
     static bool attr_done[64] = {false};
@@ -269,7 +271,7 @@ cudaError_t launch_permute(const int32_t* topk_idx, const int32_t* k_per_token, 
     return launch_pdl(permute_small_kernel, dim3(1), dim3(1024), smem, s, topk_idx, k_per_token,
                       T, k_max, E_r, W, counts, offsets, sorted_token, inv_row, status);
   }
-  if (W > 0) {
+  if (W > 0 && !bitmap_ready) {
     cudaError_t e = launch_pdl(bitmap_kernel, dim3(W), dim3(256), 0, s, topk_idx, k_per_token, T,
                                k_max, E_r, W, bitmap, status);
     if (e != cudaSuccess) return e;

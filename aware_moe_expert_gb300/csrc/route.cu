@@ -271,27 +271,50 @@ __device__ __forceinline__ int warp_topk(const float* __restrict__ P, int S, siz
 // One warp per token, eight tokens per CTA.  P holds S partial logit arrays
 // [T, E_r] one after another (S = 1: finished logits).  kpt == nullptr: every
 // token keeps k_max units.
+//
+// bitmap != nullptr: the CTA also writes its byte of the permutation's unit
+// membership bitmap (bit j of byte b of row u = token 8 b + j selected u;
+// rows of row_bytes = 4 * ceil(T / 32) bytes, the uint32 words the scan
+// reads), so the permutation needs no pass of its own over topk_idx.  The
+// last CTA also zeroes the row bytes past the last token group.
 template <int IPL>
 __global__ void __launch_bounds__(256) topk_gate_kernel(
     const float* __restrict__ P, int S, const float* __restrict__ bias, int n_sub,
     float* __restrict__ logits_out, const int32_t* __restrict__ kpt, int T, int E_r,
     int k_max, int score, int renorm, float route_scale, int32_t* __restrict__ topk_idx,
-    float* __restrict__ topk_w, int32_t* status) {
+    float* __restrict__ topk_w, int32_t* status, uint8_t* __restrict__ bitmap,
+    int row_bytes) {
+  __shared__ uint32_t s_bits[256];
   pdl_wait_and_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
-  if (t >= T) return;
-  int u;
-  float w;
-  const size_t row = static_cast<size_t>(t) * E_r;
-  warp_topk<IPL>(P + row, S, static_cast<size_t>(T) * E_r, bias, n_sub,
-                 logits_out != nullptr ? logits_out + row : nullptr,
-                 kpt != nullptr ? kpt[t] : k_max, E_r, k_max, score,
-                 renorm, route_scale, status, lane, &u, &w);
-  if (lane < k_max) {
-    const size_t o = static_cast<size_t>(t) * k_max + lane;
-    topk_idx[o] = u;
-    topk_w[o] = w;
+  if (bitmap != nullptr) {
+    for (int v = threadIdx.x; v < E_r; v += blockDim.x) s_bits[v] = 0u;
+    __syncthreads();
+  }
+  if (t < T) {
+    int u;
+    float w;
+    const size_t row = static_cast<size_t>(t) * E_r;
+    warp_topk<IPL>(P + row, S, static_cast<size_t>(T) * E_r, bias, n_sub,
+                   logits_out != nullptr ? logits_out + row : nullptr,
+                   kpt != nullptr ? kpt[t] : k_max, E_r, k_max, score,
+                   renorm, route_scale, status, lane, &u, &w);
+    if (lane < k_max) {
+      const size_t o = static_cast<size_t>(t) * k_max + lane;
+      topk_idx[o] = u;
+      topk_w[o] = w;
+    }
+    if (bitmap != nullptr && u >= 0) atomicOr(&s_bits[u], 1u << warp);
+  }
+  if (bitmap != nullptr) {
+    __syncthreads();
+    for (int v = threadIdx.x; v < E_r; v += blockDim.x) {
+      uint8_t* r = bitmap + static_cast<size_t>(v) * row_bytes;
+      r[blockIdx.x] = static_cast<uint8_t>(s_bits[v]);
+      if (blockIdx.x + 1 == gridDim.x)
+        for (int b = blockIdx.x + 1; b < row_bytes; ++b) r[b] = 0;
+    }
   }
 }
 
@@ -781,13 +804,16 @@ cudaError_t launch_topk_gate(const float* partial, int S, const float* bias, int
                              float* logits_out, const int32_t* k_per_token, int T, int E_r,
                              int k_max, int score, int renorm, float route_scale,
                              int32_t* topk_idx, float* topk_w, int32_t* status,
-                             cudaStream_t s) {
+                             cudaStream_t s, uint32_t* bitmap) {
   if (T <= 0) return cudaSuccess;
+  if (E_r > 256) return cudaErrorInvalidValue;
   const int grid = (T + 7) / 8;
+  uint8_t* bm = reinterpret_cast<uint8_t*>(bitmap);
+  const int row_bytes = 4 * ((T + 31) / 32);
 #define MOE_TOPK_LAUNCH(IPL)                                                                 \
   launch_pdl(topk_gate_kernel<IPL>, dim3(grid), dim3(256), 0, s, partial, S, bias, n_sub,     \
              logits_out, k_per_token, T, E_r, k_max, score, renorm, route_scale, topk_idx,    \
-             topk_w, status)
+             topk_w, status, bm, row_bytes)
   if (E_r <= 32) return MOE_TOPK_LAUNCH(1);
   if (E_r <= 64) return MOE_TOPK_LAUNCH(2);
   if (E_r <= 128) return MOE_TOPK_LAUNCH(4);

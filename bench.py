@@ -583,7 +583,7 @@ def run_ours(args, wl, rank, world, local):
                 "kernel": "moe_gate_up (row gather + grouped gate|up GEMM, SwiGLU epilogue)",
                 "algorithmic_flops": alg, "peak_source": peaks["source"] + " bf16_tflops (burst)"}
 
-    n_launch = launches_per_step(wl, T, args.path, fold=fold is not None) + \
+    n_launch = launches_per_step(wl, T, args.path, fold=fold is not None, cg=cg is not None) + \
         (2 if cg is not None else 0)
     us = ms * 1000.0
     res = {
@@ -633,13 +633,14 @@ def run_ours(args, wl, rank, world, local):
     return res, d
 
 
-def launches_per_step(wl, T, path=0, fold=False):
+def launches_per_step(wl, T, path=0, fold=False, cg=False):
     """Kernels libmoe enqueues per moe_layer_forward (mirrors the host
     sequencing in csrc/api.cu: router + top-k (one cluster launch on CUDA
     cores, or the tensor-core GEMM and the top-k kernel), permutation (fused
-    into the router launch for <= 8 tokens), [folding], [shared expert],
-    gate|up (+ the split-K reduction of the weight-stationary family), down
-    (+ its split reduction), combine)."""
+    into the router launch for <= 8 tokens; above 256 tokens the top-k kernel
+    also writes its bitmap), [folding], [shared expert], gate|up (+ the
+    split-K reduction of the weight-stationary family), down (+ its split
+    reduction), combine)."""
     n_cap = T * wl.k_max
     decode = path == 2 or (path == 0 and n_cap <= 64 * wl.E_r)
     budget = 256 << 20
@@ -651,7 +652,10 @@ def launches_per_step(wl, T, path=0, fold=False):
         n = 1
     else:
         n = 1 if cluster_router else 2               # logits (+ top-k)
-        n += 1 if (T + 31) // 32 <= 8 else 3        # permutation (one CTA, or bitmap/scan/scatter)
+        if (T + 31) // 32 <= 8:
+            n += 1                                   # permutation in one CTA
+        else:                                        # [bitmap,] scan, scatter
+            n += 2 if not (cluster_router or fold or cg) else 3
     n += 4 if fold else 0                            # fold: scores, pool, target map, remap
     n += 2 if wl.I_shared else 0                     # shared expert gate|up, down
     if decode_ffn:

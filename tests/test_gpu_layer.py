@@ -130,11 +130,13 @@ def test_full_size_routing_and_permutation_bit_exact(name):
 @pytest.mark.parametrize("name,T", [("tiny", None), ("qwen_decode", 64), ("qwen_decode", 256),
                                     ("qwen_decode", 300), ("mixtral_decode", None),
                                     ("qwen_decode", 1), ("qwen_decode", 8), ("mixtral_decode", 5),
-                                    ("tiny", 7), ("tiny_i192", 4)])
+                                    ("tiny", 7), ("tiny_i192", 4), ("tiny", 1000),
+                                    ("qwen_decode", 1024)])
 def test_layer_forward_equals_component_calls(name, T):
     """moe_layer_forward gives bit-identical results to moe_route ->
     moe_permute -> moe_grouped_ffn -> moe_combine on the same inputs (for
-    T <= 8 the layer runs router, permutation and row gather as one launch)."""
+    T <= 8 the layer runs router, permutation and row gather as one launch;
+    for T > 256 its top-k kernel also writes the permutation's bitmap)."""
     if name == "tiny_i192":   # no fused decode FFN (I_sub % 128 != 0): gate|up, down
         wl = replace(WL.TINY, I_sub=192, name="tiny-i192")
     else:

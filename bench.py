@@ -397,7 +397,9 @@ def run_ours(args, wl, rank, world, local):
         import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize(dev)
-    smi_path = os.path.join(ROOT, "gpurun_out", f"bench_clocks_r{rank}.csv")
+    import tempfile
+    smi_path = os.path.join(os.environ.get("MOE_BENCH_CLOCKS_DIR", tempfile.gettempdir()),
+                            f"moe_bench_clocks_r{rank}.csv")
     os.makedirs(os.path.dirname(smi_path), exist_ok=True)
     with ClockSampler(local, smi_path) as cs:
         t_wall0 = time.perf_counter()

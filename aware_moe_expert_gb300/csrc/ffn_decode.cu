@@ -87,6 +87,23 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr));
 }
 
+// 1 on every one of the 128 epilogue threads iff `ok` is non-zero on all of
+// them (named barrier 1 with an AND reduction).  The epilogue warps meet at
+// named barriers inside an item, so they must leave the item loop together:
+// a warp whose bounded wait gave up must not leave another waiting at one.
+__device__ __forceinline__ int epilogue_all(int ok) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.s32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 128, p;\n\t"
+      "selp.s32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(ok)
+      : "memory");
+  return r;
+}
+
 __device__ __forceinline__ int ld_acquire(const int32_t* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -393,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int slot = i % kQ;
       int ok = 1;
       if (lane == 0) ok = mbar_wait(&q_full[slot], (i / kQ) & 1, s_abort) ? 1 : 0;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
+      ok = epilogue_all(__shfl_sync(0xffffffffu, ok, 0));
       if (!ok) {
         if (lane == 0) fail(s_abort, p.status);
         break;
@@ -408,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Item it = item_of(w, n_gu, S, p.gu_tiles, p.dn_tiles);
       const Tile t = decode_tile<kChunk>(it.mt, 1, p.n_groups, s_prefix, s_offs);
       if (lane == 0) ok = mbar_wait(&tfull[acc], aphase, s_abort) ? 1 : 0;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
+      ok = epilogue_all(__shfl_sync(0xffffffffu, ok, 0));
       if (!ok) {
         if (lane == 0) fail(s_abort, p.status);
         break;

@@ -3,10 +3,13 @@
 A step is one pass of the whole hot path over one batch: router logits and
 top-k_t (moe_route), permutation (moe_permute), grouped gate|up + SwiGLU
 (moe_gate_up), grouped down (moe_down), weighted combine (moe_combine), plus
-the shared expert where the workload has one.  Inputs are seeded synthetic
-tensors already resident in HBM.  The default workload is the
-Mixtral-8x7B-shaped decode step (H 4096, 8 experts x 4 sub-experts of 3584,
-64 one-token requests, k in {2,4,6,8}); its metric is microseconds per layer.
+the shared expert where the workload has one, as one moe_layer_forward.
+Inputs are seeded synthetic tensors already resident in HBM.  The default
+workload is the Mixtral-8x7B-shaped decode step (H 4096, 8 experts x 4
+sub-experts of 3584, 64 one-token requests, k in {2,4,6,8}); its metric is
+microseconds per layer.  Decode steps are timed as K layer calls in one CUDA
+graph over rotating copies of the weights (the activated weights of
+consecutive calls span at least 4x L2); prefill steps one per graph replay.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                   [--impl ours|reference]

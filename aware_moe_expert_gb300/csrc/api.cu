@@ -292,15 +292,31 @@ moe_status do_route(const moe_layer_desc* d, const void* x, const void* router_w
                                            status, s, bm));
 }
 
+// Counters of the fused decode FFN kernel (one per 64-row chunk, the work
+// counter, the split counters), zeroed by the launch that precedes the FFN.
+// Tokens per fused-decode-FFN item: 16 when no unit can hold more than 16
+// rows (T <= 16), else 64.
+inline int decode_ffn_chunk(const moe_layer_desc* d) { return d->T <= 16 ? 16 : 64; }
+inline int decode_ffn_chunks(const moe_layer_desc* d) {
+  return static_cast<int>(static_cast<long long>(d->T) * d->k_max / decode_ffn_chunk(d) +
+                          E_r_of(d) + 1);
+}
+inline int decode_ffn_counters(const moe_layer_desc* d) {
+  return decode_ffn_chunks(d) + 1 + moe::kFfnPartSlots / 2;
+}
+
+// zero_ffn: the permutation also zeroes the fused decode FFN's counters (the
+// layer forward, whose FFN then gathers its token rows itself).
 moe_status do_permute(const moe_layer_desc* d, const int32_t* topk_idx, const int32_t* kpt,
                       int32_t* counts, int32_t* offsets, int32_t* sorted_token,
                       int32_t* inv_row, int32_t* status, void* ws, cudaStream_t s,
-                      bool bitmap_ready = false) {
+                      bool bitmap_ready = false, bool zero_ffn = false) {
   const Layout l = layout_of(*d);
-  return cuda_status(moe::launch_permute(topk_idx, kpt, d->T, d->k_max, E_r_of(d),
-                                         at<uint32_t>(ws, l.bitmap), at<int32_t>(ws, l.wprefix),
-                                         counts, offsets, sorted_token, inv_row, status, s,
-                                         bitmap_ready));
+  return cuda_status(moe::launch_permute(
+      topk_idx, kpt, d->T, d->k_max, E_r_of(d), at<uint32_t>(ws, l.bitmap),
+      at<int32_t>(ws, l.wprefix), counts, offsets, sorted_token, inv_row, status, s,
+      bitmap_ready, zero_ffn ? at<int32_t>(ws, l.chunk_done) : nullptr,
+      zero_ffn ? decode_ffn_counters(d) : 0));
 }
 
 moe_status do_gate_up(const moe_layer_desc* d, const void* x, const int32_t* sorted_token,
@@ -421,25 +437,13 @@ moe_status do_down(const moe_layer_desc* d, const void* act, const int32_t* offs
 // Both FFN projections.  Decode-shaped batches with H and I_sub multiples of
 // 128 run the fused kernel (gate|up and down overlapped in one launch);
 // otherwise gate|up then down.
-// Counters of the fused decode FFN kernel (one per 64-row chunk, the work
-// counter, the split counters), zeroed by the launch that writes x_perm.
-// Tokens per fused-decode-FFN item: 16 when no unit can hold more than 16
-// rows (T <= 16), else 64.
-inline int decode_ffn_chunk(const moe_layer_desc* d) { return d->T <= 16 ? 16 : 64; }
-inline int decode_ffn_chunks(const moe_layer_desc* d) {
-  return static_cast<int>(static_cast<long long>(d->T) * d->k_max / decode_ffn_chunk(d) +
-                          E_r_of(d) + 1);
-}
-inline int decode_ffn_counters(const moe_layer_desc* d) {
-  return decode_ffn_chunks(d) + 1 + moe::kFfnPartSlots / 2;
-}
 
 // pre_gathered: x_perm already holds the permuted rows and the decode FFN's
 // counters are zero (the fused small-batch router wrote them).
 moe_status do_grouped_ffn(const moe_layer_desc* d, const void* x, const int32_t* sorted_token,
                           const int32_t* offsets, const void* w_gate_up, const void* w_down,
                           void* y_perm, int32_t* status, void* ws, cudaStream_t s,
-                          bool pre_gathered = false) {
+                          bool pre_gathered = false, bool gather_in_ffn = false) {
   const Layout l = layout_of(*d);
   void* act = at<void>(ws, l.act);
   const long long n_cap = static_cast<long long>(d->T) * d->k_max;
@@ -448,7 +452,9 @@ moe_status do_grouped_ffn(const moe_layer_desc* d, const void* x, const int32_t*
     const int E_r = E_r_of(d);
     void* xperm = at<void>(ws, l.xperm);
     int32_t* done = at<int32_t>(ws, l.chunk_done);
-    if (!pre_gathered)
+    // the counters are zeroed by the launch that precedes the FFN: the row
+    // gather, the fused router (pre_gathered) or the permutation (gather_in_ffn)
+    if (!pre_gathered && !gather_in_ffn)
       MOE_TRY(cuda_status(moe::launch_gather_rows(x, sorted_token, offsets, E_r, d->T, d->H,
                                                   static_cast<int>(n_cap), xperm, status,
                                                   sm_count(), s, done, decode_ffn_counters(d))));
@@ -472,6 +478,11 @@ moe_status do_grouped_ffn(const moe_layer_desc* d, const void* x, const int32_t*
     a.status = status;
     a.debug_flags = d->debug_flags;
     a.sm_count = sm_count();
+    if (gather_in_ffn) {
+      a.gather_x = x;
+      a.gather_tok = sorted_token;
+      a.gather_rows = d->T;
+    }
     return cuda_status(moe::launch_decode_ffn(a, s));
   }
   MOE_TRY(do_gate_up(d, x, sorted_token, offsets, w_gate_up, act, status, ws, s));
@@ -837,7 +848,7 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, const vo
   void* yperm = at<void>(workspace, l.yperm);
   void* ysh = desc->I_shared > 0 ? at<void>(workspace, l.ysh) : nullptr;
   const int E_r = E_r_of(desc);
-  bool gathered = false;
+  bool gathered = false, gather_in_ffn = false;
   if (desc->T <= moe::kRouteFuseMaxT && !router_on_tensor_cores(*desc) &&
       moe::route_cluster_supports(desc->H, E_r)) {
     // small batch: logits, top-k, permutation (and the row gather of the
@@ -855,12 +866,15 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, const vo
     bool bitmap_done = false;
     MOE_TRY(do_route(desc, x, router_w, nullptr, k_per_token, nullptr, topk_idx, topk_w,
                      dev_status, workspace, s, &bitmap_done));
+    // the fused decode FFN gathers its token rows itself; the permutation
+    // zeroes its counters (the shared expert, if any, touches neither)
+    gather_in_ffn = use_decode_ffn(desc);
     MOE_TRY(do_permute(desc, topk_idx, k_per_token, counts, offsets, sorted_token, inv_row,
-                       dev_status, workspace, s, bitmap_done));
+                       dev_status, workspace, s, bitmap_done, gather_in_ffn));
   }
   if (ysh != nullptr) MOE_TRY(do_shared(desc, x, ysh, dev_status, workspace, s));
   MOE_TRY(do_grouped_ffn(desc, x, sorted_token, offsets, w_gate_up, w_down, yperm, dev_status,
-                         workspace, s, gathered));
+                         workspace, s, gathered, gather_in_ffn));
   return do_combine(desc, yperm, ysh, inv_row, topk_w, k_per_token, out, dev_status, s);
 }
 

@@ -33,6 +33,7 @@ constexpr int kM = 128;
 constexpr int kGU = 64;                        // neurons per gate|up item
 constexpr int kTokBox = 16;
 constexpr int kThreads = 192;
+constexpr int kGatherThreads = 128;             // warps 6..9 of the row-gathering variant
 constexpr int kQ = 4;                          // item queue depth
 constexpr uint32_t kWSub = kM * kBK * 2;        // 16 KB per weight sub-block
 constexpr uint32_t kW = kWSub * kKsub;          // 32 KB
@@ -75,6 +76,9 @@ struct FParams {
   long long out_rows;
   int32_t* status;
   uint32_t debug_flags;
+  const uint4* gx;       // GATHER: gate|up token rows are gx[gtok[r]] (bf16 [*, H])
+  const int32_t* gtok;
+  int gx_rows;
 };
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
@@ -138,8 +142,14 @@ __device__ __forceinline__ Item item_of(int w, int n_gu, int S, int gu_tiles, in
   return it;
 }
 
-template <int CHUNK, int STAGES>
-__global__ void __launch_bounds__(kThreads, 1)
+// GATHER: four more warps copy the token rows of every gate|up stage straight
+// from x (row r of the chunk = token gtok[row0 + r]) into the swizzled token
+// buffer with cp.async, so no permuted copy of x is needed; they follow the
+// item queue like the MMA and epilogue warps, arrive on every stage's `full`
+// (copies for gate|up items, none for down items, whose activation rows come
+// by TMA), and the producer then loads only weights for gate|up items.
+template <int CHUNK, int STAGES, bool GATHER = false>
+__global__ void __launch_bounds__(GATHER ? kThreads + kGatherThreads : kThreads, 1)
     decode_ffn_kernel(const __grid_constant__ CUtensorMap tmWgu,
                       const __grid_constant__ CUtensorMap tmX16,
                       const __grid_constant__ CUtensorMap tmX64,
@@ -177,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // set-up that reads nothing upstream overlaps the previous launch's tail
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], GATHER ? 1 + kGatherThreads : 1);
       mbar_init(&empty[s], 1);
     }
     mbar_init(&tfull[0], 1);
@@ -187,7 +197,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(mma_done, 1);
     for (int q = 0; q < kQ; ++q) {
       mbar_init(&q_full[q], 1);
-      mbar_init(&q_empty[q], 5);   // the MMA thread and the four epilogue warps
+      // the MMA thread, the four epilogue warps (and the four gather warps)
+      mbar_init(&q_empty[q], GATHER ? 9 : 5);
     }
     *s_abort = 0;
     fence_barrier_init();
@@ -254,7 +265,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nb = (t.rows + kTokBox - 1) / kTokBox;
         const bool wide = nb > 2;
         const uint32_t tok_rows = wide ? 64u : static_cast<uint32_t>(nb * kTokBox);
-        const uint32_t bytes = kW + kKsub * tok_rows * kBK * 2;
+        const bool gathered = GATHER && it.gu;   // token rows come from the gather warps
+        const uint32_t bytes = gathered ? kW : kW + kKsub * tok_rows * kBK * 2;
         const int kb0 = it.gu ? it.s * KB_split : 0;
         const int kb1 = it.gu ? kb0 + KB_split : KB_dn;
         const CUtensorMap* mW = it.gu ? &tmWgu : &tmWdn;
@@ -329,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             mbar_expect_tx(&full[stage], bytes);
             weights(smem + stage * kW, kb);
-            tokens(smem + kOffB + stage * kTok, &full[stage], kb);
+            if (!gathered) tokens(smem + kOffB + stage * kTok, &full[stage], kb);
             issued |= 1u << stage;
             issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
           }
@@ -401,6 +413,131 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(mma_done, 0u, nullptr);
     }
     __syncwarp();
+  } else if (GATHER && warp >= 6) {
+    // Row gather of gate|up items: thread g copies 16-byte chunk (g % 8) of
+    // token rows g / 8 + 16 i (i < kChunk / 16) of both 64-column sub-blocks
+    // of every stage; the chunk lands at chunk ^ (row % 8) of its 128-byte
+    // row (the 128-byte swizzle of the TMA boxes it replaces).  A stage's
+    // copies are one cp.async group; once a group is LAG groups old the
+    // thread waits for it, orders it for the tensor cores' async-proxy reads
+    // and arrives on that stage's `full`.  Down-item stages (no copies) are
+    // arrived on at once.  Held-back arrivals are all made before a down item
+    // and before the thread has to wait for its next item: the producer
+    // publishes that item only after a down item's activations exist, which
+    // may need these very stages.
+    constexpr int LAG = kStages - 2;
+    constexpr int kRowsPer = kChunk / 16;
+    const int g = threadIdx.x - kThreads;
+    const int chunk = g & 7, rg = g >> 3;
+    const size_t nv = static_cast<size_t>(p.H) / 8;
+    int stage = 0, astage = 0, pending = 0;
+    uint32_t phase = 0;
+    bool ok = true, bad = false;
+    auto flush = [&]() {
+      if (pending > 0) {
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        fence_proxy_async_smem();
+        for (; pending > 0; --pending) {
+          mbar_arrive(&full[astage]);
+          if (++astage == kStages) astage = 0;
+        }
+      }
+    };
+    for (int i = 0; ok; ++i) {
+      const int slot = i % kQ;
+      int avail = 1;
+      if (lane == 0) avail = mbar_try_wait(&q_full[slot], (i / kQ) & 1) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, avail, 0)) flush();   // the producer may be waiting on them
+      int got = 1;
+      if (lane == 0) got = mbar_wait(&q_full[slot], (i / kQ) & 1, s_abort) ? 1 : 0;
+      got = __shfl_sync(0xffffffffu, got, 0);
+      if (!got) {
+        ok = false;
+        break;
+      }
+      int w = 0;
+      if (lane == 0) {
+        w = s_item[slot];
+        mbar_arrive(&q_empty[slot]);
+      }
+      w = __shfl_sync(0xffffffffu, w, 0);
+      if (w < 0) break;
+      const Item it = item_of(w, n_gu, S, p.gu_tiles, p.dn_tiles);
+      const Tile t = decode_tile<kChunk>(it.mt, 1, p.n_groups, s_prefix, s_offs);
+      const uint4* src[kRowsPer];
+#pragma unroll
+      for (int j = 0; j < kRowsPer; ++j) {
+        const int r = rg + 16 * j;
+        int tok = -1;
+        if (it.gu && r < t.rows) {
+          tok = __ldg(p.gtok + t.row0 + r);
+          if (tok < 0 || tok >= p.gx_rows) {
+            bad = true;
+            tok = -1;
+          }
+        }
+        src[j] = tok >= 0 ? p.gx + static_cast<size_t>(tok) * nv + chunk : nullptr;
+      }
+      if (!it.gu) {
+        flush();
+        for (int kb = 0; kb < KB_dn; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, s_abort)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive(&full[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        astage = stage;
+        continue;
+      }
+      const int kb0 = it.s * KB_split;
+      const int kb1 = kb0 + KB_split;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(&empty[stage], phase ^ 1u, s_abort)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sb = smem_u32(smem + kOffB + stage * kTok);
+#pragma unroll
+        for (int sub = 0; sub < kKsub; ++sub)
+#pragma unroll
+          for (int j = 0; j < kRowsPer; ++j) {
+            const int r = rg + 16 * j;
+            if (src[j] != nullptr)
+              asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                               sb + sub * kTokSub + r * 128 + ((chunk ^ (r & 7)) << 4)),
+                           "l"(src[j] + (kb * kKsub + sub) * (kBK / 8))
+                           : "memory");
+          }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        if (++pending > LAG) {
+          asm volatile("cp.async.wait_group %0;" ::"n"(LAG) : "memory");
+          fence_proxy_async_smem();
+          mbar_arrive(&full[astage]);
+          if (++astage == kStages) astage = 0;
+          --pending;
+        }
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    if (ok) {
+      fence_proxy_async_smem();
+      for (; pending > 0; --pending) {
+        mbar_arrive(&full[astage]);
+        if (++astage == kStages) astage = 0;
+      }
+    } else if (lane == 0) {
+      fail(s_abort, p.status);
+    }
+    if (bad) report(p.status, MOE_ERR_BAD_INDEX);
   } else {
     const int q = warp & 3;
     const int r_in = q * 32 + lane;
@@ -539,9 +676,12 @@ cudaError_t launch_decode_ffn(const DecodeFfnArgs& a, cudaStream_t s) {
   if (a.x_rows <= 0 || a.rows <= 0) return cudaSuccess;
   CUtensorMap wgu, x16, x64, wdn, a16, a64;
   const int E_r = a.n_groups;
+  // with the row gather the x_perm maps are unused; they then describe x
+  const void* xt = a.gather_x != nullptr ? a.gather_x : a.x_perm;
+  const long long xt_rows = a.gather_x != nullptr ? a.gather_rows : a.x_rows;
   if (!make_tmap_bf16(&wgu, a.w_gate_up, static_cast<long long>(E_r) * 2 * a.I, a.H, kGU) ||
-      !make_tmap_bf16(&x16, a.x_perm, a.x_rows, a.H, kTokBox) ||
-      !make_tmap_bf16(&x64, a.x_perm, a.x_rows, a.H, 64) ||
+      !make_tmap_bf16(&x16, xt, xt_rows, a.H, kTokBox) ||
+      !make_tmap_bf16(&x64, xt, xt_rows, a.H, 64) ||
       !make_tmap_bf16(&wdn, a.w_down, static_cast<long long>(E_r) * a.H, a.I, kM) ||
       !make_tmap_bf16(&a16, a.act, a.rows, a.I, kTokBox) ||
       !make_tmap_bf16(&a64, a.act, a.rows, a.I, 64))
@@ -562,8 +702,22 @@ cudaError_t launch_decode_ffn(const DecodeFfnArgs& a, cudaStream_t s) {
   p.out_rows = a.rows;
   p.status = a.status;
   p.debug_flags = a.debug_flags;
+  p.gx = static_cast<const uint4*>(a.gather_x);
+  p.gtok = a.gather_tok;
+  p.gx_rows = a.gather_rows;
+  const bool gather = a.gather_x != nullptr;
+  if (gather && a.gather_tok == nullptr) return cudaErrorInvalidValue;
   if (a.chunk == 16) {
     using Cfg = FfnCfg<16, 6>;
+    if (gather) {
+      static bool attr_done[64] = {false};
+      cudaError_t e = set_smem_once(decode_ffn_kernel<16, 6, true>,
+                                    static_cast<int>(Cfg::kSmemBytes), attr_done);
+      if (e != cudaSuccess) return e;
+      return launch_pdl(decode_ffn_kernel<16, 6, true>, dim3(a.sm_count),
+                        dim3(kThreads + kGatherThreads), Cfg::kSmemBytes, s, wgu, x16, x64, wdn,
+                        a16, a64, p);
+    }
     static bool attr_done[64] = {false};
     cudaError_t e = set_smem_once(decode_ffn_kernel<16, 6>, static_cast<int>(Cfg::kSmemBytes),
                                   attr_done);
@@ -572,6 +726,15 @@ cudaError_t launch_decode_ffn(const DecodeFfnArgs& a, cudaStream_t s) {
                       Cfg::kSmemBytes, s, wgu, x16, x64, wdn, a16, a64, p);
   }
   using Cfg = FfnCfg<64, 4>;
+  if (gather) {
+    static bool attr_done[64] = {false};
+    cudaError_t e = set_smem_once(decode_ffn_kernel<64, 4, true>,
+                                  static_cast<int>(Cfg::kSmemBytes), attr_done);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(decode_ffn_kernel<64, 4, true>, dim3(a.sm_count),
+                      dim3(kThreads + kGatherThreads), Cfg::kSmemBytes, s, wgu, x16, x64, wdn,
+                      a16, a64, p);
+  }
   static bool attr_done[64] = {false};
   cudaError_t e = set_smem_once(decode_ffn_kernel<64, 4>, static_cast<int>(Cfg::kSmemBytes),
                                 attr_done);

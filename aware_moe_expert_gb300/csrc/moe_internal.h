@@ -89,11 +89,13 @@ cudaError_t launch_paths_rows(const int32_t* n_paths, const int32_t* slot, const
 
 // ---- permute.cu
 // bitmap_ready: the top-k kernel already wrote `bitmap` (T > 256 only).
+// Also zeroes zero_ptr[0, zero_n) (counters of the kernel that follows).
 cudaError_t launch_permute(const int32_t* topk_idx, const int32_t* k_per_token, int T,
                            int k_max, int E_r, uint32_t* bitmap, int32_t* wprefix,
                            int32_t* counts, int32_t* offsets, int32_t* sorted_token,
                            int32_t* inv_row, int32_t* status, cudaStream_t s,
-                           bool bitmap_ready = false);
+                           bool bitmap_ready = false, int32_t* zero_ptr = nullptr,
+                           int zero_n = 0);
 // T above which launch_permute builds the bitmap (below: one CTA, no bitmap)
 constexpr int kPermuteBitmapMinT = 257;
 // also zeroes zero_ptr[0, zero_n) (counters for the kernel that follows)
@@ -193,6 +195,9 @@ struct DecodeFfnArgs {
   int32_t* status;
   uint32_t debug_flags;
   int sm_count;
+  const void* gather_x;      // non-null: gate|up items copy their token rows from
+  const int32_t* gather_tok; //   gather_x[gather_tok[r]] (bf16 [gather_rows, H]) instead
+  int gather_rows;           //   of reading x_perm
 };
 
 cudaError_t launch_decode_ffn(const DecodeFfnArgs& a, cudaStream_t s);

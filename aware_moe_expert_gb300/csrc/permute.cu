@@ -112,9 +112,12 @@ __global__ void __launch_bounds__(256) scatter_kernel(
     const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ kpt, int T, int k_max,
     int E_r, int W, const uint32_t* __restrict__ bitmap, const int32_t* __restrict__ wprefix,
     const int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-    int32_t* __restrict__ sorted_token, int32_t* __restrict__ inv_row) {
+    int32_t* __restrict__ sorted_token, int32_t* __restrict__ inv_row,
+    int32_t* __restrict__ zero_ptr, int zero_n) {
   __shared__ int32_t s_off[257];
   pdl_wait_and_trigger();
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < zero_n; i += gridDim.x * blockDim.x)
+    zero_ptr[i] = 0;
   if (threadIdx.x < 32) scan_counts(counts, E_r, s_off, threadIdx.x);
   __syncthreads();
   if (blockIdx.x == 0)
@@ -173,7 +176,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
 __global__ void __launch_bounds__(1024) permute_small_kernel(
     const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ kpt, int T, int k_max,
     int E_r, int W, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-    int32_t* __restrict__ sorted_token, int32_t* __restrict__ inv_row, int32_t* status) {
+    int32_t* __restrict__ sorted_token, int32_t* __restrict__ inv_row, int32_t* status,
+    int32_t* __restrict__ zero_ptr, int zero_n) {
   extern __shared__ uint32_t sm[];
   uint32_t* bits = sm;
   int32_t* pre = reinterpret_cast<int32_t*>(sm + E_r * W);
@@ -181,6 +185,7 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(
   int32_t* s_off = s_cnt + 256;
   pdl_wait_and_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int i = tid; i < zero_n; i += blockDim.x) zero_ptr[i] = 0;
   for (int i = tid; i < E_r * W; i += blockDim.x) bits[i] = 0u;
   __syncthreads();
   const int slots = T * k_max;
@@ -260,7 +265,7 @@ cudaError_t launch_permute(const int32_t* topk_idx, const int32_t* k_per_token, 
                            int k_max, int E_r, uint32_t* bitmap, int32_t* wprefix,
                            int32_t* counts, int32_t* offsets, int32_t* sorted_token,
                            int32_t* inv_row, int32_t* status, cudaStream_t s,
-                           bool bitmap_ready) {
+                           bool bitmap_ready, int32_t* zero_ptr, int zero_n) {
   const int W = (T + 31) / 32;
   static_assert(kPermuteBitmapMinT == 8 * 32 + 1, "the one-CTA path takes W <= 8");
   if (W > 0 && W <= 8) {
@@ -269,7 +274,8 @@ cudaError_t launch_permute(const int32_t* topk_idx, const int32_t* k_per_token, 
     cudaError_t e = set_smem_once(permute_small_kernel, (2 * 256 * 8 + 256 + 257) * 4, attr_done);
     if (e != cudaSuccess) return e;
     return launch_pdl(permute_small_kernel, dim3(1), dim3(1024), smem, s, topk_idx, k_per_token,
-                      T, k_max, E_r, W, counts, offsets, sorted_token, inv_row, status);
+                      T, k_max, E_r, W, counts, offsets, sorted_token, inv_row, status, zero_ptr,
+                      zero_n);
   }
   if (W > 0 && !bitmap_ready) {
     cudaError_t e = launch_pdl(bitmap_kernel, dim3(W), dim3(256), 0, s, topk_idx, k_per_token, T,
@@ -284,7 +290,7 @@ cudaError_t launch_permute(const int32_t* topk_idx, const int32_t* k_per_token, 
   e = launch_pdl(scatter_kernel, dim3(blocks), dim3(256), 0, s, topk_idx, k_per_token, T, k_max,
                  E_r, W, static_cast<const uint32_t*>(bitmap),
                  static_cast<const int32_t*>(wprefix), static_cast<const int32_t*>(counts),
-                 offsets, sorted_token, inv_row);
+                 offsets, sorted_token, inv_row, zero_ptr, zero_n);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

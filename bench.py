@@ -643,9 +643,9 @@ def launches_per_step(wl, T, path=0, fold=False, cg=False):
     sequencing in csrc/api.cu: router + top-k (one cluster launch on CUDA
     cores, or the tensor-core GEMM and the top-k kernel), permutation (fused
     into the router launch for <= 8 tokens; above 256 tokens the top-k kernel
-    also writes its bitmap), [folding], [shared expert], gate|up (+ the
-    split-K reduction of the weight-stationary family), down (+ its split
-    reduction), combine)."""
+    also writes its bitmap), [folding], [shared expert], the fused decode FFN
+    or gate|up (+ the split-K reduction of the weight-stationary family) and
+    down (+ its split reduction), combine)."""
     n_cap = T * wl.k_max
     decode = path == 2 or (path == 0 and n_cap <= 64 * wl.E_r)
     budget = 256 << 20
@@ -664,7 +664,9 @@ def launches_per_step(wl, T, path=0, fold=False, cg=False):
     n += 4 if fold else 0                            # fold: scores, pool, target map, remap
     n += 2 if wl.I_shared else 0                     # shared expert gate|up, down
     if decode_ffn:
-        n += 1 if fused_front else 2                 # (row gather +) fused decode FFN kernel
+        # fused decode FFN; it gathers its token rows itself inside
+        # moe_layer_forward, the fold and proxy-router layers run the row gather
+        n += 1 if (fused_front or not (fold or cg)) else 2
     else:
         # gate|up GEMM; the decode family reads a gathered copy of x, the
         # prefill kernel gathers its rows itself

@@ -65,3 +65,36 @@ def test_skipped_load_times_out_and_context_survives(path):
     ref = O.layer_forward(spec_of(desc), bf16_bits(x), None, unit_fetch(wgu), unit_fetch(wd),
                           k.cpu().numpy(), logits=L.cpu().numpy())
     assert_close_layer(y[: ref["n_assign"]].to(torch.float64).cpu().numpy(), ref["y_perm"])
+
+
+def test_layer_forward_gathering_ffn_times_out_and_context_survives():
+    """The same through moe_layer_forward, whose fused decode FFN gathers its
+    token rows itself (four more warps on the stage barriers): the skipped
+    load must still end every wait, and a normal call afterwards is right."""
+    desc, x, wgu, wd, L, k = _setup(B.PATH_DECODE, B.DEBUG_SKIP_FIRST_LOAD)
+    g = torch.Generator(device=DEV).manual_seed(9)
+    router_w = (torch.randn(desc.E_r, desc.H, generator=g, device=DEV)
+                / math.sqrt(desc.H)).to(torch.bfloat16)
+    ws = torch.empty(B.moe_workspace_size(desc), dtype=torch.uint8, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = torch.empty(desc.T, desc.H, dtype=torch.bfloat16, device=DEV)
+    B.check(B.moe_layer_forward(desc, x, router_w, wgu, wd, k, out, st, ws))
+    assert B.moe_get_device_status(st) == 5                    # MOE_ERR_DEVICE_TIMEOUT
+    desc.debug_flags = 0
+    st.zero_()
+    B.check(B.moe_layer_forward(desc, x, router_w, wgu, wd, k, out, st, ws))
+    assert B.moe_get_device_status(st) == 0
+    ref = O.layer_forward(spec_of(desc), bf16_bits(x), bf16_bits(router_w), unit_fetch(wgu),
+                          unit_fetch(wd), k.cpu().numpy())
+    got = out.to(torch.float64).cpu().numpy()
+    # fp32 GPU logits vs fp64 oracle logits: compare tokens away from near ties
+    from parity_utils import tie_safe_tokens
+    Lg = torch.empty(desc.T, desc.E_r, dtype=torch.float32, device=DEV)
+    idx = torch.empty(desc.T, desc.k_max, dtype=torch.int32, device=DEV)
+    w = torch.empty(desc.T, desc.k_max, dtype=torch.float32, device=DEV)
+    B.check(B.moe_route(desc, x, router_w, None, k, Lg, idx, w, st, ws))
+    L64 = ref["logits"]
+    delta = 2.0 * np.abs(Lg.cpu().numpy().astype(np.float64) - L64).max(axis=1) + 1e-7
+    ok, n_tied = tie_safe_tokens(L64, idx.cpu().numpy(), k.cpu().numpy(), delta)
+    assert n_tied <= 2
+    assert_close_layer(got[ok], ref["out"][ok], "out")

@@ -1,6 +1,8 @@
-"""The layer at the largest routing budget the ABI accepts: k_max = 32 over
-E_r = 256 units, every token at k_t = 32 (MoE-Prism §III-C1: a request's
-budget can be any number of sub-experts up to the layer's maximum).
+"""Edge cases of the whole layer against the oracle.
+
+The largest routing budget the ABI accepts: k_max = 32 over E_r = 256 units,
+every token at k_t = 32 (MoE-Prism §III-C1: a request's budget can be any
+number of sub-experts up to the layer's maximum).
 
 The Qwen3-30B-A3B-shaped decode layer (H 2048, 128 experts x 2 sub-experts of
 384) at four token counts exercises every kernel family at that budget: the
@@ -10,6 +12,9 @@ the bitmap permutation (T = 300), and the tensor-core router, the top-k
 kernel writing the bitmap and the prefill grouped GEMMs (T = 1024, where
 T * k_max exceeds 64 * E_r).  Every token is compared with the oracle up to
 T = 64; above, a seeded sample with the first and last token.
+
+The degenerate layers with a single expert (one unit at k = 1; one expert
+split four ways, all selected), and a shared expert at decode token counts.
 """
 from dataclasses import replace
 
@@ -47,3 +52,35 @@ def test_layer_at_k_max_32_both_families(path):
     """The same budget forced onto each grouped-GEMM family (T = 64)."""
     wl, d, desc, out, Lg, idx = _run_layer(K32, T=64, path=path)
     _compare(wl, d, desc, out, Lg, idx, np.arange(64))
+
+
+# The degenerate layer: one routing unit, k = 1, so every token's gate is 1
+# (softmax over a single logit) and the layer is one dense SwiGLU FFN.
+ONE_UNIT = replace(WL.TINY, name="one-unit-h256-i128", n_experts=1, n_sub=1, k_max=1,
+                   k_choices=(1,))
+# One expert split into four sub-experts, all four selected by every token:
+# the gate-weighted sum of the slices (MoE-Prism §III-B1 Eq. (3) with
+# softmax gates).
+ONE_EXPERT_SPLIT = replace(WL.TINY, name="one-expert-x4-h256-i128", n_experts=1, n_sub=4,
+                           k_max=4, k_choices=(4,))
+
+
+@pytest.mark.parametrize("wl", [ONE_UNIT, ONE_EXPERT_SPLIT], ids=lambda w: w.name)
+@pytest.mark.parametrize("T", [1, 8, 200])
+def test_layer_with_a_single_expert(wl, T):
+    wl, d, desc, out, Lg, idx = _run_layer(wl, T=T)
+    _compare(wl, d, desc, out, Lg, idx, np.arange(T))
+
+
+# DeepSeek-V3-shaped layer (H 7168, I_sub 2048, a shared expert, sigmoid
+# scores renormalised over the selection) with 16 routed experts, at decode
+# token counts: the shared expert's dense GEMMs on a handful of rows and the
+# fused decode FFN at H = 7168.
+DEEPSEEK_SMALL = replace(WL.DEEPSEEK_PREFILL, name="deepseek-v3-shape-e16-decode", n_experts=16,
+                         tokens_per_request=1, phase="decode")
+
+
+@pytest.mark.parametrize("T", [1, 5, 64])
+def test_layer_shared_expert_at_decode_sizes(T):
+    wl, d, desc, out, Lg, idx = _run_layer(DEEPSEEK_SMALL, T=T)
+    _compare(wl, d, desc, out, Lg, idx, np.arange(T))

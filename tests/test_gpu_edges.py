@@ -14,7 +14,8 @@ T * k_max exceeds 64 * E_r).  Every token is compared with the oracle up to
 T = 64; above, a seeded sample with the first and last token.
 
 The degenerate layers with a single expert (one unit at k = 1; one expert
-split four ways, all selected), and a shared expert at decode token counts.
+split four ways, all selected), every unit selected by every token (k =
+E_r), and a shared expert at decode token counts.
 """
 from dataclasses import replace
 
@@ -83,4 +84,19 @@ DEEPSEEK_SMALL = replace(WL.DEEPSEEK_PREFILL, name="deepseek-v3-shape-e16-decode
 @pytest.mark.parametrize("T", [1, 5, 64])
 def test_layer_shared_expert_at_decode_sizes(T):
     wl, d, desc, out, Lg, idx = _run_layer(DEEPSEEK_SMALL, T=T)
+    _compare(wl, d, desc, out, Lg, idx, np.arange(T))
+
+
+# Every token selects every unit (k = E_r = 32): the dense gate-weighted
+# mixture of all sub-experts (MoE-Prism §II, Eq. (2) with k = all), every
+# unit serving all T tokens.
+ALL_UNITS = replace(WL.TINY, name="all-units-e8x4-h256", n_experts=8, n_sub=4, k_max=32,
+                    k_choices=(32,))
+
+
+@pytest.mark.parametrize("T", [1, 64, 200])
+def test_layer_with_every_unit_selected(T):
+    wl, d, desc, out, Lg, idx = _run_layer(ALL_UNITS, T=T)
+    sel = np.sort(idx.cpu().numpy(), axis=1)
+    assert (sel == np.arange(32)[None, :]).all()
     _compare(wl, d, desc, out, Lg, idx, np.arange(T))

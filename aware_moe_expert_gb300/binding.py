@@ -259,7 +259,9 @@ def moe_combine(desc, y_perm, y_shared, inv_row, topk_w, k_per_token, out, dev_s
 
 def moe_layer_forward(desc, x, router_w, w_gate_up, w_down, k_per_token, out, dev_status,
                       workspace, stream=None) -> int:
-    d = desc.c()
+    """desc: a LayerDesc, or the MoeLayerDesc its c() returned (a serving loop
+    can build that once and skip the conversion on every call)."""
+    d = desc if isinstance(desc, MoeLayerDesc) else desc.c()
     return lib().moe_layer_forward(ctypes.byref(d), _ptr(x), _ptr(router_w), _ptr(w_gate_up),
                                    _ptr(w_down), _ptr(k_per_token), _ptr(out), _ptr(dev_status),
                                    _ptr(workspace), _stream(stream))

@@ -15,7 +15,8 @@ T = 64; above, a seeded sample with the first and last token.
 
 The degenerate layers with a single expert (one unit at k = 1; one expert
 split four ways, all selected), every unit selected by every token (k =
-E_r), and a shared expert at decode token counts.
+E_r), a shared expert at decode token counts, and 9 to 16 tokens (the fused
+decode FFN's 16-token chunks gathering their own rows).
 """
 from dataclasses import replace
 
@@ -99,4 +100,14 @@ def test_layer_with_every_unit_selected(T):
     wl, d, desc, out, Lg, idx = _run_layer(ALL_UNITS, T=T)
     sel = np.sort(idx.cpu().numpy(), axis=1)
     assert (sel == np.arange(32)[None, :]).all()
+    _compare(wl, d, desc, out, Lg, idx, np.arange(T))
+
+
+@pytest.mark.parametrize("name,T", [("qwen_decode", 9), ("qwen_decode", 12), ("qwen_decode", 16),
+                                    ("mixtral_decode", 16), ("tiny", 9)])
+def test_layer_between_the_cluster_router_and_64_token_chunks(name, T):
+    """9 to 16 tokens: routed and permuted by the general kernels (more than
+    one cluster's eight tokens), then the fused decode FFN with 16-token
+    chunks that gathers its token rows from x itself."""
+    wl, d, desc, out, Lg, idx = _run_layer(WL.ALL[name], T=T)
     _compare(wl, d, desc, out, Lg, idx, np.arange(T))

@@ -131,7 +131,8 @@ def test_full_size_routing_and_permutation_bit_exact(name):
                                     ("qwen_decode", 300), ("mixtral_decode", None),
                                     ("qwen_decode", 1), ("qwen_decode", 8), ("mixtral_decode", 5),
                                     ("tiny", 7), ("tiny_i192", 4), ("tiny", 1000),
-                                    ("qwen_decode", 1024)])
+                                    ("qwen_decode", 1024), ("qwen_decode", 12),
+                                    ("mixtral_decode", 16), ("tiny", 9)])
 def test_layer_forward_equals_component_calls(name, T):
     """moe_layer_forward gives bit-identical results to moe_route ->
     moe_permute -> moe_grouped_ffn -> moe_combine on the same inputs (for

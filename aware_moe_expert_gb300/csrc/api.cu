@@ -730,6 +730,10 @@ moe_status do_route_cg(const moe_layer_desc* d, const moe_cg_router* cg, const v
 
 }  // namespace
 
+namespace moe {
+moe_status validate_desc(const moe_layer_desc* d) { return validate(d); }
+}  // namespace moe
+
 extern "C" {
 
 size_t moe_workspace_size(const moe_layer_desc* desc) {

@@ -7,7 +7,14 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/moe.h"
+
 namespace moe {
+
+// ---- api.cu
+// Host validation of a layer descriptor: the status every entry point of
+// include/moe.h returns for an invalid or unsupported descriptor.
+moe_status validate_desc(const moe_layer_desc* d);
 
 // ---- route.cu
 // Partial logits P[s, t, u] over router_slices(T, H, E_r) slices of the

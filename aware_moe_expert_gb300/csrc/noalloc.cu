@@ -62,10 +62,9 @@ extern "C" moe_status moe_permute_static(const moe_layer_desc* desc, const int32
                                          const int32_t* k_per_token, int32_t* counts,
                                          int32_t* offsets, int32_t* sorted_token,
                                          int32_t* inv_row, int32_t* dev_status, void* stream) {
-  // moe_workspace_size returns 0 exactly when the desc is invalid or unsupported
-  if (desc == nullptr || moe_workspace_size(desc) == 0) {
-    return desc == nullptr ? MOE_ERR_INVALID_ARGUMENT : MOE_ERR_UNSUPPORTED_SHAPE;
-  }
+  // the same descriptor checks, with the same status, as moe_permute
+  const moe_status v = moe::validate_desc(desc);
+  if (v != MOE_OK) return v;
   if (!aligned4(counts) || !aligned4(offsets) || !aligned4(dev_status))
     return MOE_ERR_INVALID_ARGUMENT;
   if (desc->T > 0 && (!aligned4(topk_idx) || !aligned4(k_per_token) || !aligned4(sorted_token) ||

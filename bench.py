@@ -4,19 +4,26 @@ A step is one pass of the whole hot path over one batch: router logits and
 top-k_t (moe_route), permutation (moe_permute), grouped gate|up + SwiGLU
 (moe_gate_up), grouped down (moe_down), weighted combine (moe_combine), plus
 the shared expert where the workload has one, as one moe_layer_forward.
-Inputs are seeded synthetic tensors already resident in HBM.  The default
+Inputs are seeded synthetic tensors already resident in HBM.  The headline
 workload is the Mixtral-8x7B-shaped decode step (H 4096, 8 experts x 4
 sub-experts of 3584, 64 one-token requests, k in {2,4,6,8}); its metric is
 microseconds per layer.  Decode steps are timed as K layer calls in one CUDA
 graph over rotating copies of the weights (the activated weights of
 consecutive calls span at least 4x L2); prefill steps one per graph replay.
 
+With no --workload the line's value is the headline workload's, and every
+workload (tiny; Mixtral-8x7B-shaped decode; Qwen3-30B-A3B-shaped prefill;
+Qwen3-30B-A3B-shaped decode at T = 1, 8, 64, 256, 1024; DeepSeek-V3-shaped
+prefill) is run the same way, one after the other, and summarised in the
+line's "workloads" object (value, roofline, realised routing, clocks, e2e).
+
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                  [--impl ours|reference]
+                  [--impl ours|reference] [--profile-calls N]
 
 --impl reference times the fp64 CPU oracle on the host cores on a bounded
-sample of the same workload.  Under torchrun (N > 1) every rank runs an
+sample of the headline workload.  Under torchrun (N > 1) every rank runs an
 independent replica (the layer has no exchange step); rank 0 prints.
+--profile-calls N makes N untimed layer calls on one weight copy (for ncu).
 """
 from __future__ import annotations
 
@@ -46,7 +53,14 @@ def parse():
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=30)
     p.add_argument("--warmup", type=int, default=5)
-    p.add_argument("--workload", default="mixtral_decode")
+    p.add_argument("--workload", default=None,
+                   help="one workload only (default: the Mixtral-8x7B-shaped decode step as the "
+                        "headline line, then every other workload into its 'workloads' object)")
+    p.add_argument("--no-sweep", action="store_true",
+                   help="headline workload only (no 'workloads' object)")
+    p.add_argument("--profile-calls", type=int, default=0,
+                   help="N > 0: no timing; build the workload's inputs (one weight copy), make N "
+                        "moe_layer_forward calls and check the device status (for ncu captures)")
     p.add_argument("--T", type=int, default=None, help="override the token count")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -196,9 +210,6 @@ def run_ours(args, wl, rank, world, local):
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
     d = make_layer_inputs(wl, dev, seed=wl.seed + 1000 * rank)
     if args.k_normal is not None:
         from aware_moe_expert_gb300.inputs import draw_k_normal
@@ -965,10 +976,54 @@ def run_paths(args, wl, rank, world, local):
             "expansion_flops_saved": 4.0 * H * wl.I_sub * (n_paths - n_exp)}
 
 
+# The default run: the headline workload first (the line's own value), then
+# every other workload, each summarised in the line's "workloads" object.
+SWEEP = [("mixtral_decode", None), ("tiny", None), ("qwen_prefill", None),
+         ("qwen_decode", 1), ("qwen_decode", 8), ("qwen_decode", 64), ("qwen_decode", 256),
+         ("qwen_decode", 1024), ("deepseek_prefill", None)]
+
+
+def workload_summary(res):
+    """The per-workload entry of the sweep: value, roofline, realised routing,
+    clocks and the end-to-end number of one run_ours result."""
+    keep = ("value", "unit", "higher_is_better", "ms_per_step", "roofline", "roofline_layer",
+            "realised", "clocks", "e2e", "breakdown_us", "gpu_launches")
+    out = {k: res[k] for k in keep if k in res}
+    out["config"] = {k: res["config"][k] for k in ("workload", "T", "l2") if k in res["config"]}
+    return out
+
+
+def profile_calls(args, wl, local):
+    """--profile-calls N: N layer calls on one weight copy, nothing timed."""
+    import torch
+    from aware_moe_expert_gb300 import binding as B
+    from aware_moe_expert_gb300.inputs import make_layer_inputs
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    d = make_layer_inputs(wl, dev)
+    desc = B.desc_for(wl, expert_bias=d["expert_bias"], w_shared_gate_up=d.get("w_shared_gate_up"),
+                      w_shared_down=d.get("w_shared_down"))
+    desc.path = args.path
+    if args.force_pair:
+        desc.debug_flags |= B.DEBUG_FORCE_PAIR
+    layer = B.MoeLayer(desc, dev)
+    for _ in range(args.profile_calls):
+        layer.forward(d["x"], d["router_w"], d["w_gate_up"], d["w_down"], d["k_per_token"])
+    torch.cuda.synchronize(dev)
+    code = layer.device_status()
+    return {"mode": "profile-calls", "workload": wl.name, "calls": args.profile_calls,
+            "device_status": B.STATUS_NAMES.get(code, code),
+            "gb_allocated": round(torch.cuda.max_memory_allocated(dev) / 1e9, 2)}, code
+
+
 def main():
     args = parse()
     from aware_moe_expert_gb300 import workloads as WL
-    wl = WL.ALL[args.workload]
+    sweep = args.workload is None and not args.no_sweep and args.T is None and \
+        args.impl == "ours" and not (args.tiered or args.paths or args.profile_calls) and \
+        args.router == "linear" and args.fold == 0 and args.k_mode == "exact" and \
+        args.k_normal is None and args.path == 0 and not args.force_pair
+    wl = WL.ALL[args.workload or "mixtral_decode"]
     if args.T is not None:
         wl = wl.with_T(args.T)
     rank, world, local = dist_info()
@@ -977,15 +1032,36 @@ def main():
         if res is not None:
             print(json.dumps(res), flush=True)
         return
+    if args.profile_calls:
+        res, code = profile_calls(args, wl, local)
+        print(json.dumps(res), flush=True)
+        raise SystemExit(0 if code == 0 else 1)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     if args.tiered or args.paths:
         res = (run_tiered if args.tiered else run_paths)(args, wl, rank, world, local)
         if rank == 0:
             print(json.dumps(res), flush=True)
         return
     res, d = run_ours(args, wl, rank, world, local)
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline_entry(wl, d, args.cpu_budget_s)
+    del d
+    if sweep:
+        import torch
+        res["workloads"] = {wl.name: workload_summary(res)}
+        launches = res["gpu_launches"]
+        for name, T in SWEEP[1:]:
+            torch.cuda.empty_cache()
+            w2 = WL.ALL[name] if T is None else WL.ALL[name].with_T(T)
+            r2, d2 = run_ours(args, w2, rank, world, local)
+            del d2
+            res["workloads"][w2.name] = workload_summary(r2)
+            launches += r2["gpu_launches"]
+        res["gpu_launches_all_workloads"] = launches
     if rank == 0:
-        if not args.no_cpu_baseline:
-            res["cpu_baseline"] = cpu_baseline_entry(wl, d, args.cpu_budget_s)
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -127,3 +127,16 @@ def test_cg_rejects_too_many_proxy_pairs(lib):
     # m * n_sub * r = 4 * 4 * 129 > 2048
     assert B.moe_cg_workspace_size(_desc(I_sub=256), _cg(m=4, r=129)) == 0
     assert B.moe_cg_workspace_size(_desc(I_sub=256), _cg(m=4, r=128)) > 0
+
+
+@pytest.mark.parametrize("kw,status", [(dict(T=-1), 1), (dict(k_max=0), 1), (dict(H=100), 2),
+                                       (dict(n_experts=65, n_sub=4), 2)])
+def test_static_scratch_permute_reports_what_moe_permute_reports(lib, kw, status):
+    """moe_permute_static checks the descriptor exactly as moe_permute does,
+    before any CUDA call: invalid (1) and unsupported (2) descriptors give
+    the same status from both."""
+    fake = 1 << 20
+    ws = 1 << 21
+    d = _desc(**kw)
+    assert B.moe_permute(d, fake, fake, fake, fake, fake, fake, fake, ws, 0) == status
+    assert B.moe_permute_static(d, fake, fake, fake, fake, fake, fake, fake, 0) == status

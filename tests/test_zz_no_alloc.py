@@ -36,8 +36,11 @@ def _outputs(T, E_r, k_max):
             torch.zeros(1, dtype=torch.int32, device=DEV))
 
 
-@pytest.mark.parametrize("T,E_r,k_max", [(300, 256, 8), (16384, 256, 8), (4097, 32, 8),
-                                         (100, 64, 8)])
+# (16384, 256, 8) is the exact-fit boundary: 2 * 256 units * 512 words * 4 bytes
+# = 1 MiB, the whole array (one token more is refused, below).
+@pytest.mark.parametrize("T,E_r,k_max", [(300, 256, 8),
+                                         pytest.param(16384, 256, 8, id="exact-fit-1MiB"),
+                                         (4097, 32, 8), (100, 64, 8)])
 def test_static_scratch_permute_matches_workspace_permute(T, E_r, k_max):
     desc = B.LayerDesc(T=T, H=64, n_experts=E_r, n_sub=1, I_sub=64, k_max=k_max)
     ws = torch.empty(B.moe_workspace_size(desc), dtype=torch.uint8, device=DEV)

@@ -322,6 +322,61 @@ def layer_forward(spec: LayerSpec, x, router_w, w_gate_up, w_down, k_per_token,
                 n_assign=n_assign)
 
 
+def layer_forward_routings(spec: LayerSpec, x, router_w, w_gate_up, w_down, k_per_token,
+                           expert_bias=None, logits_list=(None,), w_shared_gate_up=None,
+                           w_shared_down=None) -> list:
+    """layer_forward for several routings of the same tokens at once.
+
+    Each entry of ``logits_list`` fixes one routing: None routes on the
+    float64 logits of step 1, an array routes on those logits (e.g. a GPU's
+    fp32 logits).  Steps 2-3 run per routing; the SwiGLU FFN of every
+    (token, unit) pair that any routing selects is evaluated once (no
+    intermediate rounding) and each routing combines its own selection with
+    its own gates, plus the shared expert with weight 1.  Returns one dict per
+    routing: out, logits, topk_idx, topk_w, flags.
+    """
+    X = bf16_to_f64(x)
+    T, H = X.shape
+    assert T == spec.T and H == spec.H
+    L64 = None
+    routes = []
+    for lg in logits_list:
+        if lg is None:
+            if L64 is None:
+                L64 = router_logits(X, router_w, expert_bias, spec.n_sub)
+            routes.append(route(spec, logits=L64, k_per_token=k_per_token))
+        else:
+            routes.append(route(spec, logits=lg, k_per_token=k_per_token))
+    need = {}
+    for _, idx, _, _ in routes:
+        for t in range(T):
+            for j in range(spec.k_max):
+                u = int(idx[t, j])
+                if u >= 0:
+                    need.setdefault(u, set()).add(t)
+    y = {}
+    for u in sorted(need):
+        rows = sorted(need[u])
+        Y = swiglu_ffn(X[rows], _unit(w_gate_up, u), _unit(w_down, u))
+        for r, t in enumerate(rows):
+            y[(t, u)] = Y[r]
+    y_shared = None
+    if spec.I_shared > 0:
+        y_shared = swiglu_ffn(X, bf16_to_f64(w_shared_gate_up), bf16_to_f64(w_shared_down))
+    results = []
+    for L, idx, w, flags in routes:
+        out = np.zeros((T, H), dtype=np.float64)
+        for t in range(T):
+            for j in range(spec.k_max):
+                u = int(idx[t, j])
+                if u >= 0:
+                    out[t] += w[t, j] * y[(t, u)]
+        if y_shared is not None:
+            out += y_shared
+        results.append(dict(out=out, logits=L, topk_idx=idx, topk_w=w, flags=flags))
+    return results
+
+
 def coarse_k(k_qos: int, n_sub: int) -> int:
     """k_exec = N * ceil(k_qos / N): the budget a whole-expert layout must run
     to meet a target given in sub-expert units.  [Prism] §V-D1."""

@@ -1,12 +1,19 @@
 """End-to-end parity of moe_layer_forward on the five synthetic workloads.
 
-The GPU computes router logits in fp32 and the oracle in float64, so a token
-whose k-th and (k+1)-th logits nearly tie may legitimately select a
-different unit; such tokens must be genuine near ties (checked) and are left
-out of the element comparison.  Small workloads compare every token; the two
-large prefill workloads compare a seeded sample of tokens (the oracle runs
-on that sample: tokens are independent) plus properties that hold at any
-size (routing and permutation bit-exact from generator-given logits).
+Two comparisons per case, both against the fp64 oracle:
+  1. on the GPU's own fp32 logits (moe_route's logits_out, the same kernels
+     as inside the layer): the oracle's selection must equal the GPU's bit
+     for bit and EVERY compared token's output must be within the layer
+     tolerance, no token left out;
+  2. on the oracle's own float64 logits: a token whose k-th and (k+1)-th
+     logits nearly tie may legitimately select a different unit; such tokens
+     must be genuine near ties (checked), are counted, and are left out of
+     this mode's element comparison only.
+Small workloads compare every token; the two large prefill workloads compare
+whole 512-token requests plus a seeded sample and the first and last token
+(the oracle runs on those tokens: tokens are independent), plus properties
+that hold at any size (routing and permutation bit-exact from
+generator-given logits).
 """
 from dataclasses import replace
 
@@ -50,18 +57,23 @@ def _compare(wl, d, desc, out, Lg, idx, tokens):
     k_s = d["k_per_token"].cpu().numpy()[tokens]
     bias = None if d["expert_bias"] is None else d["expert_bias"].cpu().numpy()
     spec = spec_of(desc, T=len(tokens))
-    ref = O.layer_forward(spec, x_s, bf16_bits(d["router_w"]), unit_fetch(d["w_gate_up"]),
-                          unit_fetch(d["w_down"]), k_s, expert_bias=bias,
-                          w_shared_gate_up=(bf16_bits(d["w_shared_gate_up"])
-                                            if wl.I_shared else None),
-                          w_shared_down=(bf16_bits(d["w_shared_down"]) if wl.I_shared else None))
-    L64 = ref["logits"]
-    Lg_s = Lg.cpu().numpy()[tokens].astype(np.float64)
-    delta = 2.0 * np.abs(Lg_s - L64).max(axis=1) + 1e-7
-    ok, n_tied = tie_safe_tokens(L64, idx.cpu().numpy()[tokens], k_s, delta)
-    assert n_tied <= max(2, len(tokens) // 100), f"{n_tied} near-tie tokens"
+    Lg_s = Lg.cpu().numpy()[tokens]
+    idx_s = idx.cpu().numpy()[tokens]
+    ref64, ref32 = O.layer_forward_routings(
+        spec, x_s, bf16_bits(d["router_w"]), unit_fetch(d["w_gate_up"]), unit_fetch(d["w_down"]),
+        k_s, expert_bias=bias, logits_list=(None, Lg_s),
+        w_shared_gate_up=(bf16_bits(d["w_shared_gate_up"]) if wl.I_shared else None),
+        w_shared_down=(bf16_bits(d["w_shared_down"]) if wl.I_shared else None))
     got = out.to(torch.float64).cpu().numpy()[tokens]
-    fro = assert_close_layer(got[ok], ref["out"][ok], wl.name)
+    # 1. the GPU's fp32 logits: same selection, every token within tolerance
+    np.testing.assert_array_equal(ref32["topk_idx"], idx_s)
+    fro = assert_close_layer(got, ref32["out"], f"{wl.name} (GPU logits)")
+    # 2. float64 logits: near ties counted and left out of this mode only
+    L64 = ref64["logits"]
+    delta = 2.0 * np.abs(Lg_s.astype(np.float64) - L64).max(axis=1) + 1e-7
+    ok, n_tied = tie_safe_tokens(L64, idx_s, k_s, delta)
+    assert n_tied <= max(2, len(tokens) // 100), f"{n_tied} near-tie tokens"
+    assert_close_layer(got[ok], ref64["out"][ok], f"{wl.name} (fp64 logits)")
     return fro, n_tied
 
 
@@ -86,13 +98,17 @@ def test_layer_qwen_decode_sweep(T):
     _compare(wl, d, desc, out, Lg, idx, np.sort(tokens))
 
 
-@pytest.mark.parametrize("name,n_sample", [("qwen_prefill", 96), ("deepseek_prefill", 24)])
-def test_layer_prefill_sampled(name, n_sample):
+@pytest.mark.parametrize("name,request_idx,n_sample", [("qwen_prefill", 5, 64),
+                                                      ("deepseek_prefill", 0, 32)])
+def test_layer_prefill_sampled(name, request_idx, n_sample):
+    """One whole 512-token request, a seeded sample of the other tokens, and
+    the first and last token of the batch (the ragged tail)."""
     wl, d, desc, out, Lg, idx = _run_layer(WL.ALL[name])
     rng = np.random.default_rng(12345)
-    tokens = np.sort(rng.choice(wl.T, n_sample, replace=False))
-    # always include the first and the last token (ragged tail of the batch)
-    tokens = np.unique(np.concatenate([[0, wl.T - 1], tokens]))
+    req = np.arange(request_idx * wl.tokens_per_request, (request_idx + 1) * wl.tokens_per_request)
+    tokens = np.unique(np.concatenate([[0, wl.T - 1], req,
+                                       rng.choice(wl.T, n_sample, replace=False)]))
+    assert len(tokens) >= wl.tokens_per_request + 1
     _compare(wl, d, desc, out, Lg, idx, tokens)
 
 

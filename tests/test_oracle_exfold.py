@@ -160,28 +160,77 @@ def test_pool_and_targets_satisfy_their_definitions():
             assert set(tg) <= inside and len(tg) == len(set(tg))
 
 
-def test_pool_scores_follow_the_blocked_fp32_order():
-    """The score is an fp32 sum over 64-token blocks added in block order: a
-    second formulation (per-block cumulative sums) gives the same bits, and the
-    float64 sum agrees to rounding."""
+def test_pool_scores_are_the_exact_aggregate_weight():
+    """The score is the real-number sum of each unit's fp32 routed weights
+    (times h): math.fsum (correctly rounded) agrees to float64 rounding, and
+    a separate per-route loop with h applied route by route gives the same."""
+    import math
     idx, w, k = _random_routing(200, 16, 6, 5)
-    got = F.pool_scores(idx, w, k, 16)
-    want = np.zeros(16, dtype=np.float32)
-    for b0 in range(0, 200, 64):
-        seq = [[] for _ in range(16)]
-        for t in range(b0, min(200, b0 + 64)):
-            for j in range(k[t]):
-                seq[idx[t, j]].append(w[t, j])
-        for u in range(16):
-            part = np.cumsum(np.array(seq[u], dtype=np.float32), dtype=np.float32)[-1] \
-                if seq[u] else np.float32(0)
-            want[u] = np.float32(want[u] + part)
-    np.testing.assert_array_equal(got, want)
-    exact = np.zeros(16)
+    h = np.random.default_rng(6).random(16).astype(np.float32) + 0.5
+    got = F.pool_scores(idx, w, k, 16, unit_scale=h)
+    terms = [[] for _ in range(16)]
     for t in range(200):
         for j in range(k[t]):
-            exact[idx[t, j]] += float(w[t, j])
-    np.testing.assert_allclose(got, exact, rtol=1e-5)
+            terms[idx[t, j]].append(float(w[t, j]) * float(h[idx[t, j]]))
+    want = np.array([math.fsum(v) for v in terms])
+    np.testing.assert_allclose(got, want, rtol=1e-14, atol=0)
+
+
+def test_fp32_evaluations_stay_within_the_stated_bound():
+    """Any fp32 order of the score's additions (forward, reversed, in
+    64-token blocks) then the fp32 product with h lands within
+    score_error_bound of the exact score."""
+    idx, w, k = _random_routing(300, 24, 8, 8)
+    h = np.random.default_rng(9).random(24).astype(np.float32) + 0.5
+    exact = F.pool_scores(idx, w, k, 24, unit_scale=h)
+    bound = F.score_error_bound(idx, w, k, 24, unit_scale=h)
+    seqs = [[] for _ in range(24)]
+    for t in range(300):
+        for j in range(k[t]):
+            seqs[idx[t, j]].append(np.float32(w[t, j]))
+    for order in ("forward", "reverse", "blocks"):
+        for u in range(24):
+            v = seqs[u] if order != "reverse" else seqs[u][::-1]
+            if order == "blocks":
+                acc = np.float32(0)
+                for b0 in range(0, len(v), 7):
+                    part = np.float32(0)
+                    for x in v[b0:b0 + 7]:
+                        part = np.float32(part + x)
+                    acc = np.float32(acc + part)
+            else:
+                acc = np.float32(0)
+                for x in v:
+                    acc = np.float32(acc + x)
+            ev = float(np.float32(acc * h[u]))
+            assert abs(ev - exact[u]) <= bound[u], (order, u)
+
+
+def test_worked_example_tells_the_exact_score_from_an_fp32_sum():
+    """Mutation check on the fixture: with the score added in fp32 (any
+    order; the fixture's unit has two terms) the pool would be {0, 1}, not
+    the exact sum's {1, 5}; the fixture therefore fails an oracle that
+    evaluates the score in fp32."""
+    E_r, D, idx, w, k, L, S, pool, expect = _load_golden()
+    fp32 = np.zeros(E_r, dtype=np.float32)
+    for t in range(idx.shape[0]):
+        for j in range(k[t]):
+            fp32[idx[t, j]] = np.float32(fp32[idx[t, j]] + w[t, j])
+    assert F.select_pool(fp32, D).tolist() == [0, 1]
+    assert F.select_pool(F.pool_scores(idx, w, k, E_r), D).tolist() == pool == [1, 5]
+
+
+def test_exact_score_tie_goes_to_the_lower_index():
+    """0.25 + 0.5 and 0.75 are exact in any precision: a true tie, the lower
+    unit index enters the pool."""
+    idx = np.array([[3, 1], [3, -1]])
+    w = np.array([[0.75, 0.25], [0.0, 0.0]], dtype=np.float32)
+    idx2 = np.array([[4, 1], [1, -1]])
+    w2 = np.array([[0.75, 0.25], [0.5, 0.0]], dtype=np.float32)
+    # unit 1: 0.25 + 0.5 = 0.75, unit 4: 0.75
+    assert F.select_pool(F.pool_scores(idx2, w2, [2, 1], 6), 1).tolist() == [1]
+    sc = F.pool_scores(idx, w, [2, 1], 6)
+    assert sc[3] == 0.75 and sc[1] == 0.25
 
 
 def test_static_pool_and_unit_scale():

@@ -105,3 +105,60 @@ def test_path_recipe_shares_every_second_source():
     assert s.tolist() == [[3, 3, 7, 7], [2, 2, -1, -1]]
     assert t.tolist() == idx.tolist()
     assert torch.equal(b[0], w[0]) and b[1, 2:].abs().sum() == 0
+
+
+def test_shared_expert_term_closed_form():
+    """The shared expert adds with weight 1 on top of the paths.  One-hot
+    shared weights (neuron n reads gate input a_n and up input b_n, writes
+    output c_n) make its term the closed form sum_n silu(x_{a_n}) x_{b_n} at
+    c_n; with diagonal paths the rest is the vanilla layer (the layer
+    oracle's FFN).  Dropping the shared term, or scaling it, fails this."""
+    x, wgu, wd = _layer(11, T=5, H=10, E=4, I=3)
+    idx, w, k = _routing(5, 4, 3, 12)
+    a, b, c = [1, 4, 7], [2, 5, 9], [0, 3, 3]          # two neurons write output 3
+    sgu = np.zeros((2 * 3, 10))
+    sd = np.zeros((10, 3))
+    for n in range(3):
+        sgu[n, a[n]] = 1.0
+        sgu[3 + n, b[n]] = 1.0
+        sd[c[n], n] = 1.0
+    out, _ = P.paths_forward(x, lambda u: wgu[u], lambda u: wd[u], idx, idx, w, k,
+                             w_shared_gate_up=sgu, w_shared_down=sd)
+    vanilla = np.zeros_like(x)
+    for t in range(5):
+        for j in range(k[t]):
+            vanilla[t] += w[t, j] * O.swiglu_ffn(x[t:t + 1], wgu[idx[t, j]], wd[idx[t, j]])[0]
+    shared = np.zeros_like(x)
+    for t in range(5):
+        for n in range(3):
+            g = x[t, a[n]]
+            shared[t, c[n]] += g / (1.0 + np.exp(-g)) * x[t, b[n]]
+    np.testing.assert_allclose(out, vanilla + shared, rtol=1e-12, atol=1e-12)
+    assert np.abs(shared).max() > 0.1                  # the term is not negligible here
+    assert not np.allclose(out, vanilla + 0.5 * shared, rtol=1e-6, atol=1e-6)
+
+
+def test_paths_sharing_a_target_sum_before_the_projection():
+    """Two paths of one token with the same target j: the projection is
+    linear, so sum_i beta_i D_j(U_i(h)) = D_j(sum_i beta_i U_i(h)); with
+    one-hot weights both equal the closed form at the target's output."""
+    H, E = 8, 3
+    a, b, c = [0, 2, 4], [1, 3, 5], [6, 7, 0]
+    wgu = np.zeros((E, 2, H))
+    wd = np.zeros((E, H, 1))
+    for u in range(E):
+        wgu[u, 0, a[u]] = 1.0
+        wgu[u, 1, b[u]] = 1.0
+        wd[u, c[u], 0] = 1.0
+    x = np.arange(1, H + 1, dtype=np.float64)[None, :] / 3
+    src = np.array([[0, 2, 1]])
+    tgt = np.array([[1, 1, 1]])                        # every path projects through unit 1
+    beta = np.array([[0.5, -2.0, 0.25]])
+    out, n_exp = P.paths_forward(x, lambda u: wgu[u], lambda u: wd[u], src, tgt, beta, [3])
+    s = lambda g: g / (1 + np.exp(-g))  # noqa: E731
+    want = np.zeros(H)
+    want[c[1]] = sum(beta[0, j] * s(x[0, a[src[0, j]]]) * x[0, b[src[0, j]]] for j in range(3))
+    np.testing.assert_allclose(out[0], want, rtol=1e-14)
+    merged = sum(beta[0, j] * P.expansion(x, wgu[src[0, j]]) for j in range(3))
+    np.testing.assert_allclose(out, P.projection(merged, wd[1]), rtol=1e-14)
+    assert n_exp == 3

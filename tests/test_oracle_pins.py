@@ -44,10 +44,18 @@ def naive_moe(x, router_w, Wg, Wu, Wd, k, score="softmax", renorm=False, scale=1
     """Plain per-token MoE with whole experts given as lists of (Wg, Wu, Wd)."""
     T = x.shape[0]
     E = router_w.shape[0]
+    logits = [[float(np.dot(x[t], router_w[e])) + (0.0 if bias is None else bias[e])
+               for e in range(E)] for t in range(T)]
+    return naive_moe_from_logits(x, logits, Wg, Wu, Wd, k, score, renorm, scale)
+
+
+def naive_moe_from_logits(x, logits, Wg, Wu, Wd, k, score="softmax", renorm=False, scale=1.0):
+    """naive_moe on given router logits [T][E]."""
+    T = x.shape[0]
     out = np.zeros((T, Wd[0].shape[0]))
     for t in range(T):
-        logit = [float(np.dot(x[t], router_w[e])) + (0.0 if bias is None else bias[e])
-                 for e in range(E)]
+        logit = [float(v) for v in logits[t]]
+        E = len(logit)
         # brute-force top-k: repeatedly take the largest, lower index on ties
         left = list(range(E))
         sel = []
@@ -474,3 +482,32 @@ def test_budget_generators_and_modes():
     assert apply_k_mode(base, "coarse", 4, 8).tolist() == [4, 4, 4, 4, 8, 8, 8]
     assert apply_k_mode(base, "coarse", 2, 7).tolist() == [2, 2, 4, 4, 6, 7, 7]
     assert [O.coarse_k(int(v), 4) for v in base] == [4, 4, 4, 4, 8, 8, 8]
+
+
+def test_several_routings_at_once_match_the_naive_layer():
+    """layer_forward_routings: every routing it returns equals the naive
+    formulation run on that routing's own logits (the float64 logits of the
+    router, or perturbed fp32 logits that select differently for some
+    tokens), shared expert included."""
+    rng = np.random.default_rng(14)
+    T, H, E, I_sub, k_max, I_sh = 7, 16, 6, 8, 3, 4
+    x = rng.normal(size=(T, H))
+    R = rng.normal(size=(E, H)) / math.sqrt(H)
+    Wg = rng.normal(size=(E, I_sub, H)) / math.sqrt(H)
+    Wu = rng.normal(size=(E, I_sub, H)) / math.sqrt(H)
+    Wd = rng.normal(size=(E, H, I_sub)) / math.sqrt(I_sub)
+    sgu = rng.normal(size=(2 * I_sh, H))
+    sd = rng.normal(size=(H, I_sh))
+    wgu, wd = split_experts(Wg, Wu, Wd, 1)
+    k = rng.integers(1, k_max + 1, size=T)
+    L64 = x @ R.T
+    L32 = (L64 + rng.normal(size=L64.shape) * 0.3).astype(np.float32)
+    spec = O.LayerSpec(T=T, H=H, n_experts=E, n_sub=1, I_sub=I_sub, k_max=k_max,
+                       I_shared=I_sh)
+    r64, r32 = O.layer_forward_routings(spec, x, R, wgu, wd, k, logits_list=(None, L32),
+                                        w_shared_gate_up=sgu, w_shared_down=sd)
+    sh = np.stack([neuron_sum_expert(x[t], sgu[:I_sh], sgu[I_sh:], sd) for t in range(T)])
+    for res, L in ((r64, L64), (r32, L32.astype(np.float64))):
+        ref = naive_moe_from_logits(x, L, Wg, Wu, Wd, k)
+        assert rel_err(res["out"], ref + sh) <= 1e-12
+    assert not np.array_equal(r64["topk_idx"], r32["topk_idx"])   # the routings differ

@@ -25,8 +25,14 @@ sum over active paths).  Path selection (a compatibility bias learned by
 fine-tuning) is out of scope: paths arrive as inputs.
 
 Readings: the page's experts are this layer's routing units; a token's
-sources are listed in first-occurrence order of its paths; everything is
-fp64 with no intermediate rounding.
+sources are listed in first-occurrence order of its paths; several paths of
+a token may share a target (and a source); the shared expert, when given,
+adds with weight 1; everything is fp64 with no intermediate rounding.
+
+Pinned (tests/test_oracle_pcomoe.py): diagonal paths = the vanilla layer;
+source grouping = per-path recomputation; one-hot closed forms for the
+source/target roles, for paths sharing a target and for the shared-expert
+term; unique-source bookkeeping by brute force.
 """
 from __future__ import annotations
 

@@ -25,7 +25,7 @@ struct Layout {
   size_t logits, router_partial, topk_idx, topk_w, counts, offsets, sorted_token, inv_row, bitmap,
       wprefix, xperm, act, yperm, act_sh, ysh, split_word, partial, chunk_done, ffn_part,
       fold_ws, fold_idx, fold_w, fold_k, p_srcs, p_nsrc, p_slot, p_counts, p_offsets, p_sorted,
-      p_inv, p_row, p_act, total;
+      p_inv, p_tgts, p_ntgt, p_tslot, p_wtgt, p_act, total;
   int router_slices;   // slices of the CUDA-core router (0: the tensor-core router runs)
   int max_split;       // K splits the decode gate|up kernel may use (1: none)
   int max_split_down;  // K splits the decode down kernel may use
@@ -113,9 +113,10 @@ Layout layout_of(const moe_layer_desc& d) {
   l.fold_idx = take(n_cap * 4);
   l.fold_w = take(n_cap * 4);
   l.fold_k = take(T * 4);
-  // path-composed execution: unique sources, their permutation, the
-  // expansion row of every path, and the path-ordered expansion rows (in the
-  // permuted-x region when it is wide enough: x_perm is free by then)
+  // path-composed execution: distinct sources and their permutation,
+  // distinct targets, the combine weights of the target rows, and the
+  // target-ordered down input rows (in the permuted-x region when it is wide
+  // enough: x_perm is free by then)
   l.p_srcs = take(n_cap * 4);
   l.p_nsrc = take(T * 4);
   l.p_slot = take(n_cap * 4);
@@ -123,7 +124,10 @@ Layout layout_of(const moe_layer_desc& d) {
   l.p_offsets = take((E_r + 1) * 4);
   l.p_sorted = take(n_cap * 4);
   l.p_inv = take(n_cap * 4);
-  l.p_row = take(n_cap * 4);
+  l.p_tgts = take(n_cap * 4);
+  l.p_ntgt = take(T * 4);
+  l.p_tslot = take(n_cap * 4);
+  l.p_wtgt = take(n_cap * 4);
   l.p_act = d.I_sub <= d.H ? l.xperm : take(n_cap * d.I_sub * 2);
   l.total = o;
   return l;
@@ -428,7 +432,12 @@ moe_status do_down(const moe_layer_desc* d, const void* act, const int32_t* offs
   g.out_rows = n_cap;
   g.status = status;
   g.debug_flags = 0;
-  g.force_pair = (d->debug_flags & MOE_DEBUG_FORCE_PAIR) != 0u;
+  // The down projection reads act through TMA (no row gather), so CTA pairs
+  // apply as they are: with K = I_sub >= 1024 their main loops are long
+  // enough to win (DeepSeek-V3 shape, I_sub 2048: 2444 -> 2370 us measured
+  // on GB300); with short K (Qwen3-30B-A3B shape, I_sub 768) single CTAs
+  // stay ahead (140 vs 147 us).
+  g.force_pair = (d->debug_flags & MOE_DEBUG_FORCE_PAIR) != 0u || d->I_sub >= 1024;
   g.sm_count = sm_count();
   g.max_rows_hint = static_cast<int>(n_cap);
   return cuda_status(moe::launch_gemm(g, s));
@@ -579,11 +588,14 @@ moe_status do_layer_paths(const moe_layer_desc* d, const void* x, const void* w_
   int32_t* offs_s = at<int32_t>(ws, l.p_offsets);
   int32_t* sorted_s = at<int32_t>(ws, l.p_sorted);
   int32_t* inv_s = at<int32_t>(ws, l.p_inv);
+  int32_t* tgts = at<int32_t>(ws, l.p_tgts);
+  int32_t* ntgt = at<int32_t>(ws, l.p_ntgt);
+  int32_t* tslot = at<int32_t>(ws, l.p_tslot);
+  float* wtgt = at<float>(ws, l.p_wtgt);
   int32_t* counts = at<int32_t>(ws, l.counts);
   int32_t* offsets = at<int32_t>(ws, l.offsets);
   int32_t* sorted_token = at<int32_t>(ws, l.sorted_token);
   int32_t* inv_row = at<int32_t>(ws, l.inv_row);
-  int32_t* row_of = at<int32_t>(ws, l.p_row);
   void* act_s = at<void>(ws, l.act);
   void* act_p = at<void>(ws, l.p_act);
   void* yperm = at<void>(ws, l.yperm);
@@ -593,18 +605,18 @@ moe_status do_layer_paths(const moe_layer_desc* d, const void* x, const void* w_
   MOE_TRY(do_permute(d, srcs, nsrc, at<int32_t>(ws, l.p_counts), offs_s, sorted_s, inv_s, status,
                      ws, s));
   MOE_TRY(do_gate_up(d, x, sorted_s, offs_s, w_gate_up, act_s, status, ws, s));
-  // projections: one per path, grouped by target, reading its source's row
-  MOE_TRY(do_permute(d, tgt_idx, n_paths, counts, offsets, sorted_token, inv_row, status, ws, s));
-  MOE_TRY(cuda_status(moe::launch_paths_rows(n_paths, slot, inv_s, inv_row, d->T, d->k_max,
-                                             row_of, s)));
-  MOE_TRY(cuda_status(moe::launch_gather_rows(act_s, row_of, offsets, E_r,
-                                              static_cast<int>(n_cap), d->I_sub,
-                                              static_cast<int>(n_cap), act_p, status, sm_count(),
-                                              s)));
+  // projections: one per (token, distinct target); its input row is the
+  // beta-weighted sum of the expansions of the paths into that target
+  MOE_TRY(cuda_status(moe::launch_paths_sources(tgt_idx, n_paths, d->T, d->k_max, E_r, tgts,
+                                                ntgt, tslot, status, s)));
+  MOE_TRY(do_permute(d, tgts, ntgt, counts, offsets, sorted_token, inv_row, status, ws, s));
+  MOE_TRY(cuda_status(moe::launch_paths_merge(n_paths, slot, tslot, ntgt, beta, inv_s, inv_row,
+                                              act_s, d->T, d->k_max, d->I_sub, n_cap, n_cap,
+                                              act_p, wtgt, status, s)));
   MOE_TRY(do_down(d, act_p, offsets, w_down, yperm, status, ws, s));
   void* ysh = d->I_shared > 0 ? at<void>(ws, l.ysh) : nullptr;
   if (ysh != nullptr) MOE_TRY(do_shared(d, x, ysh, status, ws, s));
-  return do_combine(d, yperm, ysh, inv_row, beta, n_paths, out, status, s);
+  return do_combine(d, yperm, ysh, inv_row, wtgt, ntgt, out, status, s);
 }
 
 // ---------------------------------------------------------------- proxy router

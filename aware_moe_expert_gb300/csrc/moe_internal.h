@@ -84,15 +84,20 @@ cudaError_t launch_fold_decode(const int32_t* topk_idx, const float* topk_w,
                                int32_t* pool_out, void* ws, int32_t* status, cudaStream_t s);
 
 // ---- paths.cu: path-composed execution
-// Distinct sources per token (first-occurrence order), their count, and each
-// path's source position (all [T, k_max] / [T]).
+// Distinct values of a per-path unit list (sources or targets) per token in
+// first-occurrence order, their count, and each path's position among them
+// (all [T, k_max] / [T]).
 cudaError_t launch_paths_sources(const int32_t* src_idx, const int32_t* n_paths, int T, int k_max,
                                  int E_r, int32_t* srcs, int32_t* n_src, int32_t* slot,
                                  int32_t* status, cudaStream_t s);
-// row_of[target-sorted position of path (t, j)] = source-sorted row of its expansion
-cudaError_t launch_paths_rows(const int32_t* n_paths, const int32_t* slot, const int32_t* inv_src,
-                              const int32_t* inv_tgt, int T, int k_max, int32_t* row_of,
-                              cudaStream_t s);
+// Down input of every (token, distinct target) row: act_tgt[inv_tgt[t, ts]] =
+// bf16(sum over the token's paths j with tslot[t, j] == ts, in path order, of
+// beta[t, j] * act_src[inv_src[t, slot[t, j]]]) in fp32; w_tgt[t, ts] = 1.
+cudaError_t launch_paths_merge(const int32_t* n_paths, const int32_t* slot, const int32_t* tslot,
+                               const int32_t* n_tgt, const float* beta, const int32_t* inv_src,
+                               const int32_t* inv_tgt, const void* act_src, int T, int k_max,
+                               int I_sub, long long n_src_rows, long long n_tgt_rows,
+                               void* act_tgt, float* w_tgt, int32_t* status, cudaStream_t s);
 
 // ---- permute.cu
 // bitmap_ready: the top-k kernel already wrote `bitmap` (T > 256 only).

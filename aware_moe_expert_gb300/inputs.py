@@ -186,18 +186,37 @@ def make_fold_tables(E_r: int, device="cpu", seed: int = 11):
     return S.float().contiguous().to(device), L.float().contiguous().to(device)
 
 
-def make_paths(topk_idx: torch.Tensor, topk_w: torch.Tensor):
+def make_paths(topk_idx: torch.Tensor, topk_w: torch.Tensor, mode: str = "share_source"):
     """Synthetic composed paths from a routing (a path router is trained, out
-    of scope): a token's selected units in slot order are the targets; even
-    slots are their own source, odd slots take the previous slot's unit as
-    source, so consecutive paths share an expansion; the path weight is the
-    unit's gate weight.  Returns (src_idx, tgt_idx, beta), -1 / 0 after k_t
-    (slots past k_t are -1 in topk_idx)."""
-    tgt = topk_idx.clone()
-    src = topk_idx.clone()
-    src[:, 1::2] = topk_idx[:, 0:-1:2] if topk_idx.shape[1] % 2 == 0 else topk_idx[:, 0:-2:2]
-    src = torch.where(tgt >= 0, src, torch.full_like(src, -1))
-    beta = torch.where(tgt >= 0, topk_w, torch.zeros_like(topk_w))
+    of scope).  A token's selected units in slot order, u_0, u_1, ...; the
+    path weight is the slot's gate weight.  Recipes:
+      share_source   slot j targets u_j; even slots are their own source, odd
+                     slots take u_{j-1} as source (consecutive paths share
+                     an expansion)
+      share_target   even slots are diagonal (u_j, u_j); odd slots keep u_j
+                     as source and take u_{j-1} as target (consecutive paths
+                     share a projection)
+      duplicate      like share_target, and every slot j = 3 mod 4 repeats
+                     the path of slot j - 1 (the same (source, target) twice)
+    Returns (src_idx, tgt_idx, beta), -1 / 0 after k_t (slots past k_t are -1
+    in topk_idx)."""
+    k_max = topk_idx.shape[1]
+    prev = topk_idx.clone()
+    n_odd = k_max // 2
+    prev[:, 1:2 * n_odd:2] = topk_idx[:, 0:2 * n_odd - 1:2]
+    if mode == "share_source":
+        src, tgt = prev, topk_idx.clone()
+    elif mode in ("share_target", "duplicate"):
+        src, tgt = topk_idx.clone(), prev
+        if mode == "duplicate":
+            src[:, 3::4] = src[:, 2:k_max - 1:4][:, :src[:, 3::4].shape[1]]
+            tgt[:, 3::4] = tgt[:, 2:k_max - 1:4][:, :tgt[:, 3::4].shape[1]]
+    else:
+        raise ValueError(mode)
+    live = topk_idx >= 0
+    src = torch.where(live, src, torch.full_like(src, -1))
+    tgt = torch.where(live, tgt, torch.full_like(tgt, -1))
+    beta = torch.where(live, topk_w, torch.zeros_like(topk_w))
     return src.contiguous(), tgt.contiguous(), beta.contiguous()
 
 

@@ -43,7 +43,14 @@ class Workload:
         return self.n_sub * self.I_sub
 
     def with_T(self, T: int) -> "Workload":
-        return replace(self, T=T, name=f"{self.name.split('@')[0]}@T{T}")
+        base, _, tags = self.name.partition("@")
+        tags = [t for t in tags.split("@") if t and not t.startswith("T")]
+        return replace(self, T=T, name="@".join([base, *tags, f"T{T}"]))
+
+    def with_experts(self, n: int) -> "Workload":
+        base, _, tags = self.name.partition("@")
+        tags = [t for t in tags.split("@") if t and not t.startswith("E")]
+        return replace(self, n_experts=n, name="@".join([base, f"E{n}", *tags]))
 
 
 # Tiny k-aware layer: 16 experts x 4 sub-experts of 128, k ~ U{1..8} per token.

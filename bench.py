@@ -62,6 +62,9 @@ def parse():
                    help="N > 0: no timing; build the workload's inputs (one weight copy), make N "
                         "moe_layer_forward calls and check the device status (for ncu captures)")
     p.add_argument("--T", type=int, default=None, help="override the token count")
+    p.add_argument("--n-experts", type=int, default=None,
+                   help="override the expert count (a smaller case of the same layer shape, "
+                        "for profiler captures)")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -1020,12 +1023,15 @@ def main():
     args = parse()
     from aware_moe_expert_gb300 import workloads as WL
     sweep = args.workload is None and not args.no_sweep and args.T is None and \
+        args.n_experts is None and \
         args.impl == "ours" and not (args.tiered or args.paths or args.profile_calls) and \
         args.router == "linear" and args.fold == 0 and args.k_mode == "exact" and \
         args.k_normal is None and args.path == 0 and not args.force_pair
     wl = WL.ALL[args.workload or "mixtral_decode"]
     if args.T is not None:
         wl = wl.with_T(args.T)
+    if args.n_experts is not None:
+        wl = wl.with_experts(args.n_experts)
     rank, world, local = dist_info()
     if args.impl == "reference":
         res = run_reference(args, wl, rank, world)

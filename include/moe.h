@@ -237,15 +237,19 @@ moe_status moe_layer_forward_fold(const moe_layer_desc* desc, const moe_fold_des
  * and a projection D_u(z) = z Wd_u; a path (i, j) is D_j(U_i(h)), and
  *     out_t = sum_{j < n_paths[t]} beta[t,j] * D_{tgt[t,j]}(U_{src[t,j]}(x_t))
  *             (+ the shared expert, weight 1, when desc->I_shared > 0),
- * with U_i evaluated once per distinct source of a token (paths listed in
- * slot order; diagonal paths i == j are the plain layer).
+ * with U_i evaluated once per distinct source of a token and D_j once per
+ * distinct target: D is linear, so the paths of a token into one target j
+ * are projected together, D_j(sum_i beta_ij U_i(x_t)) (the weighted sum of
+ * their bf16 expansion rows formed in fp32, in slot order, rounded to bf16).
+ * Paths are listed in slot order; diagonal paths i == j are the plain layer.
  *   src_idx, tgt_idx  int32 [T, k_max]: units of each path's expansion and
- *                     projection; a token's targets must be distinct
- *                     (MOE_ERR_BAD_INDEX otherwise), its sources may repeat
+ *                     projection; a token's sources and targets may repeat
+ *                     (a repeated (i, j) pair adds its weights)
  *   beta              fp32 [T, k_max]: path weights
  *   n_paths           int32 [T], each in [1, k_max]
  *   out               bf16 [T, H]
- * Path selection (a learned compatibility bias) is the caller's.  Workspace:
+ * Unit indices outside [0, E_r) give MOE_ERR_BAD_INDEX.  Path selection (a
+ * learned compatibility bias) is the caller's.  Workspace:
  * moe_workspace_size(desc) bytes.  Requires I_sub % 8 == 0. */
 moe_status moe_layer_forward_paths(const moe_layer_desc* desc, const void* x,
                                    const void* w_gate_up, const void* w_down,

@@ -88,6 +88,17 @@ def test_layer_shared_expert_at_decode_sizes(T):
     _compare(wl, d, desc, out, Lg, idx, np.arange(T))
 
 
+@pytest.mark.parametrize("T,path", [(128, B.PATH_AUTO), (300, B.PATH_AUTO), (257, B.PATH_PREFILL),
+                                    (700, B.PATH_AUTO)])
+def test_layer_shared_expert_at_prefill_sizes(T, path):
+    """The shared expert's dense GEMMs on single-CTA tiles (up to 600 rows)
+    and on CTA pairs (700 rows), with ragged last tiles, next to the routed
+    GEMMs at H = 7168 (routed down on CTA pairs: I_sub = 2048): every token
+    against the oracle."""
+    wl, d, desc, out, Lg, idx = _run_layer(DEEPSEEK_SMALL, T=T, path=path)
+    _compare(wl, d, desc, out, Lg, idx, np.arange(T))
+
+
 # Every token selects every unit (k = E_r = 32): the dense gate-weighted
 # mixture of all sub-experts (MoE-Prism §II, Eq. (2) with k = all), every
 # unit serving all T tokens.

@@ -41,7 +41,13 @@ def _gpu_permute(desc, idx, k):
 @pytest.mark.parametrize("T,E_r,k_max,skew", [(1, 8, 4, 0.0), (31, 64, 8, 0.0), (32, 64, 8, 0.0),
                                               (33, 64, 8, 0.0), (1000, 128, 8, 1.1),
                                               (1024, 256, 16, 0.0), (4097, 32, 8, 2.0),
-                                              (16384, 256, 8, 0.5), (70, 3, 3, 0.0)])
+                                              (16384, 256, 8, 0.5), (70, 3, 3, 0.0),
+                                              # scatter CTAs of 256 slots spanning one
+                                              # bitmap word (k_max 8), half a word (16),
+                                              # several words (k_max 1, 2, 3)
+                                              (8192, 128, 8, 1.1), (2048, 256, 1, 0.0),
+                                              (3072, 64, 2, 0.7), (4096, 256, 8, 0.0),
+                                              (2048, 48, 3, 0.0), (1024, 33, 5, 0.0)])
 def test_permute_bit_exact(T, E_r, k_max, skew):
     idx, k = _random_routing(T, E_r, k_max, seed=T + E_r, skew=skew)
     desc = B.LayerDesc(T=T, H=64, n_experts=E_r, n_sub=1, I_sub=64, k_max=k_max)

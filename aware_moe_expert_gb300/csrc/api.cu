@@ -196,7 +196,6 @@ inline moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK 
     if (_st != MOE_OK) return _st;         \
   } while (0)
 
-
 // Tokens per weight-stationary item: 64 when units hold few rows (decode),
 // else larger chunks so each weight tile is reused across more tokens.
 int decode_chunk(const moe_layer_desc* d) {
@@ -296,7 +295,7 @@ moe_status do_route(const moe_layer_desc* d, const void* x, const void* router_w
                                            status, s, bm));
 }
 
-// Counters of the fused decode FFN kernel (one per 64-row chunk, the work
+// Counters of the fused decode FFN kernel (one per token chunk, the work
 // counter, the split counters), zeroed by the launch that precedes the FFN.
 // Tokens per fused-decode-FFN item: 16 when no unit can hold more than 16
 // rows (T <= 16), else 64.
@@ -447,12 +446,13 @@ moe_status do_down(const moe_layer_desc* d, const void* act, const int32_t* offs
 // 128 run the fused kernel (gate|up and down overlapped in one launch);
 // otherwise gate|up then down.
 
-// pre_gathered: x_perm already holds the permuted rows and the decode FFN's
-// counters are zero (the fused small-batch router wrote them).
+// gather_in_ffn: the decode FFN reads its token rows from x itself and its
+// counters are already zero (the router or the permutation zeroed them);
+// otherwise a row-gather launch writes x_perm and zeroes them.
 moe_status do_grouped_ffn(const moe_layer_desc* d, const void* x, const int32_t* sorted_token,
                           const int32_t* offsets, const void* w_gate_up, const void* w_down,
                           void* y_perm, int32_t* status, void* ws, cudaStream_t s,
-                          bool pre_gathered = false, bool gather_in_ffn = false) {
+                          bool gather_in_ffn = false) {
   const Layout l = layout_of(*d);
   void* act = at<void>(ws, l.act);
   const long long n_cap = static_cast<long long>(d->T) * d->k_max;
@@ -462,8 +462,8 @@ moe_status do_grouped_ffn(const moe_layer_desc* d, const void* x, const int32_t*
     void* xperm = at<void>(ws, l.xperm);
     int32_t* done = at<int32_t>(ws, l.chunk_done);
     // the counters are zeroed by the launch that precedes the FFN: the row
-    // gather, the fused router (pre_gathered) or the permutation (gather_in_ffn)
-    if (!pre_gathered && !gather_in_ffn)
+    // gather, or the fused router or the permutation (gather_in_ffn)
+    if (!gather_in_ffn)
       MOE_TRY(cuda_status(moe::launch_gather_rows(x, sorted_token, offsets, E_r, d->T, d->H,
                                                   static_cast<int>(n_cap), xperm, status,
                                                   sm_count(), s, done, decode_ffn_counters(d))));
@@ -864,16 +864,15 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, const vo
   void* yperm = at<void>(workspace, l.yperm);
   void* ysh = desc->I_shared > 0 ? at<void>(workspace, l.ysh) : nullptr;
   const int E_r = E_r_of(desc);
-  bool gathered = false, gather_in_ffn = false;
+  // the fused decode FFN gathers its token rows from x itself; the launch
+  // before it (router or permutation) zeroes its counters
+  const bool gather_in_ffn = use_decode_ffn(desc);
   if (desc->T <= moe::kRouteFuseMaxT && !router_on_tensor_cores(*desc) &&
       moe::route_cluster_supports(desc->H, E_r)) {
-    // small batch: logits, top-k, permutation (and the row gather of the
-    // fused decode FFN) in one launch
-    gathered = use_decode_ffn(desc);
+    // small batch: logits, top-k and permutation in one launch
     moe::RoutePermuteOut f{counts, offsets, sorted_token, inv_row,
-                           gathered ? at<void>(workspace, l.xperm) : nullptr,
-                           gathered ? at<int32_t>(workspace, l.chunk_done) : nullptr,
-                           gathered ? decode_ffn_counters(desc) : 0};
+                           gather_in_ffn ? at<int32_t>(workspace, l.chunk_done) : nullptr,
+                           gather_in_ffn ? decode_ffn_counters(desc) : 0};
     MOE_TRY(cuda_status(moe::launch_route_cluster(
         x, router_w, desc->expert_bias, desc->n_sub, k_per_token, desc->T, desc->H, E_r,
         desc->k_max, desc->score, desc->renorm, desc->route_scale, nullptr, topk_idx, topk_w,
@@ -882,15 +881,12 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, const vo
     bool bitmap_done = false;
     MOE_TRY(do_route(desc, x, router_w, nullptr, k_per_token, nullptr, topk_idx, topk_w,
                      dev_status, workspace, s, &bitmap_done));
-    // the fused decode FFN gathers its token rows itself; the permutation
-    // zeroes its counters (the shared expert, if any, touches neither)
-    gather_in_ffn = use_decode_ffn(desc);
     MOE_TRY(do_permute(desc, topk_idx, k_per_token, counts, offsets, sorted_token, inv_row,
                        dev_status, workspace, s, bitmap_done, gather_in_ffn));
   }
   if (ysh != nullptr) MOE_TRY(do_shared(desc, x, ysh, dev_status, workspace, s));
   MOE_TRY(do_grouped_ffn(desc, x, sorted_token, offsets, w_gate_up, w_down, yperm, dev_status,
-                         workspace, s, gathered, gather_in_ffn));
+                         workspace, s, gather_in_ffn));
   return do_combine(desc, yperm, ysh, inv_row, topk_w, k_per_token, out, dev_status, s);
 }
 

@@ -37,15 +37,15 @@ cudaError_t launch_topk_gate(const float* partial, int S, const float* bias, int
 
 // Logits and top-k_t of clusters of eight tokens in one launch (mma.sync
 // tiles, H % 16 == 0, E_r <= 256).  With `fuse` (T <= 8 only) the same launch also
-// writes the permutation (counts, offsets, sorted_token, inv_row), copies the
-// permuted x rows into x_perm (when non-null) and zeroes zero_ptr[0, zero_n).
+// writes the permutation (counts, offsets, sorted_token, inv_row) and zeroes
+// zero_ptr[0, zero_n).  Router rows and the expert bias are read before the
+// launch's dependency wait (they are layer parameters); x and k after it.
 struct RoutePermuteOut {
   int32_t* counts;
   int32_t* offsets;
   int32_t* sorted_token;
   int32_t* inv_row;
-  void* x_perm;
-  int32_t* zero_ptr;
+  int32_t* zero_ptr;   // counters of the kernel that follows, zeroed here (nullable)
   int zero_n;
 };
 bool route_cluster_supports(int H, int E_r);

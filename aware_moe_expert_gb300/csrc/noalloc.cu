@@ -2,12 +2,11 @@
 // file-scope device array instead of a caller-provided workspace.
 //
 // Who needs it: a caller that may not allocate device memory at the point
-// where it routes tokens.  Typical cases are code that runs while a stream is
-// being captured into a CUDA graph (an allocation there is an error), a
-// serving loop that promised never to enter the allocator on its hot path
-// (an allocation can synchronise the device or fail when memory is
-// fragmented), and a plug-in that is handed device pointers for its inputs
-// and outputs but has no way to own an extra buffer.  Such a caller still
+// where it routes tokens.  Typical cases are a serving loop that promised
+// never to enter the allocator on its hot path (an allocation can
+// synchronise the device or fail when memory is fragmented), and a plug-in
+// that is handed device pointers for its inputs and outputs but has no way
+// to own an extra buffer.  Such a caller still
 // passes every input and output; only the scratch comes from here.
 //
 // The scratch is one array per device that loads this library, kept until

@@ -327,9 +327,9 @@ __global__ void __launch_bounds__(256) topk_gate_kernel(
 // 8 tokens, bf16 in, fp32 out).  The warps' partial tiles are added in warp
 // order, and each CTA pushes its logits into CTA 0's shared memory.  After a
 // cluster barrier CTA 0 runs the warp top-k per token.  With a single cluster
-// holding every token (T <= 8) the same launch also builds the permutation in
-// shared memory and, after a second cluster barrier, every CTA copies its
-// share of the permuted x rows.
+// holding every token (T <= 8) CTA 0 also builds the permutation in shared
+// memory, writes it out and zeroes the next kernel's counters, while the
+// other CTAs have already exited.
 constexpr int kClTok = 8;
 constexpr int kClThreads = 512;
 constexpr int kClWarps = kClThreads / 32;
@@ -352,18 +352,18 @@ struct ClusterRouteParams {
   int MT;                // 16-unit m-tiles per CTA: ceil(ceil(E_r / C) / 16)
   int kc;                // hidden columns per staged chunk (multiple of 16)
   int ns;                // chunk buffers (1: all of H at once, or 2)
-  // fused permutation (nullptr: route only) and row gather (x_perm nullptr: none)
+  // fused permutation (nullptr: route only); zero_ptr: counters of the next
+  // kernel that this launch zeroes
   int32_t* counts;
   int32_t* offsets;
   int32_t* sorted_token;
   int32_t* inv_row;
-  uint4* x_perm;
   int32_t* zero_ptr;
   int zero_n;
 };
 
 struct ClusterSmem {
-  uint32_t pitch, rows, stage, red, all, bits, off, sorted, wt, total;
+  uint32_t pitch, rows, stage, red, all, bits, off, wt, bias, total;
 };
 
 // Staged rows per buffer: MT * 16 unit rows, then the eight token rows, each
@@ -386,10 +386,10 @@ __host__ __device__ inline ClusterSmem cluster_smem(int E_r, int MT, int kc, int
   b += 256 * 4;
   o.off = b;
   b += 260 * 4;
-  o.sorted = b;
-  b += 256 * 4;
   o.wt = b;
   b += kClWarps * 4;
+  o.bias = b;
+  b += 256 * 4;
   o.total = b;
   return o;
 }
@@ -442,8 +442,8 @@ __global__ void __launch_bounds__(kClThreads, 1) route_cluster_kernel(const Clus
   float* s_all = reinterpret_cast<float*>(csm + L.all);
   uint32_t* s_bits = reinterpret_cast<uint32_t*>(csm + L.bits);
   int32_t* s_off = reinterpret_cast<int32_t*>(csm + L.off);
-  int32_t* s_sorted = reinterpret_cast<int32_t*>(csm + L.sorted);
   int32_t* s_wt = reinterpret_cast<int32_t*>(csm + L.wt);
+  float* s_bias = reinterpret_cast<float*>(csm + L.bias);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_ctarank();
   const bool fused = p.counts != nullptr;
@@ -473,29 +473,47 @@ __global__ void __launch_bounds__(kClThreads, 1) route_cluster_kernel(const Clus
           make_uint4(0u, 0u, 0u, 0u);
     }
   }
-  pdl_wait_and_trigger();
-
   // chunk c -> buffer c % ns: unit rows [0, nu), token rows [MT * 16, + nt)
   const int vc = p.kc / 8;                       // 16-byte vectors per chunk row
   const int n_chunks = (nv + vc - 1) / vc;
   const uint32_t stage0 = smem_u32(csm + L.stage);
-  auto issue = [&](int c) {
+  auto issue_rows = [&](int c, int r0, int nr, const uint4* base_src, uint32_t srow0) {
     const uint32_t base = stage0 + static_cast<uint32_t>((c % p.ns) * stage_bytes);
     const int v0 = c * vc, nvc = min(vc, nv - v0);
-    const int total = (nu + nt) * nvc;
+    const int total = nr * nvc;
     for (int i = tid; i < total; i += kClThreads) {
       const int r = i / nvc, v = i - r * nvc;
-      const uint4* src;
-      uint32_t srow;
-      if (r < nu) {
-        src = p.rw + static_cast<size_t>(u0 + r) * nv;
-        srow = static_cast<uint32_t>(r);
-      } else {
-        src = p.x + static_cast<size_t>(t0 + r - nu) * nv;
-        srow = tok_row0 + static_cast<uint32_t>(r - nu);
-      }
-      cp_async16(base + srow * pitch + static_cast<uint32_t>(v * 16), src + v0 + v);
+      cp_async16(base + (srow0 + static_cast<uint32_t>(r)) * pitch + static_cast<uint32_t>(v * 16),
+                 base_src + static_cast<size_t>(r0 + r) * nv + v0 + v);
     }
+  };
+  auto issue_w = [&](int c) { issue_rows(c, u0, nu, p.rw, 0u); };
+  auto issue_x = [&](int c) { issue_rows(c, t0, nt, p.x, tok_row0); };
+  const bool two = n_chunks > 1 && p.ns > 1;
+  // The router rows and the expert bias are layer parameters, not outputs of
+  // the kernel this launch may overlap, so their loads go out before the
+  // dependency wait; the token rows (and k_t) are read after it.
+  if (nu > 0) {
+    issue_w(0);
+    if (two) issue_w(1);
+  }
+  if (rank == 0)
+    for (int u = tid; u < E_r; u += kClThreads)
+      s_bias[u] = p.bias != nullptr ? __ldg(p.bias + u / p.n_sub) : 0.f;
+  pdl_wait_and_trigger();
+  const int kt_pre =
+      (rank == 0 && warp < nt) ? (p.kpt != nullptr ? __ldg(p.kpt + t0 + warp) : p.k_max) : 0;
+  if (nu > 0) {
+    issue_x(0);
+    cp_async_commit();                           // group 0: rows of chunk 0 (and chunk 1's units)
+    if (two) {
+      issue_x(1);
+      cp_async_commit();
+    }
+  }
+  auto issue = [&](int c) {
+    issue_w(c);
+    issue_x(c);
     cp_async_commit();
   };
   float acc[kClMaxMt][4];
@@ -503,10 +521,6 @@ __global__ void __launch_bounds__(kClThreads, 1) route_cluster_kernel(const Clus
   for (int m = 0; m < kClMaxMt; ++m)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[m][j] = 0.f;
-  if (nu > 0) {
-    issue(0);
-    if (n_chunks > 1 && p.ns > 1) issue(1);
-  }
   for (int c = 0; c < n_chunks && nu > 0; ++c) {
     if (c + 1 < n_chunks && p.ns > 1)
       cp_async_wait<1>();
@@ -565,9 +579,9 @@ __global__ void __launch_bounds__(kClThreads, 1) route_cluster_kernel(const Clus
       const int t = t0 + warp;
       const size_t row = static_cast<size_t>(t) * E_r;
       float w;
-      k = warp_topk<IPL>(s_all + warp * E_r, 1, 0, p.bias, p.n_sub,
+      k = warp_topk<IPL>(s_all + warp * E_r, 1, 0, p.bias != nullptr ? s_bias : nullptr, 1,
                          p.logits_out != nullptr ? p.logits_out + row : nullptr,
-                         p.kpt != nullptr ? p.kpt[t] : p.k_max, E_r, p.k_max, p.score,
+                         kt_pre, E_r, p.k_max, p.score,
                          p.renorm, p.route_scale, p.status, lane, &my_u, &w);
       if (lane < p.k_max) {
         const size_t o = static_cast<size_t>(t) * p.k_max + lane;
@@ -607,28 +621,15 @@ __global__ void __launch_bounds__(kClThreads, 1) route_cluster_kernel(const Clus
         if (lane < k) {
           pos = s_off[my_u] + __popc(s_bits[my_u] & ((1u << warp) - 1u));
           p.sorted_token[pos] = t;
-          s_sorted[pos] = t;
         }
         p.inv_row[static_cast<size_t>(t) * p.k_max + lane] = pos;
       }
     }
   }
-  if (fused) {
-    cluster_sync_all();
-    if (p.x_perm != nullptr) {
-      const int n = ld_cluster_s32(mapa_shared(smem_u32(s_off + E_r), 0u));
-      const uint32_t sorted0 = mapa_shared(smem_u32(s_sorted), 0u);
-      for (int r = static_cast<int>(rank) + p.C * warp; r < n; r += p.C * kClWarps) {
-        const int t = ld_cluster_s32(sorted0 + static_cast<uint32_t>(r * 4));
-        const uint4* src = p.x + static_cast<size_t>(t) * nv;
-        uint4* dst = p.x_perm + static_cast<size_t>(r) * nv;
-        for (int v = lane; v < nv; v += 32) dst[v] = __ldg(src + v);
-      }
-    }
-    if (rank == 0)
-      for (int i = tid; i < p.zero_n; i += kClThreads) p.zero_ptr[i] = 0;
-    cluster_sync_all();
-  }
+  // CTA 0 alone finishes: no other CTA reads its shared memory after the
+  // barrier above, so the others may already have exited
+  if (fused && rank == 0)
+    for (int i = tid; i < p.zero_n; i += kClThreads) p.zero_ptr[i] = 0;
 }
 
 }  // namespace
@@ -790,7 +791,6 @@ cudaError_t launch_route_cluster(const void* x, const void* router_w, const floa
     p.offsets = fuse->offsets;
     p.sorted_token = fuse->sorted_token;
     p.inv_row = fuse->inv_row;
-    p.x_perm = static_cast<uint4*>(fuse->x_perm);
     p.zero_ptr = fuse->zero_ptr;
     p.zero_n = fuse->zero_ptr != nullptr ? fuse->zero_n : 0;
   }

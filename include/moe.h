@@ -21,6 +21,14 @@
  *    caller-owned int32 in device memory that the caller zeroes; the first
  *    error wins.  Read it with moe_get_device_status (the only call that
  *    synchronises).
+ *  - Kernels are launched with programmatic dependent launch: the first
+ *    kernel of a call may start while the previous kernel on `stream`
+ *    finishes.  It reads the layer's parameters (router_w, expert_bias)
+ *    before it waits for that kernel and every other input after; so a
+ *    parameter must not be written by a kernel on the same stream that is
+ *    still running when the call starts (one that lets its dependents launch
+ *    early).  Inputs written by the preceding kernel (x, k_per_token, ...)
+ *    are always read after it has finished.
  *  - `workspace` is caller-owned device memory of at least
  *    moe_workspace_size(desc) bytes, 256-byte aligned.  Calls on the same
  *    workspace must not overlap in time.
@@ -167,9 +175,8 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, const vo
                              void* workspace, void* stream);
 
 /* moe_permute without a workspace, for callers that cannot allocate device
- * memory where they route (while a stream is being captured into a CUDA
- * graph, inside a serving loop that must stay out of the allocator, or in a
- * plug-in that owns no buffers of its own).  The published method has no
+ * memory where they route (inside a serving loop that must stay out of the
+ * allocator, or in a plug-in that owns no buffers of its own).  The published method has no
  * counterpart to this call: it only changes where the scratch lives.
  *   Arguments and results are those of moe_permute, minus `workspace`.
  *   Scratch: a 1 MiB array in device memory that every GPU loading this

@@ -1,8 +1,8 @@
 """moe_permute_static: the permutation for callers that cannot allocate.
 
-Some callers cannot hand the library a workspace: they route tokens while a
-stream is being captured into a CUDA graph, inside a serving loop that must
-stay out of the allocator, or from a plug-in that owns no device buffers.
+Some callers cannot hand the library a workspace: they route tokens inside a
+serving loop that must stay out of the allocator, or from a plug-in that owns
+no device buffers.
 moe_permute_static keeps its scratch in the library's own device array; this
 checks, through the C ABI, that it returns exactly what moe_permute (with a
 workspace) returns, on two different routings in a row (so nothing left in

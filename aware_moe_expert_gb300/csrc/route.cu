@@ -183,7 +183,7 @@ __device__ __forceinline__ unsigned long long warp_select_topk(const uint32_t (&
 // bias[u / n_sub] when bias is given, and is stored to lout[u] when lout is
 // given.  Lane j < k ends up holding the j-th unit (*out_u) and its gate
 // weight after renormalisation and route_scale (*out_w).  Returns k.
-template <int IPL>
+template <int IPL, int SB = 2>
 __device__ __forceinline__ int warp_topk(const float* __restrict__ P, int S, size_t sstride,
                                          const float* __restrict__ bias, int n_sub,
                                          float* __restrict__ lout, int kt, int E_r, int k_max,
@@ -208,7 +208,6 @@ __device__ __forceinline__ int warp_topk(const float* __restrict__ P, int S, siz
     }
   }
   // add the remaining partial rows in slice order, SB slices' loads in flight
-  constexpr int SB = IPL >= 4 ? 2 : 8 / IPL;
   for (int s0 = 1; s0 < S; s0 += SB) {
     float pv[SB][IPL];
 #pragma unroll
@@ -277,7 +276,7 @@ __device__ __forceinline__ int warp_topk(const float* __restrict__ P, int S, siz
 // rows of row_bytes = 4 * ceil(T / 32) bytes, the uint32 words the scan
 // reads), so the permutation needs no pass of its own over topk_idx.  The
 // last CTA also zeroes the row bytes past the last token group.
-template <int IPL>
+template <int IPL, int SB>
 __global__ void __launch_bounds__(256) topk_gate_kernel(
     const float* __restrict__ P, int S, const float* __restrict__ bias, int n_sub,
     float* __restrict__ logits_out, const int32_t* __restrict__ kpt, int T, int E_r,
@@ -296,7 +295,7 @@ __global__ void __launch_bounds__(256) topk_gate_kernel(
     int u;
     float w;
     const size_t row = static_cast<size_t>(t) * E_r;
-    warp_topk<IPL>(P + row, S, static_cast<size_t>(T) * E_r, bias, n_sub,
+    warp_topk<IPL, SB>(P + row, S, static_cast<size_t>(T) * E_r, bias, n_sub,
                    logits_out != nullptr ? logits_out + row : nullptr,
                    kpt != nullptr ? kpt[t] : k_max, E_r, k_max, score,
                    renorm, route_scale, status, lane, &u, &w);
@@ -810,8 +809,11 @@ cudaError_t launch_topk_gate(const float* partial, int S, const float* bias, int
   const int grid = (T + 7) / 8;
   uint8_t* bm = reinterpret_cast<uint8_t*>(bitmap);
   const int row_bytes = 4 * ((T + 31) / 32);
+  // many partial slices (split-K routers of small batches): every slice's
+  // loads in one round trip; otherwise two at a time (fewer registers)
 #define MOE_TOPK_LAUNCH(IPL)                                                                 \
-  launch_pdl(topk_gate_kernel<IPL>, dim3(grid), dim3(256), 0, s, partial, S, bias, n_sub,     \
+  launch_pdl(S > 2 ? topk_gate_kernel<IPL, 8> : topk_gate_kernel<IPL, 2>, dim3(grid),        \
+             dim3(256), 0, s, partial, S, bias, n_sub,                                        \
              logits_out, k_per_token, T, E_r, k_max, score, renorm, route_scale, topk_idx,    \
              topk_w, status, bm, row_bytes)
   if (E_r <= 32) return MOE_TOPK_LAUNCH(1);

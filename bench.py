@@ -581,8 +581,19 @@ def run_ours(args, wl, rank, world, local):
     F_router = 2.0 * T * H * router_rows
     F = F_routed + F_shared + F_router
     Bytes = 2.0 * (D * 3 * H * I_sub + 3 * H * wl.I_shared + router_rows * H + 2 * T * H)
-    t_roof_us = max(F / (peaks["bf16_tflops"] * 1e12), Bytes / (peaks["hbm_gbs"] * 1e9)) * 1e6
-    bound = "tensor" if F / (peaks["bf16_tflops"] * 1e12) > Bytes / (peaks["hbm_gbs"] * 1e9) else "hbm"
+    # The bf16 peak a tensor-bound line is judged against: the burst rate
+    # (cuBLAS timed alone) for steps under 1 ms, the sustained rate (cuBLAS
+    # back to back for seconds, at the power cap) for longer steps, which run
+    # back to back under the same cap.  Both fractions are reported.
+    long_step = ms >= 1.0
+    P_bf16 = peaks["bf16_tflops_sustained"] if long_step else peaks["bf16_tflops"]
+    peak_kind = "sustained" if long_step else "burst"
+    t_F = F / (P_bf16 * 1e12)
+    t_B = Bytes / (peaks["hbm_gbs"] * 1e9)
+    t_roof_us = max(t_F, t_B) * 1e6
+    bound = "tensor" if t_F > t_B else "hbm"
+    t_roof_burst_us = max(F / (peaks["bf16_tflops"] * 1e12), t_B) * 1e6
+    t_roof_sus_us = max(F / (peaks["bf16_tflops_sustained"] * 1e12), t_B) * 1e6
 
     # dominant kernel.  Decode: moe_grouped_ffn, whose work is one fused
     # kernel (gate|up + SwiGLU + down) after the row gather; prefill: the
@@ -601,11 +612,15 @@ def run_ours(args, wl, rank, world, local):
     else:
         alg = 4.0 * H * I_sub * n_assign
         achieved = alg / (gu_us * 1e-6) / 1e12
-        pk = peaks["bf16_tflops"]
+        pk = P_bf16
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk, "unit": "TFLOP/s",
                 "frac": round(achieved / pk, 4), "traffic": traffic_for(wl.name, "gate_up", 1.0),
                 "kernel": "moe_gate_up (row gather + grouped gate|up GEMM, SwiGLU epilogue)",
-                "algorithmic_flops": alg, "peak_source": peaks["source"] + " bf16_tflops (burst)"}
+                "algorithmic_flops": alg,
+                "peak_source": peaks["source"] + (" bf16_tflops_sustained (step of 1 ms or more)"
+                                                  if long_step else " bf16_tflops (burst)"),
+                "frac_burst": round(achieved / peaks["bf16_tflops"], 4),
+                "frac_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4)}
 
     n_launch = launches_per_step(wl, T, args.path, fold=fold is not None, cg=cg is not None) + \
         (2 if cg is not None else 0)
@@ -639,7 +654,10 @@ def run_ours(args, wl, rank, world, local):
                             f"per step vs {l2 >> 20} MiB L2)")}
     res["realised"] = {"n_assign": n_assign, "distinct_units": D, "k_mean": n_assign / T}
     res["roofline_layer"] = {"t_roof_us": round(t_roof_us, 2), "bound": bound,
-                             "frac": round(t_roof_us / us, 4), "flops": F, "bytes": Bytes}
+                             "frac": round(t_roof_us / us, 4), "flops": F, "bytes": Bytes,
+                             "bf16_peak": peak_kind,
+                             "frac_burst": round(t_roof_burst_us / us, 4),
+                             "frac_sustained": round(t_roof_sus_us / us, 4)}
     res["roofline"] = roof
     res["breakdown_us"] = {k: round(v, 2) for k, v in parts.items()}
     res["gpu_launches"] = n_launch * args.steps

@@ -29,17 +29,30 @@ __global__ void __launch_bounds__(256) bitmap_kernel(const int32_t* __restrict__
   for (int u = threadIdx.x; u < E_r; u += blockDim.x) bits[u] = 0u;
   __syncthreads();
   const int word = blockIdx.x;
-  for (int i = threadIdx.x; i < 32 * k_max; i += blockDim.x) {
+  // a thread's slots (at most 32 * 32 / 256 = 4): every load in flight at once
+  constexpr int kPer = 4;
+  int kk[kPer], uu[kPer];
+#pragma unroll
+  for (int r = 0; r < kPer; ++r) {
+    const int i = threadIdx.x + r * blockDim.x;
+    const int t = word * 32 + i / k_max;
+    const bool in = i < 32 * k_max && t < T;
+    kk[r] = in ? kpt[t] : 0;
+    uu[r] = in ? topk_idx[static_cast<size_t>(word) * 32 * k_max + i] : -1;
+  }
+#pragma unroll
+  for (int r = 0; r < kPer; ++r) {
+    const int i = threadIdx.x + r * blockDim.x;
     const int tl = i / k_max, j = i - tl * k_max;
     const int t = word * 32 + tl;
-    if (t >= T) continue;
-    int k = kpt[t];
+    if (i >= 32 * k_max || t >= T) continue;
+    int k = kk[r];
     if (k < 1 || k > k_max) {
       if (j == 0) report(status, MOE_ERR_K_RANGE);
       k = min(max(k, 0), k_max);
     }
     if (j >= k) continue;
-    const int u = topk_idx[static_cast<size_t>(t) * k_max + j];
+    const int u = uu[r];
     if (u < 0 || u >= E_r) {
       report(status, MOE_ERR_BAD_INDEX);
       continue;
@@ -125,10 +138,11 @@ __global__ void __launch_bounds__(256) scatter_kernel(
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= static_cast<long long>(T) * k_max) return;
   const int t = static_cast<int>(i / k_max), j = static_cast<int>(i - static_cast<long long>(t) * k_max);
-  const int k = min(max(kpt[t], 0), k_max);
+  const int kt = kpt[t];
+  const int u = topk_idx[i];   // read with k_t (unused past it)
+  const int k = min(max(kt, 0), k_max);
   int pos = -1;
   if (j < k) {
-    const int u = topk_idx[i];
     if (u >= 0 && u < E_r) {
       const int w = t >> 5;
       const uint32_t below = (1u << (t & 31)) - 1u;

@@ -32,7 +32,8 @@ EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_gate_up", "moe
            "moe_get_device_status", "moe_status_string", "moe_permute_static",
            "moe_cg_workspace_size", "moe_pack_proxy_rows", "moe_route_cg",
            "moe_layer_forward_cg", "moe_fold_decode", "moe_layer_forward_fold",
-           "moe_cost_lookup", "moe_tier_schedule", "moe_layer_forward_paths")
+           "moe_cost_lookup", "moe_tier_schedule", "moe_layer_forward_paths",
+           "moe_layer_forward_host")
 
 
 class MoeLayerDesc(ctypes.Structure):
@@ -97,6 +98,8 @@ def lib() -> ctypes.CDLL:
             "moe_shared_ffn": (ctypes.c_int, [D, vp, vp, i32p, vp, vp]),
             "moe_combine": (ctypes.c_int, [D, vp, vp, i32p, vp, i32p, vp, i32p, vp]),
             "moe_layer_forward": (ctypes.c_int, [D, vp, vp, vp, vp, i32p, vp, i32p, vp, vp]),
+            "moe_layer_forward_host": (ctypes.c_int, [D, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                                      vp, vp, vp]),
             "moe_get_device_status": (ctypes.c_int, [i32p, vp]),
             "moe_cg_workspace_size": (ctypes.c_size_t, [D, ctypes.POINTER(MoeCgRouter)]),
             "moe_pack_proxy_rows": (ctypes.c_int, [D, ctypes.c_int32, vp, i32p, vp, i32p, vp]),
@@ -265,6 +268,17 @@ def moe_layer_forward(desc, x, router_w, w_gate_up, w_down, k_per_token, out, de
     return lib().moe_layer_forward(ctypes.byref(d), _ptr(x), _ptr(router_w), _ptr(w_gate_up),
                                    _ptr(w_down), _ptr(k_per_token), _ptr(out), _ptr(dev_status),
                                    _ptr(workspace), _stream(stream))
+
+
+def moe_layer_forward_host(desc, x_host, k_host, out_host, x_dev, k_dev, out_dev, router_w,
+                           w_gate_up, w_down, dev_status, workspace, stream=None) -> int:
+    """x_host, k_host, out_host: CPU tensors (pinned for an asynchronous call)
+    or raw host addresses; the rest as for moe_layer_forward."""
+    d = desc if isinstance(desc, MoeLayerDesc) else desc.c()
+    return lib().moe_layer_forward_host(ctypes.byref(d), _ptr(x_host), _ptr(k_host),
+                                        _ptr(out_host), _ptr(x_dev), _ptr(k_dev), _ptr(out_dev),
+                                        _ptr(router_w), _ptr(w_gate_up), _ptr(w_down),
+                                        _ptr(dev_status), _ptr(workspace), _stream(stream))
 
 
 @dataclass

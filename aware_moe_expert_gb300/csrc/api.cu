@@ -890,6 +890,28 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, const vo
   return do_combine(desc, yperm, ysh, inv_row, topk_w, k_per_token, out, dev_status, s);
 }
 
+moe_status moe_layer_forward_host(const moe_layer_desc* desc, const void* x_host,
+                                  const int32_t* k_host, void* out_host, void* x_dev,
+                                  int32_t* k_dev, void* out_dev, const void* router_w,
+                                  const void* w_gate_up, const void* w_down,
+                                  int32_t* dev_status, void* workspace, void* stream) {
+  MOE_TRY(validate(desc));
+  if (desc->T == 0) return MOE_OK;
+  if (x_host == nullptr || k_host == nullptr || out_host == nullptr)
+    return MOE_ERR_INVALID_ARGUMENT;
+  MOE_TRY(check_ptrs({x_dev, router_w, w_gate_up, w_down, out_dev}));
+  MOE_TRY(check_ptrs4({k_dev, dev_status}));
+  MOE_TRY(check_ws(workspace));
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t act_bytes = static_cast<size_t>(desc->T) * desc->H * 2;
+  MOE_TRY(cuda_status(cudaMemcpyAsync(x_dev, x_host, act_bytes, cudaMemcpyHostToDevice, s)));
+  MOE_TRY(cuda_status(cudaMemcpyAsync(k_dev, k_host, static_cast<size_t>(desc->T) * 4,
+                                      cudaMemcpyHostToDevice, s)));
+  MOE_TRY(moe_layer_forward(desc, x_dev, router_w, w_gate_up, w_down, k_dev, out_dev,
+                            dev_status, workspace, stream));
+  return cuda_status(cudaMemcpyAsync(out_host, out_dev, act_bytes, cudaMemcpyDeviceToHost, s));
+}
+
 size_t moe_cg_workspace_size(const moe_layer_desc* desc, const moe_cg_router* cg) {
   if (validate_cg(desc, cg) != MOE_OK) return 0;
   return cg_layout_of(*desc, *cg).total;

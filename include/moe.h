@@ -174,6 +174,24 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, const vo
                              const int32_t* k_per_token, void* out, int32_t* dev_status,
                              void* workspace, void* stream);
 
+/* moe_layer_forward for callers whose token-side tensors live in host memory
+ * (a serving loop that receives activations from the host and returns the
+ * layer's output there).  On `stream`: x_host -> x_dev (bf16 [T, H]) and
+ * k_host -> k_dev (int32 [T]) host-to-device copies, moe_layer_forward on the
+ * device copies, then out_dev -> out_host (bf16 [T, H]).  x_dev, k_dev and
+ * out_dev are caller-owned device buffers of those sizes; the weights, the
+ * workspace and dev_status are as for moe_layer_forward.  Nothing is
+ * allocated.  With pinned (page-locked) host buffers the whole call is
+ * asynchronous; pageable ones make the copies synchronise with the host.
+ * Host-side argument errors are reported before any copy is enqueued; a
+ * failed copy returns MOE_ERR_CUDA.  (A host-memory convenience around the
+ * layer of MoE-Prism §III-B; the paper's layer is moe_layer_forward.) */
+moe_status moe_layer_forward_host(const moe_layer_desc* desc, const void* x_host,
+                                  const int32_t* k_host, void* out_host, void* x_dev,
+                                  int32_t* k_dev, void* out_dev, const void* router_w,
+                                  const void* w_gate_up, const void* w_down,
+                                  int32_t* dev_status, void* workspace, void* stream);
+
 /* moe_permute without a workspace, for callers that cannot allocate device
  * memory where they route (inside a serving loop that must stay out of the
  * allocator, or in a plug-in that owns no buffers of its own).  The published method has no

@@ -85,6 +85,21 @@ def test_host_rejects_bad_arguments_without_a_gpu(lib):
     assert B.moe_grouped_ffn(d, fake + 2, fake, fake, fake, fake, fake, fake, ws, 0) == 1
     # workspace missing or misaligned
     assert B.moe_layer_forward(d, fake, fake, fake, fake, fake, fake, fake, None, 0) == 3
+
+
+def test_host_buffer_forward_rejects_bad_arguments_before_copying(lib):
+    """moe_layer_forward_host checks the descriptor, the host and device
+    pointers and the workspace on the host, before any copy is enqueued."""
+    d = _desc()
+    fake = 1 << 20                      # aligned, never dereferenced
+    ws = 1 << 21
+    args = [fake] * 9                   # x_host, k_host, out_host, x_dev, k_dev, out_dev, weights
+    assert B.moe_layer_forward_host(_desc(H=100), *args, fake, ws, 0) == 2
+    assert B.moe_layer_forward_host(d, None, *args[1:], fake, ws, 0) == 1
+    assert B.moe_layer_forward_host(d, *args[:3], None, *args[4:], fake, ws, 0) == 1
+    assert B.moe_layer_forward_host(d, *args, None, ws, 0) == 1
+    assert B.moe_layer_forward_host(d, *args, fake, None, 0) == 3
+    assert B.moe_layer_forward_host(_desc(T=0), *args, fake, ws, 0) == 0
     assert B.moe_layer_forward(d, fake, fake, fake, fake, fake, fake, fake, ws + 16, 0) == 3
     # shared expert requested without weights
     assert B.moe_shared_ffn(_desc(), fake, fake, fake, ws, 0) == 1

@@ -243,3 +243,31 @@ def test_layer_prefill_ragged_token_counts(T):
         tokens = np.unique(np.concatenate([[0, T - 1], rng.choice(T, 256, replace=False)]))
     fro, n_tied = _compare(wl, d, desc, out, Lg, idx, tokens)
     assert fro <= 5e-3
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name,T", [("qwen_decode", 1), ("qwen_decode", 8), ("mixtral_decode", None),
+                                    ("tiny", 300)])
+def test_host_buffer_forward_matches_the_device_forward(name, T):
+    """moe_layer_forward_host (x and k copied in from pinned host memory, out
+    copied back) gives exactly what moe_layer_forward gives on device copies
+    of the same inputs, on two calls in a row."""
+    wl = WL.ALL[name] if T is None else WL.ALL[name].with_T(T)
+    d = make_layer_inputs(wl, DEV)
+    desc = B.desc_for(wl, expert_bias=d["expert_bias"])
+    layer = B.MoeLayer(desc, DEV)
+    ref = layer.forward(d["x"], d["router_w"], d["w_gate_up"], d["w_down"], d["k_per_token"])
+    assert layer.device_status() == 0
+    x_h = d["x"].cpu().pin_memory()
+    k_h = d["k_per_token"].cpu().pin_memory()
+    x_d = torch.empty_like(d["x"])
+    k_d = torch.empty_like(d["k_per_token"])
+    out_d = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    for _ in range(2):
+        out_h = torch.zeros(wl.T, wl.H, dtype=torch.bfloat16).pin_memory()
+        B.check(B.moe_layer_forward_host(desc, x_h, k_h, out_h, x_d, k_d, out_d, d["router_w"],
+                                         d["w_gate_up"], d["w_down"], st, layer.workspace),
+                "moe_layer_forward_host")
+        assert B.moe_get_device_status(st) == 0     # synchronises the stream
+        assert torch.equal(out_h.view(torch.int16), ref.cpu().view(torch.int16))

@@ -567,8 +567,61 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// Encoded tensor maps, keyed by everything that goes into them, so that a
+// call on tensors seen before skips the encoding (host time of the small
+// decode calls); host memory only.  A direct-mapped table: a slot whose key
+// differs is re-encoded and overwritten.
+namespace {
+struct TmapKey {
+  const void* base;
+  long long rows;
+  int cols, box_rows, elem;
+  bool operator==(const TmapKey& o) const {
+    return base == o.base && rows == o.rows && cols == o.cols && box_rows == o.box_rows &&
+           elem == o.elem;
+  }
+};
+constexpr int kTmapSlots = 256;
+struct TmapCache {
+  std::mutex mu;
+  TmapKey key[kTmapSlots] = {};
+  CUtensorMap map[kTmapSlots];
+  bool used[kTmapSlots] = {};
+};
+TmapCache& tmap_cache() {
+  static TmapCache c;
+  return c;
+}
+int tmap_slot(const TmapKey& k) {
+  uint64_t h = reinterpret_cast<uintptr_t>(k.base) >> 4;
+  h ^= static_cast<uint64_t>(k.rows) * 0x9E3779B97F4A7C15ull;
+  h ^= (static_cast<uint64_t>(k.cols) << 20) ^ (static_cast<uint64_t>(k.box_rows) << 8) ^
+       static_cast<uint64_t>(k.elem);
+  h ^= h >> 29;
+  return static_cast<int>(h % kTmapSlots);
+}
+bool tmap_lookup(const TmapKey& k, CUtensorMap* m) {
+  TmapCache& c = tmap_cache();
+  const int i = tmap_slot(k);
+  std::lock_guard<std::mutex> g(c.mu);
+  if (!c.used[i] || !(c.key[i] == k)) return false;
+  *m = c.map[i];
+  return true;
+}
+void tmap_store(const TmapKey& k, const CUtensorMap& m) {
+  TmapCache& c = tmap_cache();
+  const int i = tmap_slot(k);
+  std::lock_guard<std::mutex> g(c.mu);
+  c.key[i] = k;
+  c.map[i] = m;
+  c.used[i] = true;
+}
+}  // namespace
+
 // bf16 [rows, cols] row-major, box = 64 columns x box_rows rows, 128-B swizzle.
 bool make_tmap_bf16(CUtensorMap* m, const void* base, long long rows, int cols, int box_rows) {
+  const TmapKey key{base, rows, cols, box_rows, 2};
+  if (rows > 0 && tmap_lookup(key, m)) return true;
   auto fn = encode_fn();
   if (fn == nullptr || rows <= 0) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
@@ -579,11 +632,15 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, long long rows, int cols, 
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  if (r != CUDA_SUCCESS) return false;
+  tmap_store(key, *m);
+  return true;
 }
 
 // fp32 [rows, cols] row-major, boxes of 32 columns (128 bytes) x box_rows.
 bool make_tmap_f32(CUtensorMap* m, const void* base, long long rows, int cols, int box_rows) {
+  const TmapKey key{base, rows, cols, box_rows, 4};
+  if (rows > 0 && tmap_lookup(key, m)) return true;
   auto fn = encode_fn();
   if (fn == nullptr || rows <= 0 || cols % 32 != 0 ||
       (reinterpret_cast<uintptr_t>(base) & 15u) != 0)
@@ -596,7 +653,9 @@ bool make_tmap_f32(CUtensorMap* m, const void* base, long long rows, int cols, i
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  if (r != CUDA_SUCCESS) return false;
+  tmap_store(key, *m);
+  return true;
 }
 
 bool gemm_supports_f32_router(int E_r) { return E_r == 64 || E_r == 128 || E_r == 256; }

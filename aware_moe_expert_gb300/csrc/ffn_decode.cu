@@ -56,7 +56,10 @@ struct FfnCfg {
   static constexpr uint32_t kOffOffs = kOffPrefix + (kMaxGroups + 1) * 4;
   static constexpr uint32_t kOffX = (kOffOffs + (kMaxGroups + 1) * 4 + 15) / 16 * 16;
   static constexpr uint32_t kSmemBytes = kOffX + kGU * 17 * 4 + 1024;
-  static constexpr uint32_t kTmemCols = 2 * CHUNK < 32 ? 32 : 2 * CHUNK;  // 2 accumulators
+  // two accumulator buffers of CHUNK columns, or of 2 * CHUNK when a down item
+  // is two 128-row blocks (DPAIR: one block per half of the buffer)
+  static constexpr uint32_t kTmemCols = 2 * CHUNK < 32 ? 32 : 2 * CHUNK;
+  static constexpr uint32_t kTmemColsPair = 4 * CHUNK < 32 ? 32 : 4 * CHUNK;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -66,7 +69,7 @@ struct FParams {
   int H;
   int I;
   int gu_tiles;          // I / 64 gate|up items per token chunk
-  int dn_tiles;          // H / 128 down items per token chunk
+  int dn_tiles;          // down items per token chunk: H / 128, or H / 256 (DPAIR)
   __nv_bfloat16* act;    // [out_rows, I]
   __nv_bfloat16* y;      // [out_rows, H]
   int32_t* done;         // [m-tiles] gate|up items finished per chunk; zero at launch
@@ -148,7 +151,7 @@ __device__ __forceinline__ Item item_of(int w, int n_gu, int S, int gu_tiles, in
 // item queue like the MMA and epilogue warps, arrive on every stage's `full`
 // (copies for gate|up items, none for down items, whose activation rows come
 // by TMA), and the producer then loads only weights for gate|up items.
-template <int CHUNK, int STAGES, bool GATHER = false>
+template <int CHUNK, int STAGES, bool GATHER = false, bool DPAIR = false>
 __global__ void __launch_bounds__(GATHER ? kThreads + kGatherThreads : kThreads, 1)
     decode_ffn_kernel(const __grid_constant__ CUtensorMap tmWgu,
                       const __grid_constant__ CUtensorMap tmX16,
@@ -212,7 +215,7 @@ __global__ void __launch_bounds__(GATHER ? kThreads + kGatherThreads : kThreads,
     tma_prefetch_desc(&tmA64);
   }
   if (warp == 1) {
-    tmem_alloc(s_tmem, kTmemCols);
+    tmem_alloc(s_tmem, DPAIR ? Cfg::kTmemColsPair : kTmemCols);
     tmem_relinquish();
   }
   pdl_wait_and_trigger();
@@ -225,7 +228,9 @@ __global__ void __launch_bounds__(GATHER ? kThreads + kGatherThreads : kThreads,
   const uint32_t tmem_base = *s_tmem;
   const int n_mt = *s_total;
   const int KB_gu = p.H / (kBK * kKsub);
-  const int KB_dn = p.I / (kBK * kKsub);
+  // stages of a down item: 128 columns of K each, or 64 (DPAIR)
+  const int KB_dn = DPAIR ? p.I / kBK : p.I / (kBK * kKsub);
+  constexpr int acc_cols = DPAIR ? 2 * kChunk : kChunk;   // TMEM columns per accumulator buffer
   // Few gate|up items (small batches): split each over the hidden dimension
   // so that more SMs stream the weights; the last split to finish adds the
   // partial sums in split order and applies SwiGLU.
@@ -266,13 +271,20 @@ __global__ void __launch_bounds__(GATHER ? kThreads + kGatherThreads : kThreads,
         const bool wide = nb > 2;
         const uint32_t tok_rows = wide ? 64u : static_cast<uint32_t>(nb * kTokBox);
         const bool gathered = GATHER && it.gu;   // token rows come from the gather warps
-        const uint32_t bytes = gathered ? kW : kW + kKsub * tok_rows * kBK * 2;
+        const bool dpair = DPAIR && !it.gu;   // two weight blocks, one token sub-block
+        const uint32_t bytes =
+            gathered ? kW : kW + (dpair ? 1u : static_cast<uint32_t>(kKsub)) * tok_rows * kBK * 2;
         const int kb0 = it.gu ? it.s * KB_split : 0;
         const int kb1 = it.gu ? kb0 + KB_split : KB_dn;
         const CUtensorMap* mW = it.gu ? &tmWgu : &tmWdn;
         const CUtensorMap* mT = it.gu ? (wide ? &tmX64 : &tmX16) : (wide ? &tmA64 : &tmA16);
-        const int wrow = it.gu ? t.g * 2 * p.I + it.m * kGU : t.g * p.H + it.m * kM;
+        const int wrow = it.gu ? t.g * 2 * p.I + it.m * kGU : t.g * p.H + it.m * (dpair ? 2 * kM : kM);
         auto weights = [&](uint8_t* sa, int kb) {
+          if (dpair) {   // rows wrow.. and wrow + 128.. of the stage's 64 columns
+            tma_load_2d(sa, mW, &full[stage], kb * kBK, wrow);
+            tma_load_2d(sa + kWSub, mW, &full[stage], kb * kBK, wrow + kM);
+            return;
+          }
 #pragma unroll
           for (int j = 0; j < kKsub; ++j) {
             const int kc = (kb * kKsub + j) * kBK;
@@ -284,7 +296,8 @@ __global__ void __launch_bounds__(GATHER ? kThreads + kGatherThreads : kThreads,
         auto tokens = [&](uint8_t* sb, uint64_t* bar, int kb) {
 #pragma unroll
           for (int j = 0; j < kKsub; ++j) {
-            const int kc = (kb * kKsub + j) * kBK;
+            if (dpair && j > 0) break;
+            const int kc = dpair ? kb * kBK : (kb * kKsub + j) * kBK;
             if (wide) {
               tma_load_2d(sb + j * kTokSub, mT, bar, kc, t.row0);
             } else {
@@ -380,20 +393,35 @@ __global__ void __launch_bounds__(GATHER ? kThreads + kGatherThreads : kThreads,
           break;
         }
         tc_fence_after();
-        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kChunk);
+        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * acc_cols);
+        const bool dpair = DPAIR && !it.gu;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(&full[stage], phase, s_abort)) {
             ok = false;
             break;
           }
           tc_fence_after();
+          if (dpair) {
+            // weight blocks 0 and 1 of the stage against its one token
+            // sub-block, into the two halves of the accumulator buffer
+            const uint64_t b = sdesc_sw128(smem_u32(smem + kOffB + stage * kTok));
 #pragma unroll
-          for (int j = 0; j < kKsub; ++j) {
-            const uint64_t a = sdesc_sw128(smem_u32(smem + stage * kW + j * kWSub));
-            const uint64_t b = sdesc_sw128(smem_u32(smem + kOffB + stage * kTok + j * kTokSub));
+            for (int h = 0; h < 2; ++h) {
+              const uint64_t a = sdesc_sw128(smem_u32(smem + stage * kW + h * kWSub));
 #pragma unroll
-            for (int k = 0; k < kBK / 16; ++k)
-              umma_bf16(d, a + 2u * k, b + 2u * k, idesc, (kb | j | k) != 0 ? 1u : 0u);
+              for (int k = 0; k < kBK / 16; ++k)
+                umma_bf16(d + static_cast<uint32_t>(h * kChunk), a + 2u * k, b + 2u * k, idesc,
+                          (kb | k) != 0 ? 1u : 0u);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < kKsub; ++j) {
+              const uint64_t a = sdesc_sw128(smem_u32(smem + stage * kW + j * kWSub));
+              const uint64_t b = sdesc_sw128(smem_u32(smem + kOffB + stage * kTok + j * kTokSub));
+#pragma unroll
+              for (int k = 0; k < kBK / 16; ++k)
+                umma_bf16(d, a + 2u * k, b + 2u * k, idesc, (kb | j | k) != 0 ? 1u : 0u);
+            }
           }
           umma_commit(&empty[stage]);
           if (++stage == kStages) {
@@ -569,7 +597,7 @@ __global__ void __launch_bounds__(GATHER ? kThreads + kGatherThreads : kThreads,
       }
       tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                          static_cast<uint32_t>(acc * kChunk);
+                          static_cast<uint32_t>(acc * acc_cols);
       if (it.gu && S == 1) {
         const bool is_gate = q < 2;
         const int nl = (q & 1) * 32 + lane;
@@ -637,16 +665,20 @@ __global__ void __launch_bounds__(GATHER ? kThreads + kGatherThreads : kThreads,
           if (warp == 2 && lane == 0) atomicAdd(p.done + it.mt, 1);
         }
       } else {
-        const int col = it.m * kM + r_in;
-        for (int c0 = 0; c0 < t.rows; c0 += 16) {
-          uint32_t v[16];
-          tmem_ld16(tb + c0, v);
-          tmem_ld_wait();
+        // down: one 128-row block, or two (DPAIR: rows h * 128 + r_in)
+#pragma unroll 1
+        for (int h = 0; h < (DPAIR ? 2 : 1); ++h) {
+          const int col = it.m * (DPAIR ? 2 * kM : kM) + h * kM + r_in;
+          for (int c0 = 0; c0 < t.rows; c0 += 16) {
+            uint32_t v[16];
+            tmem_ld16(tb + static_cast<uint32_t>(h * kChunk) + c0, v);
+            tmem_ld_wait();
 #pragma unroll
-          for (int cc = 0; cc < 16; ++cc) {
-            const long long r = static_cast<long long>(t.row0) + c0 + cc;
-            if (c0 + cc < t.rows && r < p.out_rows)
-              p.y[r * p.H + col] = __float2bfloat16_rn(__uint_as_float(v[cc]));
+            for (int cc = 0; cc < 16; ++cc) {
+              const long long r = static_cast<long long>(t.row0) + c0 + cc;
+              if (c0 + cc < t.rows && r < p.out_rows)
+                p.y[r * p.H + col] = __float2bfloat16_rn(__uint_as_float(v[cc]));
+            }
           }
         }
       }
@@ -664,7 +696,7 @@ __global__ void __launch_bounds__(GATHER ? kThreads + kGatherThreads : kThreads,
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc(tmem_base, DPAIR ? Cfg::kTmemColsPair : kTmemCols);
   }
 }
 
@@ -726,21 +758,45 @@ cudaError_t launch_decode_ffn(const DecodeFfnArgs& a, cudaStream_t s) {
                       Cfg::kSmemBytes, s, wgu, x16, x64, wdn, a16, a64, p);
   }
   using Cfg = FfnCfg<64, 4>;
+  // Small I with 64-token chunks: down items of two 128-row blocks (half as
+  // many items, each streaming twice the weights through the same 32 KB
+  // stages).  Same-box A/B, Qwen3-30B-A3B-shaped decode (I_sub 384): T = 64
+  // 197.4 -> 186.8 us, T = 256 222.3 -> 212.0, T = 1024 238.2 -> 231.7; with
+  // 16-token chunks (T <= 16) the halved item count costs more than it saves
+  // (T = 1 28.6 -> 32.4 us), so those keep one block per item.  A template
+  // parameter: the other variants keep their code and registers.
+  const bool dpair = a.I <= 1024 && a.H % (2 * kM) == 0;
+  if (dpair) p.dn_tiles = a.H / (2 * kM);
+  auto go = [&](auto kern, int threads) -> cudaError_t {
+    return launch_pdl(kern, dim3(a.sm_count), dim3(threads), Cfg::kSmemBytes, s, wgu, x16, x64,
+                      wdn, a16, a64, p);
+  };
   if (gather) {
+    if (dpair) {
+      static bool attr_done[64] = {false};
+      cudaError_t e = set_smem_once(decode_ffn_kernel<64, 4, true, true>,
+                                    static_cast<int>(Cfg::kSmemBytes), attr_done);
+      if (e != cudaSuccess) return e;
+      return go(decode_ffn_kernel<64, 4, true, true>, kThreads + kGatherThreads);
+    }
     static bool attr_done[64] = {false};
     cudaError_t e = set_smem_once(decode_ffn_kernel<64, 4, true>,
                                   static_cast<int>(Cfg::kSmemBytes), attr_done);
     if (e != cudaSuccess) return e;
-    return launch_pdl(decode_ffn_kernel<64, 4, true>, dim3(a.sm_count),
-                      dim3(kThreads + kGatherThreads), Cfg::kSmemBytes, s, wgu, x16, x64, wdn,
-                      a16, a64, p);
+    return go(decode_ffn_kernel<64, 4, true>, kThreads + kGatherThreads);
+  }
+  if (dpair) {
+    static bool attr_done[64] = {false};
+    cudaError_t e = set_smem_once(decode_ffn_kernel<64, 4, false, true>,
+                                  static_cast<int>(Cfg::kSmemBytes), attr_done);
+    if (e != cudaSuccess) return e;
+    return go(decode_ffn_kernel<64, 4, false, true>, kThreads);
   }
   static bool attr_done[64] = {false};
   cudaError_t e = set_smem_once(decode_ffn_kernel<64, 4>, static_cast<int>(Cfg::kSmemBytes),
                                 attr_done);
   if (e != cudaSuccess) return e;
-  return launch_pdl(decode_ffn_kernel<64, 4>, dim3(a.sm_count), dim3(kThreads), Cfg::kSmemBytes,
-                    s, wgu, x16, x64, wdn, a16, a64, p);
+  return go(decode_ffn_kernel<64, 4>, kThreads);
 }
 
 }  // namespace moe

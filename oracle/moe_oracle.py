@@ -31,9 +31,13 @@ Readings taken where the pages are silent (each is also a test pin or noted):
   * the shared expert is added with weight 1 and is not part of k.
 
 Pinned: every function here is pinned by a test in tests/test_oracle_pins.py
-against closed forms, brute force or an independent formulation.  Element
-values of a full random layer are "parity unpinned" beyond those pins: the
-pages print no worked numerical example of a layer output.
+against closed forms (one-hot weights reduce the layer to silu(x_a) x_b w at
+output c), identities the pages state (all sub-experts of an expert at equal
+gate equal the monolithic expert; k = E_r equals the dense gate-weighted sum;
+the repeated-row router reproduces the unsplit layer) and brute force (top-k
+against a full sort, the permutation enumerated on tiny inputs).  The pages
+print no worked numerical example of a layer output, so there is no stored
+value from them to compare against.
 """
 from __future__ import annotations
 

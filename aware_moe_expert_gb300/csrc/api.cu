@@ -242,7 +242,7 @@ moe_status do_logits_gemm(const moe_layer_desc* d, const void* x, const void* ro
 }
 
 // bitmap_done (nullable): ask the top-k kernel to write the permutation's
-// bitmap as well (layer forward, T > 256); *bitmap_done says whether it did.
+// bitmap as well (layer forward, T >= kPermuteBitmapMinT); *bitmap_done says whether it did.
 moe_status do_route(const moe_layer_desc* d, const void* x, const void* router_w,
                     const float* logits_in, const int32_t* kpt, float* logits_out,
                     int32_t* topk_idx, float* topk_w, int32_t* status, void* ws,

@@ -100,7 +100,7 @@ cudaError_t launch_paths_merge(const int32_t* n_paths, const int32_t* slot, cons
                                void* act_tgt, float* w_tgt, int32_t* status, cudaStream_t s);
 
 // ---- permute.cu
-// bitmap_ready: the top-k kernel already wrote `bitmap` (T > 256 only).
+// bitmap_ready: the top-k kernel already wrote `bitmap` (T >= kPermuteBitmapMinT only).
 // Also zeroes zero_ptr[0, zero_n) (counters of the kernel that follows).
 cudaError_t launch_permute(const int32_t* topk_idx, const int32_t* k_per_token, int T,
                            int k_max, int E_r, uint32_t* bitmap, int32_t* wprefix,
@@ -108,8 +108,11 @@ cudaError_t launch_permute(const int32_t* topk_idx, const int32_t* k_per_token, 
                            int32_t* inv_row, int32_t* status, cudaStream_t s,
                            bool bitmap_ready = false, int32_t* zero_ptr = nullptr,
                            int zero_n = 0);
-// T above which launch_permute builds the bitmap (below: one CTA, no bitmap)
-constexpr int kPermuteBitmapMinT = 257;
+// T from which launch_permute uses the bitmap kernels (below: one CTA, no bitmap).
+// Measured on the Qwen3-30B-A3B-shaped decode at T = 256: the one-CTA kernel
+// took 7.2 us in the layer, the bitmap path (top-k writes the bitmap, then
+// scan and scatter) ~4 us at T = 1024.
+constexpr int kPermuteBitmapMinT = 129;
 // also zeroes zero_ptr[0, zero_n) (counters for the kernel that follows)
 cudaError_t launch_gather_rows(const void* x, const int32_t* sorted_token,
                                const int32_t* offsets, int E_r, int T, int H, int n_cap,

@@ -186,7 +186,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
 
 // Decode-sized batches in one CTA (1024 threads): bitmap, word prefixes,
 // offsets and scatter all in shared memory (W = ceil(T/32) <= 8 words per
-// unit, T <= 256).  Same result as bitmap_kernel + scan_kernel + scatter_kernel.
+// unit, T < kPermuteBitmapMinT).  Same result as bitmap_kernel + scan_kernel +
+// scatter_kernel.
 __global__ void __launch_bounds__(1024) permute_small_kernel(
     const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ kpt, int T, int k_max,
     int E_r, int W, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
@@ -281,8 +282,8 @@ cudaError_t launch_permute(const int32_t* topk_idx, const int32_t* k_per_token, 
                            int32_t* inv_row, int32_t* status, cudaStream_t s,
                            bool bitmap_ready, int32_t* zero_ptr, int zero_n) {
   const int W = (T + 31) / 32;
-  static_assert(kPermuteBitmapMinT == 8 * 32 + 1, "the one-CTA path takes W <= 8");
-  if (W > 0 && W <= 8) {
+  static_assert(kPermuteBitmapMinT <= 8 * 32 + 1, "the one-CTA path takes W <= 8");
+  if (T > 0 && T < kPermuteBitmapMinT) {
     const int smem = (2 * E_r * W + 256 + 257) * 4;
     static bool attr_done[64] = {false};
     cudaError_t e = set_smem_once(permute_small_kernel, (2 * 256 * 8 + 256 + 257) * 4, attr_done);

@@ -709,7 +709,7 @@ def launches_per_step(wl, T, path=0, fold=False, cg=False):
     """Kernels libmoe enqueues per moe_layer_forward (mirrors the host
     sequencing in csrc/api.cu: router + top-k (one cluster launch on CUDA
     cores, or the tensor-core GEMM and the top-k kernel), permutation (fused
-    into the router launch for <= 8 tokens; above 256 tokens the top-k kernel
+    into the router launch for <= 8 tokens; above 128 tokens the top-k kernel
     also writes its bitmap), [folding], [shared expert], the fused decode FFN
     or gate|up (+ the split-K reduction of the weight-stationary family) and
     down (+ its split reduction), combine)."""
@@ -724,7 +724,7 @@ def launches_per_step(wl, T, path=0, fold=False, cg=False):
         n = 1
     else:
         n = 1 if cluster_router else 2               # logits (+ top-k)
-        if (T + 31) // 32 <= 8:
+        if T <= 128:
             n += 1                                   # permutation in one CTA
         else:                                        # [bitmap,] scan, scatter
             n += 2 if not (cluster_router or fold or cg) else 3

@@ -145,6 +145,7 @@ def test_full_size_routing_and_permutation_bit_exact(name):
 
 @pytest.mark.parametrize("name,T", [("tiny", None), ("qwen_decode", 64), ("qwen_decode", 256),
                                     ("qwen_decode", 300), ("mixtral_decode", None),
+                                    ("qwen_decode", 128), ("qwen_decode", 129),
                                     ("qwen_decode", 1), ("qwen_decode", 8), ("mixtral_decode", 5),
                                     ("tiny", 7), ("tiny_i192", 4), ("tiny", 1000),
                                     ("qwen_decode", 1024), ("qwen_decode", 12),

@@ -47,7 +47,11 @@ def _gpu_permute(desc, idx, k):
                                               # several words (k_max 1, 2, 3)
                                               (8192, 128, 8, 1.1), (2048, 256, 1, 0.0),
                                               (3072, 64, 2, 0.7), (4096, 256, 8, 0.0),
-                                              (2048, 48, 3, 0.0), (1024, 33, 5, 0.0)])
+                                              (2048, 48, 3, 0.0), (1024, 33, 5, 0.0),
+                                              # the one-CTA kernel's last size and the
+                                              # bitmap kernels' first ones
+                                              (128, 256, 16, 0.0), (129, 256, 16, 0.0),
+                                              (200, 128, 8, 1.1), (256, 256, 32, 0.0)])
 def test_permute_bit_exact(T, E_r, k_max, skew):
     idx, k = _random_routing(T, E_r, k_max, seed=T + E_r, skew=skew)
     desc = B.LayerDesc(T=T, H=64, n_experts=E_r, n_sub=1, I_sub=64, k_max=k_max)

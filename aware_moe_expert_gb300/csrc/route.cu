@@ -183,31 +183,38 @@ __device__ __forceinline__ unsigned long long warp_select_topk(const uint32_t (&
 // bias[u / n_sub] when bias is given, and is stored to lout[u] when lout is
 // given.  Lane j < k ends up holding the j-th unit (*out_u) and its gate
 // weight after renormalisation and route_scale (*out_w).  Returns k.
-template <int IPL, int SB = 2>
-__device__ __forceinline__ int warp_topk(const float* __restrict__ P, int S, size_t sstride,
-                                         const float* __restrict__ bias, int n_sub,
-                                         float* __restrict__ lout, int kt, int E_r, int k_max,
-                                         int score, int renorm, float route_scale,
-                                         int32_t* status, int lane, int* out_u, float* out_w) {
-  int k = kt;
-  if (k < 1 || k > k_max) {
-    if (lane == 0) report(status, MOE_ERR_K_RANGE);
-    k = min(max(k, 0), k_max);
-  }
-  k = min(k, E_r);
-  float v[IPL];
-  uint32_t key[IPL];
-  bool bad = false;
+// Softmax statistics of one token's logits held IPL per lane: the maximum and
+// sum of exp(v - max) over the E_r units, reduced across the warp in a fixed
+// order (bit-identical wherever it runs).
+template <int IPL>
+__device__ __forceinline__ void softmax_stats(const float (&v)[IPL], int E_r, int lane, float* mx_out,
+                                              float* sum_out) {
+  float mx = -INFINITY, sum = 0.f;
+#pragma unroll
+  for (int i = 0; i < IPL; ++i)
+    if (lane + 32 * i < E_r) mx = fmaxf(mx, v[i]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+#pragma unroll
+  for (int i = 0; i < IPL; ++i)
+    if (lane + 32 * i < E_r) sum += expf(v[i] - mx);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  *mx_out = mx;
+  *sum_out = sum;
+}
+
+// One token's logits in a lane's IPL registers: the first partial row plus
+// the rest in slice order (SB slices' loads in flight), plus bias[u / n_sub].
+template <int IPL, int SB>
+__device__ __forceinline__ void load_logits(const float* __restrict__ P, int S, size_t sstride,
+                                            const float* __restrict__ bias, int n_sub, int E_r,
+                                            int lane, float (&v)[IPL]) {
 #pragma unroll
   for (int i = 0; i < IPL; ++i) {
     const int u = lane + 32 * i;
-    if (u < E_r) {
-      v[i] = P[u];
-    } else {
-      v[i] = 0.f;
-    }
+    v[i] = u < E_r ? P[u] : 0.f;
   }
-  // add the remaining partial rows in slice order, SB slices' loads in flight
   for (int s0 = 1; s0 < S; s0 += SB) {
     float pv[SB][IPL];
 #pragma unroll
@@ -226,8 +233,34 @@ __device__ __forceinline__ int warp_topk(const float* __restrict__ P, int S, siz
 #pragma unroll
   for (int i = 0; i < IPL; ++i) {
     const int u = lane + 32 * i;
+    if (u < E_r && bias != nullptr) v[i] += bias[u / n_sub];
+  }
+}
+
+// stats (nullable): softmax maximum and sum computed by a helper warp, read
+// after named barrier stats_bar (64 threads: this warp and the helper).
+template <int IPL, int SB = 2>
+__device__ __forceinline__ int warp_topk(const float* __restrict__ P, int S, size_t sstride,
+                                         const float* __restrict__ bias, int n_sub,
+                                         float* __restrict__ lout, int kt, int E_r, int k_max,
+                                         int score, int renorm, float route_scale,
+                                         int32_t* status, int lane, int* out_u, float* out_w,
+                                         const volatile float* stats = nullptr,
+                                         int stats_bar = 0) {
+  int k = kt;
+  if (k < 1 || k > k_max) {
+    if (lane == 0) report(status, MOE_ERR_K_RANGE);
+    k = min(max(k, 0), k_max);
+  }
+  k = min(k, E_r);
+  float v[IPL];
+  uint32_t key[IPL];
+  bool bad = false;
+  load_logits<IPL, SB>(P, S, sstride, bias, n_sub, E_r, lane, v);
+#pragma unroll
+  for (int i = 0; i < IPL; ++i) {
+    const int u = lane + 32 * i;
     if (u < E_r) {
-      if (bias != nullptr) v[i] += bias[u / n_sub];
       if (lout != nullptr) lout[u] = v[i];
       bad |= !isfinite(v[i]);
       key[i] = order_key(v[i]);
@@ -238,20 +271,14 @@ __device__ __forceinline__ int warp_topk(const float* __restrict__ P, int S, siz
   if (__any_sync(0xffffffffu, bad) && lane == 0) report(status, MOE_ERR_NONFINITE);
 
   float mx = -INFINITY, sum = 0.f;
-  if (score == MOE_SCORE_SOFTMAX) {
-#pragma unroll
-    for (int i = 0; i < IPL; ++i)
-      if (lane + 32 * i < E_r) mx = fmaxf(mx, v[i]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-#pragma unroll
-    for (int i = 0; i < IPL; ++i)
-      if (lane + 32 * i < E_r) sum += expf(v[i] - mx);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-  }
+  if (score == MOE_SCORE_SOFTMAX && stats == nullptr) softmax_stats<IPL>(v, E_r, lane, &mx, &sum);
 
   const unsigned long long best = warp_select_topk<IPL>(key, E_r, k, lane);
+  if (score == MOE_SCORE_SOFTMAX && stats != nullptr) {
+    asm volatile("bar.sync %0, 64;" ::"r"(stats_bar) : "memory");
+    mx = stats[0];
+    sum = stats[1];
+  }
   int my_u = -1;
   float my_s = 0.f;
   if (lane < k) {
@@ -332,6 +359,7 @@ __global__ void __launch_bounds__(256) topk_gate_kernel(
 constexpr int kClTok = 8;
 constexpr int kClThreads = 512;
 constexpr int kClWarps = kClThreads / 32;
+static_assert(kClWarps >= 2 * 8, "a selecting warp and a helper warp per token of a cluster block");
 constexpr int kClMaxMt = 2;                      // 16-unit m-tiles per CTA (C >= 8, E_r <= 256)
 constexpr uint32_t kClStageBudget = 208 * 1024;  // staged rows, all chunks in flight
 
@@ -362,7 +390,7 @@ struct ClusterRouteParams {
 };
 
 struct ClusterSmem {
-  uint32_t pitch, rows, stage, red, all, bits, off, wt, bias, total;
+  uint32_t pitch, rows, stage, red, all, bits, off, wt, bias, stat, total;
 };
 
 // Staged rows per buffer: MT * 16 unit rows, then the eight token rows, each
@@ -389,6 +417,8 @@ __host__ __device__ inline ClusterSmem cluster_smem(int E_r, int MT, int kc, int
   b += kClWarps * 4;
   o.bias = b;
   b += 256 * 4;
+  o.stat = b;
+  b += kClTok * 2 * 4;
   o.total = b;
   return o;
 }
@@ -443,6 +473,7 @@ __global__ void __launch_bounds__(kClThreads, 1) route_cluster_kernel(const Clus
   int32_t* s_off = reinterpret_cast<int32_t*>(csm + L.off);
   int32_t* s_wt = reinterpret_cast<int32_t*>(csm + L.wt);
   float* s_bias = reinterpret_cast<float*>(csm + L.bias);
+  volatile float* s_stat = reinterpret_cast<volatile float*>(csm + L.stat);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_ctarank();
   const bool fused = p.counts != nullptr;
@@ -574,6 +605,22 @@ __global__ void __launch_bounds__(kClThreads, 1) route_cluster_kernel(const Clus
 
   if (rank == 0) {
     int my_u = -1, k = 0;
+    // Softmax: warp kClTok + j computes token j's maximum and exp-sum (the
+    // code warp_topk would run, so the same bits) while warp j selects, and
+    // hands them over at named barrier 1 + j.
+    const bool helped = p.score == MOE_SCORE_SOFTMAX;
+    if (helped && warp >= kClTok && warp < kClTok + nt) {
+      const int j = warp - kClTok;
+      float v[IPL], mx, sum;
+      load_logits<IPL, 2>(s_all + j * E_r, 1, 0, p.bias != nullptr ? s_bias : nullptr, 1, E_r,
+                          lane, v);
+      softmax_stats<IPL>(v, E_r, lane, &mx, &sum);
+      if (lane == 0) {
+        s_stat[2 * j] = mx;
+        s_stat[2 * j + 1] = sum;
+      }
+      asm volatile("bar.sync %0, 64;" ::"r"(1 + j) : "memory");
+    }
     if (warp < nt) {
       const int t = t0 + warp;
       const size_t row = static_cast<size_t>(t) * E_r;
@@ -581,7 +628,8 @@ __global__ void __launch_bounds__(kClThreads, 1) route_cluster_kernel(const Clus
       k = warp_topk<IPL>(s_all + warp * E_r, 1, 0, p.bias != nullptr ? s_bias : nullptr, 1,
                          p.logits_out != nullptr ? p.logits_out + row : nullptr,
                          kt_pre, E_r, p.k_max, p.score,
-                         p.renorm, p.route_scale, p.status, lane, &my_u, &w);
+                         p.renorm, p.route_scale, p.status, lane, &my_u, &w,
+                         helped ? s_stat + 2 * warp : nullptr, 1 + warp);
       if (lane < p.k_max) {
         const size_t o = static_cast<size_t>(t) * p.k_max + lane;
         p.topk_idx[o] = my_u;

@@ -11,11 +11,10 @@
 //
 // The scratch is one array per device that loads this library, kept until
 // the process exits.  Its device address is looked up once per device, on
-// the first call made with that device current; make that first call before
-// any stream capture begins.  Every call shares the array, so two calls whose
-// kernels overlap on the GPU (different streams, no ordering between them)
-// race on it and must not be issued.  The array needs no clearing: each call
-// writes every scratch word it later reads.
+// the first call made with that device current.  Every call shares the
+// array, so two calls whose kernels overlap on the GPU (different streams,
+// no ordering between them) race on it and must not be issued.  The array
+// needs no clearing: each call writes every scratch word it later reads.
 #include <cuda_runtime.h>
 
 #include <mutex>

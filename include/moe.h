@@ -201,7 +201,7 @@ moe_status moe_layer_forward_host(const moe_layer_desc* desc, const void* x_host
  *   library keeps until exit; 2 * E_r * ceil(T/32) * 4 bytes must fit, else
  *   MOE_ERR_UNSUPPORTED_SHAPE (e.g. E_r = 256 allows T <= 16384).
  *   The first call on a device looks up the array's device address (a
- *   runtime call); make that first call before any stream capture.
+ *   runtime call, made once per device).
  *   All calls share the array: calls whose kernels may overlap on the GPU
  *   race and must not be issued.  Nothing in it needs clearing between calls.
  *   Allocates nothing (no cudaMalloc, cudaFree or allocating library call). */

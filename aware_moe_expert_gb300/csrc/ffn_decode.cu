@@ -763,8 +763,9 @@ cudaError_t launch_decode_ffn(const DecodeFfnArgs& a, cudaStream_t s) {
   // stages).  Same-box A/B, Qwen3-30B-A3B-shaped decode (I_sub 384): T = 64
   // 197.4 -> 186.8 us, T = 256 222.3 -> 212.0, T = 1024 238.2 -> 231.7; with
   // 16-token chunks (T <= 16) the halved item count costs more than it saves
-  // (T = 1 28.6 -> 32.4 us), so those keep one block per item.  A template
-  // parameter: the other variants keep their code and registers.
+  // (T = 1 28.6 -> 32.4 us, T = 8 74.2 -> 76.1), so those keep one block per
+  // item.  A template parameter: the other variants keep their code and
+  // registers.
   const bool dpair = a.I <= 1024 && a.H % (2 * kM) == 0;
   if (dpair) p.dn_tiles = a.H / (2 * kM);
   auto go = [&](auto kern, int threads) -> cudaError_t {

@@ -445,7 +445,6 @@ moe_status do_down(const moe_layer_desc* d, const void* act, const int32_t* offs
 // Both FFN projections.  Decode-shaped batches with H and I_sub multiples of
 // 128 run the fused kernel (gate|up and down overlapped in one launch);
 // otherwise gate|up then down.
-
 // gather_in_ffn: the decode FFN reads its token rows from x itself and its
 // counters are already zero (the router or the permutation zeroed them);
 // otherwise a row-gather launch writes x_perm and zeroes them.

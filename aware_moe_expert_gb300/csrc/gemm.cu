@@ -569,8 +569,10 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // Encoded tensor maps, keyed by everything that goes into them, so that a
 // call on tensors seen before skips the encoding (host time of the small
-// decode calls); host memory only.  A direct-mapped table: a slot whose key
-// differs is re-encoded and overwritten.
+// decode calls); host memory only.  64 sets of 4 ways: a key goes to the set
+// its hashed fields pick (every field mixed into the set index, so the 16-
+// and 64-row boxes of one tensor do not evict each other), and a new key
+// replaces the set's ways in turn.
 namespace {
 struct TmapKey {
   const void* base;
@@ -581,40 +583,57 @@ struct TmapKey {
            elem == o.elem;
   }
 };
-constexpr int kTmapSlots = 256;
+constexpr int kTmapSets = 64, kTmapWays = 4;
 struct TmapCache {
   std::mutex mu;
-  TmapKey key[kTmapSlots] = {};
-  CUtensorMap map[kTmapSlots];
-  bool used[kTmapSlots] = {};
+  TmapKey key[kTmapSets][kTmapWays] = {};
+  CUtensorMap map[kTmapSets][kTmapWays];
+  bool used[kTmapSets][kTmapWays] = {};
+  int next[kTmapSets] = {};
 };
 TmapCache& tmap_cache() {
   static TmapCache c;
   return c;
 }
-int tmap_slot(const TmapKey& k) {
-  uint64_t h = reinterpret_cast<uintptr_t>(k.base) >> 4;
-  h ^= static_cast<uint64_t>(k.rows) * 0x9E3779B97F4A7C15ull;
-  h ^= (static_cast<uint64_t>(k.cols) << 20) ^ (static_cast<uint64_t>(k.box_rows) << 8) ^
-       static_cast<uint64_t>(k.elem);
-  h ^= h >> 29;
-  return static_cast<int>(h % kTmapSlots);
+// 64-bit finaliser (xor-shift and odd-constant multiplies) of a running hash
+uint64_t tmap_mix(uint64_t h) {
+  h ^= h >> 33;
+  h *= 0xff51afd7ed558ccdull;
+  h ^= h >> 33;
+  h *= 0xc4ceb9fe1a85ec53ull;
+  h ^= h >> 33;
+  return h;
+}
+int tmap_set(const TmapKey& k) {
+  uint64_t h = tmap_mix(static_cast<uint64_t>(reinterpret_cast<uintptr_t>(k.base)));
+  h = tmap_mix(h ^ static_cast<uint64_t>(k.rows));
+  h = tmap_mix(h ^ (static_cast<uint64_t>(static_cast<uint32_t>(k.cols)) << 32 ^
+                    static_cast<uint64_t>(static_cast<uint32_t>(k.box_rows)) << 8 ^
+                    static_cast<uint64_t>(static_cast<uint32_t>(k.elem))));
+  return static_cast<int>(h % kTmapSets);
 }
 bool tmap_lookup(const TmapKey& k, CUtensorMap* m) {
   TmapCache& c = tmap_cache();
-  const int i = tmap_slot(k);
+  const int i = tmap_set(k);
   std::lock_guard<std::mutex> g(c.mu);
-  if (!c.used[i] || !(c.key[i] == k)) return false;
-  *m = c.map[i];
-  return true;
+  for (int w = 0; w < kTmapWays; ++w)
+    if (c.used[i][w] && c.key[i][w] == k) {
+      *m = c.map[i][w];
+      return true;
+    }
+  return false;
 }
 void tmap_store(const TmapKey& k, const CUtensorMap& m) {
   TmapCache& c = tmap_cache();
-  const int i = tmap_slot(k);
+  const int i = tmap_set(k);
   std::lock_guard<std::mutex> g(c.mu);
-  c.key[i] = k;
-  c.map[i] = m;
-  c.used[i] = true;
+  for (int w = 0; w < kTmapWays; ++w)
+    if (c.used[i][w] && c.key[i][w] == k) return;
+  const int w = c.next[i];
+  c.next[i] = (w + 1) % kTmapWays;
+  c.key[i][w] = k;
+  c.map[i][w] = m;
+  c.used[i][w] = true;
 }
 }  // namespace
 

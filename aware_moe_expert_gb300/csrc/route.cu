@@ -298,40 +298,61 @@ __device__ __forceinline__ int warp_topk(const float* __restrict__ P, int S, siz
 // [T, E_r] one after another (S = 1: finished logits).  kpt == nullptr: every
 // token keeps k_max units.
 //
+// HELP (softmax scores): warps 8-15 compute the softmax maximum and exp-sum
+// of token (warp - 8) with the code warp_topk would run (same bits) while
+// warp (warp - 8) selects; they meet at named barrier 1 + (warp - 8).
+//
 // bitmap != nullptr: the CTA also writes its byte of the permutation's unit
 // membership bitmap (bit j of byte b of row u = token 8 b + j selected u;
 // rows of row_bytes = 4 * ceil(T / 32) bytes, the uint32 words the scan
 // reads), so the permutation needs no pass of its own over topk_idx.  The
 // last CTA also zeroes the row bytes past the last token group.
-template <int IPL, int SB>
-__global__ void __launch_bounds__(256) topk_gate_kernel(
+template <int IPL, int SB, bool HELP = false>
+__global__ void __launch_bounds__(HELP ? 512 : 256) topk_gate_kernel(
     const float* __restrict__ P, int S, const float* __restrict__ bias, int n_sub,
     float* __restrict__ logits_out, const int32_t* __restrict__ kpt, int T, int E_r,
     int k_max, int score, int renorm, float route_scale, int32_t* __restrict__ topk_idx,
     float* __restrict__ topk_w, int32_t* status, uint8_t* __restrict__ bitmap,
     int row_bytes) {
   __shared__ uint32_t s_bits[256];
+  __shared__ float s_stat_raw[16];
+  volatile float* s_stat = s_stat_raw;
   pdl_wait_and_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + warp;
+  const int tw = warp & 7;
+  const int t = blockIdx.x * 8 + tw;
+  const bool helped = HELP && score == MOE_SCORE_SOFTMAX;
   if (bitmap != nullptr) {
     for (int v = threadIdx.x; v < E_r; v += blockDim.x) s_bits[v] = 0u;
     __syncthreads();
   }
-  if (t < T) {
+  if (HELP && warp >= 8) {
+    if (helped && t < T) {
+      float v[IPL], mx, sum;
+      load_logits<IPL, SB>(P + static_cast<size_t>(t) * E_r, S, static_cast<size_t>(T) * E_r,
+                           bias, n_sub, E_r, lane, v);
+      softmax_stats<IPL>(v, E_r, lane, &mx, &sum);
+      if (lane == 0) {
+        s_stat[2 * tw] = mx;
+        s_stat[2 * tw + 1] = sum;
+      }
+      asm volatile("bar.sync %0, 64;" ::"r"(1 + tw) : "memory");
+    }
+  } else if (t < T) {
     int u;
     float w;
     const size_t row = static_cast<size_t>(t) * E_r;
     warp_topk<IPL, SB>(P + row, S, static_cast<size_t>(T) * E_r, bias, n_sub,
-                   logits_out != nullptr ? logits_out + row : nullptr,
-                   kpt != nullptr ? kpt[t] : k_max, E_r, k_max, score,
-                   renorm, route_scale, status, lane, &u, &w);
+                       logits_out != nullptr ? logits_out + row : nullptr,
+                       kpt != nullptr ? kpt[t] : k_max, E_r, k_max, score,
+                       renorm, route_scale, status, lane, &u, &w,
+                       helped ? s_stat + 2 * tw : nullptr, 1 + tw);
     if (lane < k_max) {
       const size_t o = static_cast<size_t>(t) * k_max + lane;
       topk_idx[o] = u;
       topk_w[o] = w;
     }
-    if (bitmap != nullptr && u >= 0) atomicOr(&s_bits[u], 1u << warp);
+    if (bitmap != nullptr && u >= 0) atomicOr(&s_bits[u], 1u << tw);
   }
   if (bitmap != nullptr) {
     __syncthreads();
@@ -847,6 +868,21 @@ cudaError_t launch_route_cluster(const void* x, const void* router_w, const floa
   return run_route_cluster<8>(p, s);
 }
 
+namespace {
+// Multiprocessors of the current device (0 when it cannot be read).
+int topk_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+      cached[dev] = n;
+  }
+  return cached[dev];
+}
+}  // namespace
+
 cudaError_t launch_topk_gate(const float* partial, int S, const float* bias, int n_sub,
                              float* logits_out, const int32_t* k_per_token, int T, int E_r,
                              int k_max, int score, int renorm, float route_scale,
@@ -858,10 +894,14 @@ cudaError_t launch_topk_gate(const float* partial, int S, const float* bias, int
   uint8_t* bm = reinterpret_cast<uint8_t*>(bitmap);
   const int row_bytes = 4 * ((T + 31) / 32);
   // many partial slices (split-K routers of small batches): every slice's
-  // loads in one round trip; otherwise two at a time (fewer registers)
+  // loads in one round trip; otherwise two at a time (fewer registers).  With
+  // softmax scores and at most one CTA per SM, a second warp per token
+  // computes the softmax statistics while the first selects.
+  const bool help = S > 2 && score == MOE_SCORE_SOFTMAX && grid <= topk_sm_count();
 #define MOE_TOPK_LAUNCH(IPL)                                                                 \
-  launch_pdl(S > 2 ? topk_gate_kernel<IPL, 8> : topk_gate_kernel<IPL, 2>, dim3(grid),        \
-             dim3(256), 0, s, partial, S, bias, n_sub,                                        \
+  launch_pdl(help ? topk_gate_kernel<IPL, 8, true>                                           \
+                  : (S > 2 ? topk_gate_kernel<IPL, 8> : topk_gate_kernel<IPL, 2>),            \
+             dim3(grid), dim3(help ? 512 : 256), 0, s, partial, S, bias, n_sub,               \
              logits_out, k_per_token, T, E_r, k_max, score, renorm, route_scale, topk_idx,    \
              topk_w, status, bm, row_bytes)
   if (E_r <= 32) return MOE_TOPK_LAUNCH(1);

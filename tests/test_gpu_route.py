@@ -110,3 +110,38 @@ def test_router_logits_match_fp64(T, H, n_experts, n_sub):
     mag = np.abs(X) @ np.abs(R).T
     err = np.abs(L.cpu().numpy().astype(np.float64) - ref)
     assert (err <= H * 2.0 ** -24 * mag + 1e-6).all(), f"max err {err.max():.3e}"
+
+
+# From x through the tensor-core router with K split more than twice: softmax
+# scores take the top-k kernel whose helper warps compute the softmax
+# statistics while the selecting warps run, as long as its grid (T / 8 CTAs)
+# fits one CTA per SM; (1216, 128) is the last such T on a 152-SM GB300 and
+# (1224, 128) the first without.  Selection on the GPU's own fp32 logits is
+# bit-exact, the gates within the fp32 bound.
+@pytest.mark.parametrize("T,n_experts,n_sub,k_max", [(200, 64, 1, 8), (1024, 128, 2, 16),
+                                                     (1216, 128, 1, 8), (1224, 128, 1, 8)])
+@pytest.mark.parametrize("renorm,scale", [(False, 1.0), (True, 2.5)])
+def test_split_k_router_top_k_on_its_own_logits(T, n_experts, n_sub, k_max, renorm, scale):
+    H = 2048
+    E_r = n_experts * n_sub
+    g = torch.Generator(device=DEV).manual_seed(T + E_r)
+    x = torch.randn(T, H, generator=g, device=DEV).to(torch.bfloat16)
+    rw = (torch.randn(E_r, H, generator=g, device=DEV) / H ** 0.5).to(torch.bfloat16)
+    bias = torch.randn(n_experts, generator=g, device=DEV) * 0.1
+    k = torch.randint(1, k_max + 1, (T,), generator=torch.Generator().manual_seed(T),
+                      dtype=torch.int32).to(DEV)
+    desc = B.LayerDesc(T=T, H=H, n_experts=n_experts, n_sub=n_sub, I_sub=64, k_max=k_max,
+                       score="softmax", renorm=renorm, route_scale=scale, expert_bias=bias)
+    L = torch.empty(T, E_r, dtype=torch.float32, device=DEV)
+    idx = torch.full((T, k_max), -7, dtype=torch.int32, device=DEV)
+    w = torch.full((T, k_max), -7.0, dtype=torch.float32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ws = torch.empty(B.moe_workspace_size(desc), dtype=torch.uint8, device=DEV)
+    B.check(B.moe_route(desc, x, rw, None, k, L, idx, w, st, ws), "moe_route")
+    assert B.moe_get_device_status(st) == 0
+    Ln, kn = L.cpu().numpy(), k.cpu().numpy()
+    want_idx, flags = O.select_topk(Ln, kn, k_max)
+    assert flags == 0
+    np.testing.assert_array_equal(idx.cpu().numpy(), want_idx)
+    want_w = O.gate_weights(Ln, want_idx, kn, "softmax", renorm, scale)
+    np.testing.assert_allclose(w.cpu().numpy(), want_w, rtol=W_RTOL, atol=1e-30)
